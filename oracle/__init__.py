@@ -1,0 +1,144 @@
+"""fp64 CPU oracle for the Kimi Delta Attention core -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and its
+Python binding) never imports, links or calls it, and it never imports them: the
+two share nothing but the seeded input arrays.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, fp64, one thread per group of
+(sequence, head) units).  This module compiles it with gcc on first use and wraps
+it with ctypes.  Page citations for every formula are in the C file's header:
+the recurrence follows the nnterp encyclopedia page "Kimi-Linear" (sections 02,
+03 and 04), the gated norm the Kimi-K3 atlas page "gate-project" (sections
+"Parameters" and "Code").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB = os.path.join(_HERE, "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DEFAULT_L2_EPS = 1e-6
+
+
+def build(force: bool = False) -> str:
+    """Compile kda_oracle.c into libkda_oracle.so (plain gcc, no GPU)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.kda_oracle_recurrent.argtypes = [
+                P, P, P, P, P, P, P, P, P, P,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+            ]
+            lib.kda_oracle_recurrent.restype = ctypes.c_int
+            lib.kda_oracle_gated_rmsnorm.argtypes = [
+                P, P, P, ctypes.c_double, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+            ]
+            lib.kda_oracle_gated_rmsnorm.restype = ctypes.c_int
+            lib.kda_oracle_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def recurrent(q, k, v, g, beta, initial_state=None, *, scale=None, use_qk_l2norm=True,
+              l2_eps=DEFAULT_L2_EPS, cu_seqlens=None, return_states=False, n_threads=None):
+    """Token-by-token fp64 recurrence.
+
+    Dense form: q, k, g [B,T,H,K]; v [B,T,H,V]; beta [B,T,H]; initial_state
+    [B,H,K,V] or None.  Varlen form (``cu_seqlens`` given, int, n_seqs+1 entries):
+    the leading dimension is 1 (or absent) and initial_state is [n_seqs,H,K,V].
+    Returns ``(o [.., T, H, V] float64, final_state [N,H,K,V] float64[, states])``.
+    """
+    q, k, v, g, beta = _f32(q), _f32(k), _f32(v), _f32(g), _f32(beta)
+    if q.ndim == 3:  # [T,H,K] packed varlen without batch dim
+        q, k, v, g, beta = q[None], k[None], v[None], g[None], beta[None]
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("shape mismatch between q, k, v, g, beta")
+    if scale is None:
+        scale = 1.0 / np.sqrt(K)
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+        if B != 1:
+            raise ValueError("varlen needs batch 1")
+        N = cu.shape[0] - 1
+        if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+            raise ValueError("cu_seqlens must start at 0, end at T and not decrease")
+    else:
+        cu = None
+        N = B
+    s0 = None if initial_state is None else _f64(initial_state)
+    if s0 is not None and s0.shape != (N, H, K, V):
+        raise ValueError(f"initial_state must be {(N, H, K, V)}")
+    o = np.zeros((B, T, H, V), dtype=np.float64)
+    sf = np.zeros((N, H, K, V), dtype=np.float64)
+    states = np.zeros((B, T, H, K, V), dtype=np.float64) if return_states else None
+    lib = _load()
+    rc = lib.kda_oracle_recurrent(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0), _ptr(o), _ptr(sf), _ptr(states),
+        _ptr(cu), N if cu is not None else 0, B, T, H, K, V, float(scale), int(bool(use_qk_l2norm)),
+        float(l2_eps), int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_recurrent failed with {rc}")
+    if return_states:
+        return o, sf, states
+    return o, sf
+
+
+def gated_rmsnorm(o, gate, w, eps=1e-5):
+    """y [.., H*V] = o / sqrt(mean_v(o^2)+eps) * w * sigmoid(gate), per (token, head)."""
+    o = _f64(o)
+    gate = _f32(gate)
+    w = _f32(w)
+    H, V = o.shape[-2], o.shape[-1]
+    if gate.shape != o.shape or w.shape != (V,):
+        raise ValueError("gate must match o and w must be [V]")
+    rows = int(np.prod(o.shape[:-2]))
+    y = np.zeros(o.shape[:-2] + (H * V,), dtype=np.float64)
+    rc = _load().kda_oracle_gated_rmsnorm(_ptr(o), _ptr(gate), _ptr(w), float(eps), _ptr(y), rows, H, V)
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_gated_rmsnorm failed with {rc}")
+    return y
+
+
+def version() -> int:
+    return int(_load().kda_oracle_version())

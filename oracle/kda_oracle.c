@@ -1,0 +1,306 @@
+/*
+ * kda_oracle.c -- plain, slow, fp64 CPU oracle for the Kimi Delta Attention core.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the test-suite, the smoke check and the CPU-baseline leg of the
+ * benchmark use it.  It shares no code, header, table or helper with the CUDA
+ * library; its only common ground with the GPU path is the seeded input data.
+ *
+ * What it computes (per independent (sequence, head) unit, token by token):
+ *
+ *   q^ = q / sqrt(sum q^2 + l2_eps),  k^ = k / sqrt(sum k^2 + l2_eps)   (optional)
+ *   S  <- Diag(exp g_t) S                      decay each key channel first
+ *   D  =  beta_t (v_t - S^T k^)                delta-rule write residual
+ *   S  <- S + k^ D^T                           rank-one write
+ *   o_t = scale * S^T q^                       read-out after the write
+ *
+ * Sources (page title, section):
+ *  - nnterp encyclopedia "Kimi-Linear", section 03 "Kimi Delta Attention decays
+ *    each key channel": KDA is a gated DeltaNet whose log decay g is per key
+ *    channel, float32 and non-positive; beta is the sigmoid of b_proj; queries
+ *    and keys are L2-normalised by the kernel and queries scaled by
+ *    1/sqrt(key_dim); the state is [batch, heads, key_dim, value_dim].
+ *  - same page, section 04 "From the family module": the state decays channel by
+ *    channel before each delta-rule update; the kernels take
+ *    (query, key, value, g=, beta=, initial_state=) and return
+ *    (core_attn_out, last_recurrent_state); use_qk_l2norm_in_kernel.
+ *  - same page, section 02 "support()" value table: layouts
+ *    attention_queries/keys [batch seq heads key_dim], attention_values
+ *    [batch seq heads value_dim], decays [batch seq heads key_dim],
+ *    betas [batch seq heads], state_input / state_output
+ *    [batch heads key_dim value_dim], states [batch seq heads key_dim value_dim].
+ *  - Kimi-K3 atlas page "dense KDA layers / attention / gate-project (decode,
+ *    P = 1000)", sections "Parameters" and "Code": the head outputs pass a
+ *    gated RMSNorm over each head (head_dim = 128 weights shared by all heads,
+ *    eps = rms_norm_eps, activation 'sigmoid') before the output projection.
+ *
+ * Readings where the pages are silent (also listed in the design notes):
+ *  - the L2 norm puts its epsilon inside the square root (l2_eps, 1e-6 by default);
+ *  - the gated norm is y = o / sqrt(mean_v(o^2) + eps) * w * sigmoid(gate);
+ *  - the gate multiplies after the weight; the mean runs over value_dim of one head.
+ *
+ * Parity status: every function here is pinned by the CPU tests (closed forms,
+ * brute-force transition products, split-halves, column independence,
+ * orthonormal-key erase, norm special cases and a library RMSNorm).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KDA_ORACLE_VERSION 1
+
+int kda_oracle_version(void) { return KDA_ORACLE_VERSION; }
+
+/* ------------------------------------------------------------------------- */
+/* Recurrence                                                                 */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const float *q, *k, *v, *g, *beta;   /* token-major inputs, see kda_oracle_recurrent */
+    const double *initial_state;          /* [N,H,K,V] or NULL (zero state) */
+    double *o;                            /* [tokens,H,V] */
+    double *final_state;                  /* [N,H,K,V] or NULL */
+    double *states;                       /* [tokens,H,K,V] or NULL */
+    const int64_t *starts;                /* per-sequence first token row, N entries */
+    const int64_t *lens;                  /* per-sequence token count, N entries */
+    int64_t n_units;                      /* N * H */
+    int H, K, V;
+    double scale, l2_eps;
+    int use_qk_l2norm;
+    int n_threads, tid;
+} rec_job;
+
+/* One (sequence, head) unit, token by token, in fp64. */
+static void rec_unit(const rec_job *J, int64_t unit, double *S, double *qh, double *kh,
+                     double *u, double *delta) {
+    const int H = J->H, K = J->K, V = J->V;
+    const int64_t n = unit / H;
+    const int h = (int)(unit % H);
+    const int64_t row0 = J->starts[n], len = J->lens[n];
+
+    if (J->initial_state) {
+        const double *s0 = J->initial_state + ((size_t)n * H + h) * (size_t)K * V;
+        memcpy(S, s0, sizeof(double) * (size_t)K * V);
+    } else {
+        memset(S, 0, sizeof(double) * (size_t)K * V);
+    }
+
+    for (int64_t t = 0; t < len; ++t) {
+        const int64_t row = row0 + t;
+        const float *qt = J->q + ((size_t)row * H + h) * K;
+        const float *kt = J->k + ((size_t)row * H + h) * K;
+        const float *vt = J->v + ((size_t)row * H + h) * V;
+        const float *gt = J->g + ((size_t)row * H + h) * K;
+        const double bt = (double)J->beta[(size_t)row * H + h];
+
+        /* L2 normalisation of query and key over key_dim (optional). */
+        double sq = 0.0, sk = 0.0;
+        for (int i = 0; i < K; ++i) {
+            sq += (double)qt[i] * (double)qt[i];
+            sk += (double)kt[i] * (double)kt[i];
+        }
+        const double rq = J->use_qk_l2norm ? 1.0 / sqrt(sq + J->l2_eps) : 1.0;
+        const double rk = J->use_qk_l2norm ? 1.0 / sqrt(sk + J->l2_eps) : 1.0;
+        for (int i = 0; i < K; ++i) {
+            qh[i] = (double)qt[i] * rq;
+            kh[i] = (double)kt[i] * rk;
+        }
+
+        /* Decay each key channel (row i of S) by exp(g_t[i]) before the update. */
+        for (int i = 0; i < K; ++i) {
+            const double a = exp((double)gt[i]);
+            double *Si = S + (size_t)i * V;
+            for (int j = 0; j < V; ++j) Si[j] *= a;
+        }
+
+        /* u = S^T k^ ; delta = beta (v - u). */
+        for (int j = 0; j < V; ++j) u[j] = 0.0;
+        for (int i = 0; i < K; ++i) {
+            const double ki = kh[i];
+            const double *Si = S + (size_t)i * V;
+            for (int j = 0; j < V; ++j) u[j] += Si[j] * ki;
+        }
+        for (int j = 0; j < V; ++j) delta[j] = bt * ((double)vt[j] - u[j]);
+
+        /* S <- S + k^ delta^T. */
+        for (int i = 0; i < K; ++i) {
+            const double ki = kh[i];
+            double *Si = S + (size_t)i * V;
+            for (int j = 0; j < V; ++j) Si[j] += ki * delta[j];
+        }
+
+        /* o_t = scale * S^T q^. */
+        double *ot = J->o + ((size_t)row * H + h) * V;
+        for (int j = 0; j < V; ++j) u[j] = 0.0;
+        for (int i = 0; i < K; ++i) {
+            const double qi = qh[i];
+            const double *Si = S + (size_t)i * V;
+            for (int j = 0; j < V; ++j) u[j] += Si[j] * qi;
+        }
+        for (int j = 0; j < V; ++j) ot[j] = J->scale * u[j];
+
+        if (J->states) {
+            double *st = J->states + ((size_t)row * H + h) * (size_t)K * V;
+            memcpy(st, S, sizeof(double) * (size_t)K * V);
+        }
+    }
+
+    if (J->final_state) {
+        double *sf = J->final_state + ((size_t)n * H + h) * (size_t)K * V;
+        memcpy(sf, S, sizeof(double) * (size_t)K * V);
+    }
+}
+
+static void *rec_worker(void *arg) {
+    const rec_job *J = (const rec_job *)arg;
+    const int K = J->K, V = J->V;
+    double *S = (double *)malloc(sizeof(double) * (size_t)K * V);
+    double *buf = (double *)malloc(sizeof(double) * (size_t)(2 * K + 2 * V));
+    if (!S || !buf) {
+        free(S);
+        free(buf);
+        return (void *)1;
+    }
+    for (int64_t unit = J->tid; unit < J->n_units; unit += J->n_threads)
+        rec_unit(J, unit, S, buf, buf + K, buf + 2 * K, buf + 2 * K + V);
+    free(S);
+    free(buf);
+    return NULL;
+}
+
+/*
+ * kda_oracle_recurrent -- run the recurrence over every (sequence, head) unit.
+ *
+ * Host arrays, all row-major and contiguous:
+ *   q, k   [rows, H, K] float (bf16 values widened exactly to float by the caller)
+ *   v      [rows, H, V] float
+ *   g      [rows, H, K] float, the per-channel log decay (non-positive)
+ *   beta   [rows, H]    float
+ *   initial_state [N, H, K, V] double or NULL for a zero state
+ *   o      [rows, H, V] double (written)
+ *   final_state [N, H, K, V] double or NULL
+ *   states [rows, H, K, V] double or NULL: the state after every token
+ * Sequences: if cu_seqlens is NULL there are N = B sequences of T tokens each and
+ * rows = B*T; otherwise N = n_seqs, sequence n covers rows
+ * [cu_seqlens[n], cu_seqlens[n+1]) and rows = cu_seqlens[n_seqs].
+ * Returns 0 on success, -1 on a bad argument, -2 on an allocation failure.
+ */
+int kda_oracle_recurrent(const float *q, const float *k, const float *v, const float *g,
+                         const float *beta, const double *initial_state, double *o,
+                         double *final_state, double *states, const int64_t *cu_seqlens,
+                         int n_seqs, int B, int T, int H, int K, int V, double scale,
+                         int use_qk_l2norm, double l2_eps, int n_threads) {
+    if (!q || !k || !v || !g || !beta || !o) return -1;
+    if (H <= 0 || K <= 0 || V <= 0) return -1;
+    int64_t N;
+    int64_t *starts, *lens;
+    if (cu_seqlens) {
+        if (n_seqs <= 0) return -1;
+        N = n_seqs;
+        starts = (int64_t *)malloc(sizeof(int64_t) * (size_t)N);
+        lens = (int64_t *)malloc(sizeof(int64_t) * (size_t)N);
+        if (!starts || !lens) {
+            free(starts);
+            free(lens);
+            return -2;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            if (cu_seqlens[n + 1] < cu_seqlens[n] || cu_seqlens[n] < 0) {
+                free(starts);
+                free(lens);
+                return -1;
+            }
+            starts[n] = cu_seqlens[n];
+            lens[n] = cu_seqlens[n + 1] - cu_seqlens[n];
+        }
+    } else {
+        if (B <= 0 || T < 0) return -1;
+        N = B;
+        starts = (int64_t *)malloc(sizeof(int64_t) * (size_t)N);
+        lens = (int64_t *)malloc(sizeof(int64_t) * (size_t)N);
+        if (!starts || !lens) {
+            free(starts);
+            free(lens);
+            return -2;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            starts[n] = n * (int64_t)T;
+            lens[n] = T;
+        }
+    }
+    if (n_threads < 1) n_threads = 1;
+    const int64_t n_units = N * H;
+    if (n_threads > n_units) n_threads = (int)n_units;
+
+    rec_job *jobs = (rec_job *)malloc(sizeof(rec_job) * (size_t)n_threads);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        free(starts);
+        free(lens);
+        return -2;
+    }
+    int rc = 0;
+    int started = 0;
+    for (int i = 0; i < n_threads; ++i) {
+        rec_job J = {q, k, v, g, beta, initial_state, o, final_state, states, starts, lens,
+                     n_units, H, K, V, scale, l2_eps, use_qk_l2norm, n_threads, i};
+        jobs[i] = J;
+    }
+    for (int i = 1; i < n_threads; ++i) {
+        if (pthread_create(&th[i], NULL, rec_worker, &jobs[i]) != 0) {
+            rc = -2;
+            break;
+        }
+        started = i;
+    }
+    if (rec_worker(&jobs[0]) != NULL) rc = -2;
+    for (int i = 1; i <= started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -2;
+    }
+    free(jobs);
+    free(th);
+    free(starts);
+    free(lens);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Sigmoid-gated RMSNorm over each head                                       */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * kda_oracle_gated_rmsnorm -- y = o / sqrt(mean_v(o^2) + eps) * w * sigmoid(gate).
+ *
+ * Kimi-K3 atlas "gate-project (decode, P = 1000)", sections "Parameters" (the
+ * gated RMSNorm holds 128 weights, one vector shared by all 96 heads) and "Code"
+ * (o_norm(o, g) on [.., heads, head_dim] with activation 'sigmoid', then the
+ * heads are flattened to [.., heads * head_dim]).
+ *
+ *   o    [rows, H, V] double      gate [rows, H, V] float (bf16 values widened)
+ *   w    [V] float                y    [rows, H*V] double (written)
+ */
+int kda_oracle_gated_rmsnorm(const double *o, const float *gate, const float *w, double eps,
+                             double *y, int64_t rows, int H, int V) {
+    if (!o || !gate || !w || !y || rows < 0 || H <= 0 || V <= 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const double *x = o + ((size_t)r * H + h) * V;
+            const float *gt = gate + ((size_t)r * H + h) * V;
+            double *yt = y + ((size_t)r * H + h) * V;
+            double ss = 0.0;
+            for (int j = 0; j < V; ++j) ss += x[j] * x[j];
+            const double inv = 1.0 / sqrt(ss / (double)V + eps);
+            for (int j = 0; j < V; ++j) {
+                const double sig = 1.0 / (1.0 + exp(-(double)gt[j]));
+                yt[j] = x[j] * inv * (double)w[j] * sig;
+            }
+        }
+    }
+    return 0;
+}
