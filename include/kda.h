@@ -1,0 +1,187 @@
+/*
+ * kda.h -- C ABI of libkda, the GB300 (sm_103a) Kimi Delta Attention core.
+ *
+ * The library computes the gated delta rule with a per-key-channel decay, the
+ * mixer core of the Kimi-Linear / Kimi-K3 KDA layers, for every independent
+ * (sequence, head) unit:
+ *
+ *     q^ = q / sqrt(|q|^2 + 1e-6),  k^ = k / sqrt(|k|^2 + 1e-6)     (if use_qk_l2norm)
+ *     S_t = (I - beta_t k^_t k^_t^T) Diag(exp g_t) S_{t-1} + beta_t k^_t v_t^T
+ *     o_t = scale * S_t^T q^_t
+ *
+ * optionally followed by the head-wise sigmoid-gated RMSNorm
+ *
+ *     y = o / sqrt(mean_v(o^2) + eps) * w * sigmoid(gate)
+ *
+ * Sources (page title, section):
+ *   nnterp encyclopedia "Kimi-Linear": section 02 "support()" (the kernel's
+ *   arguments attention_queries/keys/values, decays, betas, state_input and its
+ *   outputs attention_head_outputs, state_output, with their layouts); section 03
+ *   "Kimi Delta Attention decays each key channel" (g per key channel, fp32,
+ *   non-positive; beta = sigmoid(b_proj); L2 norm and 1/sqrt(key_dim) applied in
+ *   the kernel; state [batch, heads, key_dim, value_dim]); section 03 "Loading"
+ *   (a prompt runs a chunked kernel that carries the state from one 64-token
+ *   chunk to the next, a decode step the token-by-token kernel); section 04
+ *   "From the family module" (the state decays channel by channel before each
+ *   delta-rule update; call contract (query, key, value, g=, beta=,
+ *   initial_state=) -> (core_attn_out, last_recurrent_state)).
+ *   Kimi-K3 atlas "gate-project (decode, P = 1000)": sections "Parameters" (the
+ *   gated RMSNorm holds 128 weights shared by the 96 heads) and "Code" (o_norm(o,
+ *   gate) with activation 'sigmoid', heads then flattened to heads * head_dim).
+ *
+ * Conventions for every entry point:
+ *   - Every tensor pointer is a DEVICE pointer (cudaMalloc, or any memory the
+ *     GPU can address) unless its name ends in _host.  Tensors are dense,
+ *     row-major, contiguous, 16-byte aligned.  The caller owns every buffer; the
+ *     library allocates no device memory and keeps no pointer after the call.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and returns without synchronising.  Outputs are valid once the
+ *     stream reaches that point.
+ *   - Arguments are validated on the host before anything is launched.  A bad
+ *     argument returns KDA_ERR_INVALID_ARG, an unsupported but well-formed
+ *     request KDA_ERR_UNSUPPORTED, a CUDA launch/runtime error KDA_ERR_CUDA;
+ *     nothing is launched in the first two cases.  kda_last_error() then holds a
+ *     message for the calling thread.  No C++ exception crosses the ABI.
+ *   - Precondition (not checked on the device): g lies in [-5, 0] (the layer's
+ *     gate_lower_bound is -5), beta in [0, 1].  Out-of-range values give
+ *     numerically meaningless but memory-safe results.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED = 2,  /* well-formed but not built (dims, dtype, chunk, mode) */
+    KDA_ERR_CUDA = 3,         /* a CUDA runtime / launch error */
+    KDA_ERR_TIMEOUT = 4       /* reserved: a bounded device wait gave up */
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_BF16 = 0,
+    KDA_F32 = 1
+} kda_dtype;
+
+typedef enum kda_mode {
+    KDA_MODE_AUTO = 0,    /* tensor-core path where supported, else the fp32 path */
+    KDA_MODE_TENSOR = 1,  /* tcgen05 path only (K = V = 128, chunk = 64); else UNSUPPORTED */
+    KDA_MODE_FP32 = 2     /* CUDA-core fp32 chunked path (any supported K, V, chunk) */
+} kda_mode;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int kda_version(void);
+
+/* Message describing the last failed call on this thread ("" if none). */
+const char *kda_last_error(void);
+
+/* Static name of a status code. */
+const char *kda_status_string(int status);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t kda_launch_count(void);
+
+/*
+ * kda_chunk_fwd -- chunked prefill over whole prompts.
+ *
+ * Pages: nnterp "Kimi-Linear" section 03 "Loading" (the chunked kernel carries
+ * the state from one 64-token chunk to the next and never holds it per token),
+ * section 02 (argument and output layouts), section 04 (call contract).
+ *
+ * Dense mode (cu_seqlens == NULL): N = B sequences of T tokens.
+ *   q, k   [B, T, H, K]  qkv_dtype          v [B, T, H, V] qkv_dtype
+ *   g      [B, T, H, K]  float, log decay    beta [B, T, H] float
+ *   initial_state [N, H, K, V] float or NULL (zero state)
+ *   final_state   [N, H, K, V] float or NULL; may be the same buffer as
+ *                 initial_state (updated in place)
+ *   o      [B, T, H, V]  o_dtype, the per-head outputs (head outputs before the
+ *                        gated norm); may be NULL when y is given
+ * Varlen mode (cu_seqlens != NULL): B must be 1, T is the packed token count and
+ *   sequence n covers tokens [cu_seqlens[n], cu_seqlens[n+1]), n < n_seqs;
+ *   initial_state / final_state are [n_seqs, H, K, V].  cu_seqlens is a device
+ *   int32 array of n_seqs + 1 entries.  cu_seqlens_host, if not NULL, is a host
+ *   copy of it: it is checked (starts at 0, non-decreasing, ends at T) and used to
+ *   start the longest sequences first.  Without it the device array is trusted;
+ *   kernels still clamp every sequence to [0, T] so a bad array cannot make them
+ *   read or write out of bounds.
+ * Gated norm (gate != NULL): gate [B, T, H, V] gate_dtype, norm_w [V] float,
+ *   eps > 0, y [B, T, H * V] o_dtype, y = RMSNorm_v(o) * norm_w * sigmoid(gate).
+ * chunk: tokens per chunk, 16, 32 or 64 (the tensor path needs 64).
+ * scale: applied to q^ (1/sqrt(K) for the layer).  use_qk_l2norm: 0 or 1.
+ * Supported K, V: 32, 64, 128 (fp32 path); 128 (tensor path).
+ * mode: a kda_mode.  Returns a kda_status.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                         const float *g, const float *beta, const float *initial_state,
+                         float *final_state, void *o, kda_dtype o_dtype,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
+                         int B, int T, int H, int K, int V, int chunk, float scale,
+                         int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                         const float *norm_w, float eps, void *y, int mode, void *stream);
+
+/*
+ * kda_recurrent_fwd -- the token-by-token form over T tokens (fp32 arithmetic).
+ *
+ * Pages: nnterp "Kimi-Linear" section 03 "Loading" (the token-by-token kernel;
+ * the per-token `states` readout needs it) and section 02 (`state` / `states`
+ * [batch seq heads key_dim value_dim]).
+ *
+ * Same arguments and layouts as kda_chunk_fwd, without chunk and mode, plus
+ *   states [B, T, H, K, V] float or NULL: the state after every token (varlen:
+ *          [1, T, H, K, V] indexed by packed token).
+ */
+kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                             const float *g, const float *beta, const float *initial_state,
+                             float *final_state, void *o, kda_dtype o_dtype, float *states,
+                             const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                             int n_seqs, int B, int T, int H, int K, int V, float scale,
+                             int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                             const float *norm_w, float eps, void *y, void *stream);
+
+/*
+ * kda_recurrent_step -- one decode token per sequence, gated norm fused.
+ *
+ * Pages: nnterp "Kimi-Linear" section 03 "Loading" (a decode step runs the
+ * token-by-token kernel); Kimi-K3 atlas "gate-project (decode, P = 1000)"
+ * (decode shapes [B, 96, 1, 128] in, [B, 1, 12288] after the flatten).
+ *
+ *   q, k  [B, H, K] qkv_dtype     v [B, H, V] qkv_dtype
+ *   g     [B, H, K] float         beta [B, H] float
+ *   state_in  [B, H, K, V] float or NULL (zero state)
+ *   state_out [B, H, K, V] float; may be the same buffer as state_in (in place)
+ *   o     [B, H, V] o_dtype or NULL when y is given
+ *   gate  [B, H, V] gate_dtype or NULL; norm_w [V]; eps; y [B, H * V] o_dtype
+ * Supported K, V: 32, 64, 128.
+ */
+kda_status kda_recurrent_step(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                              const float *g, const float *beta, const float *state_in,
+                              float *state_out, void *o, kda_dtype o_dtype, int B, int H, int K,
+                              int V, float scale, int use_qk_l2norm, const void *gate,
+                              kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
+                              void *stream);
+
+/*
+ * kda_gated_rmsnorm -- the head-wise sigmoid-gated RMSNorm on its own.
+ *
+ * Page: Kimi-K3 atlas "gate-project (decode, P = 1000)", sections "Parameters"
+ * and "Code".
+ *   o    [rows, H, V] o_dtype       gate [rows, H, V] gate_dtype
+ *   w    [V] float                  y    [rows, H * V] y_dtype
+ *   y = o / sqrt(mean_v(o^2) + eps) * w * sigmoid(gate); rows may be 0.
+ * Supported V: 32, 64, 128.
+ */
+kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,
+                             kda_dtype gate_dtype, const float *w, float eps, void *y,
+                             kda_dtype y_dtype, int64_t rows, int H, int V, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

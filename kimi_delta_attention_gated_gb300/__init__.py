@@ -1,0 +1,253 @@
+"""Kimi Delta Attention core on GB300: Python binding of libkda.
+
+Thin ctypes marshalling over the C ABI declared in include/kda.h: every step of
+the computation runs in libkda's CUDA kernels; torch only allocates device memory
+and supplies the current stream.  There is no CPU fallback: calling any function
+without a built libkda (or without a GPU) raises.
+
+Entry points (same names as the C ABI, minus the ``kda_`` prefix):
+  chunk_fwd       chunked prefill  (q, k, v, g, beta, initial_state) -> (o, final_state[, y])
+  recurrent_fwd   token-by-token form over T tokens, optional per-token states
+  recurrent_step  one decode token per sequence with the fused gated norm
+  gated_rmsnorm   y = RMSNorm_v(o) * w * sigmoid(gate) per (token, head)
+
+Inputs may live on the host: they are copied to the current CUDA device, and the
+results are copied back to the host, which makes the call end-to-end.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["chunk_fwd", "recurrent_fwd", "recurrent_step", "gated_rmsnorm", "launch_count",
+           "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libkda.so")
+_lib = None
+_lock = threading.Lock()
+
+BF16, F32 = 0, 1
+MODE_AUTO, MODE_TENSOR, MODE_FP32 = 0, 1, 2
+_MODES = {"auto": MODE_AUTO, "tensor": MODE_TENSOR, "fp32": MODE_FP32}
+_STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+           4: "KDA_ERR_TIMEOUT"}
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libkda.so is not built ({_LIB_PATH}); run __graft_entry__.build() "
+                               "or python kimi_delta_attention_gated_gb300/build.py")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.kda_chunk_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I,
+                                      P, I, P, F, P, I, P]
+        lib.kda_recurrent_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I,
+                                          P, I, P, F, P, P]
+        lib.kda_recurrent_step.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, F,
+                                           P, P]
+        lib.kda_gated_rmsnorm.argtypes = [P, I, P, I, P, F, P, I, ctypes.c_int64, I, I, P]
+        for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_launch_count.restype = ctypes.c_uint64
+        lib.kda_version.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise KDAError(status, _load().kda_last_error().decode())
+
+
+def launch_count() -> int:
+    """Kernels libkda has launched in this process."""
+    return int(_load().kda_launch_count())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _prep(t, device, dtype=None):
+    """Contiguous device tensor (host tensors are copied; pinned ones asynchronously)."""
+    if t is None:
+        return None
+    if dtype is not None and t.dtype != dtype:
+        t = t.to(dtype)
+    if t.device.type != "cuda":
+        t = t.to(device, non_blocking=t.is_pinned())
+    return t.contiguous()
+
+
+def _device_of(*ts):
+    for t in ts:
+        if t is not None and t.device.type == "cuda":
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _cu(cu_seqlens, device):
+    if cu_seqlens is None:
+        return None, None, 0
+    host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+    dev = cu_seqlens.to(device=device, dtype=torch.int32).contiguous()
+    return dev, host, host.numel() - 1
+
+
+def _to_host(ts, host):
+    if not host:
+        return ts
+    return tuple(None if t is None else t.to("cpu") for t in ts)
+
+
+def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use_qk_l2norm=True,
+              cu_seqlens=None, output_final_state=True, gate=None, norm_w=None, eps=1e-5,
+              out_dtype=torch.float32, mode="auto", return_o=True, o=None, y=None, final_state=None):
+    """Chunked prefill.  q, k [B,T,H,K]; v [B,T,H,V]; g [B,T,H,K] fp32; beta [B,T,H] fp32;
+    initial_state [N,H,K,V] fp32 or None.  With ``cu_seqlens`` (int, n_seqs + 1) B must be 1.
+    Returns (o, final_state) or, with ``gate``/``norm_w``, (o, final_state, y) where
+    y [B,T,H*V] is the sigmoid-gated RMSNorm of o (o is None when return_o=False).
+    Preallocated outputs may be passed as o / y / final_state (final_state may be
+    initial_state itself for an in-place update)."""
+    lib = _load()
+    host = q.device.type != "cuda"
+    dev = _device_of(q, k, v)
+    q, k, v = _prep(q, dev), _prep(k, dev), _prep(v, dev)
+    g, beta = _prep(g, dev, torch.float32), _prep(beta, dev, torch.float32)
+    initial_state = _prep(initial_state, dev, torch.float32)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    cu_d, cu_h, n_seqs = _cu(cu_seqlens, dev)
+    N = n_seqs if cu_d is not None else B
+    if gate is not None:
+        gate, norm_w = _prep(gate, dev), _prep(norm_w, dev, torch.float32)
+        if y is None:
+            y = torch.empty((B, T, H * V), device=dev, dtype=out_dtype)
+    if o is None and (return_o or gate is None):
+        o = torch.empty((B, T, H, V), device=dev, dtype=out_dtype)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), device=dev, dtype=torch.float32)
+    if scale is None:
+        scale = K ** -0.5
+    _check(lib.kda_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(final_state),
+        _ptr(o), _dt(o if o is not None else y), _ptr(cu_d), _ptr(cu_h), n_seqs, B, T, H, K, V, int(chunk),
+        float(scale), int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16,
+        _ptr(norm_w), float(eps), _ptr(y), _MODES[mode] if isinstance(mode, str) else int(mode), _stream()))
+    if gate is not None:
+        return _to_host((o, final_state, y), host)
+    return _to_host((o, final_state), host)
+
+
+def recurrent_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, use_qk_l2norm=True,
+                  cu_seqlens=None, output_final_state=True, output_states=False, gate=None,
+                  norm_w=None, eps=1e-5, out_dtype=torch.float32):
+    """Token-by-token form over T tokens (fp32).  Returns (o, final_state[, states][, y])."""
+    lib = _load()
+    host = q.device.type != "cuda"
+    dev = _device_of(q, k, v)
+    q, k, v = _prep(q, dev), _prep(k, dev), _prep(v, dev)
+    g, beta = _prep(g, dev, torch.float32), _prep(beta, dev, torch.float32)
+    initial_state = _prep(initial_state, dev, torch.float32)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    cu_d, cu_h, n_seqs = _cu(cu_seqlens, dev)
+    N = n_seqs if cu_d is not None else B
+    o = torch.empty((B, T, H, V), device=dev, dtype=out_dtype)
+    final_state = torch.empty((N, H, K, V), device=dev, dtype=torch.float32) if output_final_state else None
+    states = torch.empty((B, T, H, K, V), device=dev, dtype=torch.float32) if output_states else None
+    y = None
+    if gate is not None:
+        gate, norm_w = _prep(gate, dev), _prep(norm_w, dev, torch.float32)
+        y = torch.empty((B, T, H * V), device=dev, dtype=out_dtype)
+    if scale is None:
+        scale = K ** -0.5
+    _check(lib.kda_recurrent_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(final_state),
+        _ptr(o), _dt(o), _ptr(states), _ptr(cu_d), _ptr(cu_h), n_seqs, B, T, H, K, V, float(scale),
+        int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16, _ptr(norm_w),
+        float(eps), _ptr(y), _stream()))
+    out = [o, final_state]
+    if output_states:
+        out.append(states)
+    if gate is not None:
+        out.append(y)
+    return _to_host(tuple(out), host)
+
+
+def recurrent_step(q, k, v, g, beta, state, *, scale=None, use_qk_l2norm=True, gate=None, norm_w=None,
+                   eps=1e-5, out_dtype=torch.float32, state_out=None, return_o=True, o=None, y=None):
+    """One decode token per sequence.  q, k [B,H,K]; v [B,H,V]; g [B,H,K]; beta [B,H];
+    state [B,H,K,V] fp32 (or None).  ``state_out=state`` updates the state in place.
+    Returns (o, state_out[, y])."""
+    lib = _load()
+    host = q.device.type != "cuda"
+    dev = _device_of(q, k, v, state)
+    q, k, v = _prep(q, dev), _prep(k, dev), _prep(v, dev)
+    g, beta = _prep(g, dev, torch.float32), _prep(beta, dev, torch.float32)
+    state = _prep(state, dev, torch.float32)
+    B, H, K = q.shape
+    V = v.shape[-1]
+    if state_out is None:
+        state_out = torch.empty((B, H, K, V), device=dev, dtype=torch.float32)
+    if gate is not None:
+        gate, norm_w = _prep(gate, dev), _prep(norm_w, dev, torch.float32)
+        if y is None:
+            y = torch.empty((B, H * V), device=dev, dtype=out_dtype)
+    if o is None and (return_o or gate is None):
+        o = torch.empty((B, H, V), device=dev, dtype=out_dtype)
+    if scale is None:
+        scale = K ** -0.5
+    _check(lib.kda_recurrent_step(
+        _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(state), _ptr(state_out), _ptr(o),
+        _dt(o if o is not None else y), B, H, K, V, float(scale), int(bool(use_qk_l2norm)), _ptr(gate),
+        _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y), _stream()))
+    if gate is not None:
+        return _to_host((o, state_out, y), host)
+    return _to_host((o, state_out), host)
+
+
+def gated_rmsnorm(o, gate, w, eps=1e-5, *, out_dtype=torch.float32, y=None):
+    """y [.., H*V] = o / sqrt(mean_v(o^2) + eps) * w * sigmoid(gate) over each (token, head)."""
+    lib = _load()
+    host = o.device.type != "cuda"
+    dev = _device_of(o, gate)
+    o, gate, w = _prep(o, dev), _prep(gate, dev), _prep(w, dev, torch.float32)
+    H, V = o.shape[-2], o.shape[-1]
+    rows = o.numel() // (H * V)
+    if y is None:
+        y = torch.empty(o.shape[:-2] + (H * V,), device=dev, dtype=out_dtype)
+    _check(lib.kda_gated_rmsnorm(_ptr(o), _dt(o), _ptr(gate), _dt(gate), _ptr(w), float(eps), _ptr(y), _dt(y),
+                                 rows, H, V, _stream()))
+    return _to_host((y,), host)[0]

@@ -1,0 +1,254 @@
+// kda_abi.cu -- the extern "C" boundary of libkda: argument validation, path
+// selection and launch bookkeeping.  Declarations and their documentation are
+// in include/kda.h.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+thread_local char g_err[512] = "";
+std::atomic<uint64_t> g_launches{0};
+constexpr int kVersion = 10000;  // 1.0.0
+}  // namespace
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+kda_status check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("%s: %s", what, cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // namespace kda
+
+using kda::set_error;
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool dtype_ok(int d) { return d == KDA_BF16 || d == KDA_F32; }
+
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+#define KDA_REQUIRE(cond, code, ...) \
+    do {                             \
+        if (!(cond)) {               \
+            set_error(__VA_ARGS__);  \
+            return code;             \
+        }                            \
+    } while (0)
+
+// Checks shared by the prefill entry points; fills the sequence count.
+kda_status check_seq_args(const char *fn, const void *q, const void *k, const void *v, int qkv_dtype,
+                          const float *g, const float *beta, const float *s0, const float *sT,
+                          const void *o, int o_dtype, const int32_t *cu, const int32_t *cu_host,
+                          int n_seqs, int B, int T, int H, int K, int V, float scale,
+                          const void *gate, int gate_dtype, const float *norm_w, float eps,
+                          const void *y, int &N) {
+    // with no tokens nothing is read or written but the state (empty tensors may be NULL)
+    const bool no_tokens = (int64_t)B * T == 0;
+    KDA_REQUIRE(no_tokens || (q && k && v && g && beta), KDA_ERR_INVALID_ARG,
+                "%s: q, k, v, g and beta must not be NULL", fn);
+    KDA_REQUIRE(no_tokens || o || (gate && y), KDA_ERR_INVALID_ARG,
+                "%s: o may be NULL only when the gated norm writes y", fn);
+    KDA_REQUIRE(dtype_ok(qkv_dtype) && dtype_ok(o_dtype) && (!gate || dtype_ok(gate_dtype)),
+                KDA_ERR_UNSUPPORTED, "%s: unsupported dtype", fn);
+    KDA_REQUIRE(H > 0 && T >= 0 && B > 0, KDA_ERR_INVALID_ARG, "%s: need B > 0, T >= 0, H > 0", fn);
+    KDA_REQUIRE(dim_ok(K) && dim_ok(V), KDA_ERR_UNSUPPORTED, "%s: K=%d V=%d (supported: 32, 64, 128)", fn, K, V);
+    KDA_REQUIRE(std::isfinite(scale), KDA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
+    KDA_REQUIRE((int64_t)B * T <= (int64_t)INT32_MAX, KDA_ERR_INVALID_ARG, "%s: B*T too large", fn);
+    const void *ptrs[] = {q, k, v, g, beta, s0, sT, o, cu, gate, norm_w, y};
+    for (const void *ptr : ptrs)
+        KDA_REQUIRE(!ptr || aligned16(ptr), KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);
+    if (gate) {
+        KDA_REQUIRE(norm_w && (y || no_tokens), KDA_ERR_INVALID_ARG, "%s: the gated norm needs norm_w and y", fn);
+        KDA_REQUIRE(eps > 0.f && std::isfinite(eps), KDA_ERR_INVALID_ARG, "%s: eps must be > 0", fn);
+    }
+    if (cu) {
+        KDA_REQUIRE(B == 1, KDA_ERR_INVALID_ARG, "%s: varlen (cu_seqlens) needs B == 1", fn);
+        KDA_REQUIRE(n_seqs > 0, KDA_ERR_INVALID_ARG, "%s: varlen needs n_seqs > 0", fn);
+        if (cu_host) {
+            KDA_REQUIRE(cu_host[0] == 0, KDA_ERR_INVALID_ARG, "%s: cu_seqlens[0] must be 0", fn);
+            for (int i = 0; i < n_seqs; ++i)
+                KDA_REQUIRE(cu_host[i + 1] >= cu_host[i], KDA_ERR_INVALID_ARG,
+                            "%s: cu_seqlens must not decrease (entry %d)", fn, i + 1);
+            KDA_REQUIRE(cu_host[n_seqs] == T, KDA_ERR_INVALID_ARG, "%s: cu_seqlens[n_seqs] = %d but T = %d", fn,
+                        cu_host[n_seqs], T);
+        }
+        N = n_seqs;
+    } else {
+        KDA_REQUIRE(!cu_host, KDA_ERR_INVALID_ARG, "%s: cu_seqlens_host given without cu_seqlens", fn);
+        N = B;
+    }
+    return KDA_OK;
+}
+
+kda::SeqParams make_params(const void *q, const void *k, const void *v, int qkv_dtype, const float *g,
+                           const float *beta, const float *s0, float *sT, void *o, int o_dtype,
+                           float *states, const int32_t *cu, int N, int T, int H, float scale,
+                           int l2, const void *gate, int gate_dtype, const float *norm_w, float eps,
+                           void *y) {
+    kda::SeqParams p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.g = g;
+    p.beta = beta;
+    p.s0 = s0;
+    p.sT = sT;
+    p.o = o;
+    p.states = states;
+    p.cu_seqlens = cu;
+    p.cu_host = nullptr;
+    p.gate = gate;
+    p.norm_w = norm_w;
+    p.y = y;
+    p.N = N;
+    p.T = T;
+    p.H = H;
+    p.scale = scale;
+    p.eps = eps;
+    p.l2norm = l2 ? 1 : 0;
+    p.qkv_bf16 = qkv_dtype == KDA_BF16;
+    p.o_bf16 = o_dtype == KDA_BF16;
+    p.gate_bf16 = gate_dtype == KDA_BF16;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return kda::kVersion; }
+
+const char *kda_last_error(void) { return kda::g_err; }
+
+const char *kda_status_string(int s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+uint64_t kda_launch_count(void) { return kda::g_launches.load(std::memory_order_relaxed); }
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                         const float *g, const float *beta, const float *initial_state,
+                         float *final_state, void *o, kda_dtype o_dtype,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
+                         int B, int T, int H, int K, int V, int chunk, float scale,
+                         int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                         const float *norm_w, float eps, void *y, int mode, void *stream) {
+    kda::g_err[0] = 0;
+    int N = 0;
+    kda_status s = check_seq_args("kda_chunk_fwd", q, k, v, qkv_dtype, g, beta, initial_state,
+                                  final_state, o, o_dtype, cu_seqlens, cu_seqlens_host, n_seqs, B, T,
+                                  H, K, V, scale, gate, gate_dtype, norm_w, eps, y, N);
+    if (s != KDA_OK) return s;
+    KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, KDA_ERR_UNSUPPORTED,
+                "kda_chunk_fwd: chunk=%d (supported: 16, 32, 64)", chunk);
+    KDA_REQUIRE(mode == KDA_MODE_AUTO || mode == KDA_MODE_TENSOR || mode == KDA_MODE_FP32,
+                KDA_ERR_INVALID_ARG, "kda_chunk_fwd: unknown mode %d", mode);
+    const bool tc_ok = kda::chunk_tc_supported(K, V, chunk) && qkv_dtype == KDA_BF16;
+    KDA_REQUIRE(mode != KDA_MODE_TENSOR || tc_ok, KDA_ERR_UNSUPPORTED,
+                "kda_chunk_fwd: the tensor path needs bf16 q/k/v, K = V = 128 and chunk = 64");
+    cudaStream_t st = (cudaStream_t)stream;
+    // an empty prompt only hands the state through: the fp32 path does that without a tensor map
+    const bool use_tc = tc_ok && mode != KDA_MODE_FP32 && T > 0;
+    if (use_tc) {
+        kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o,
+                                       o_dtype, nullptr, cu_seqlens, N, T, H, scale, use_qk_l2norm,
+                                       gate, gate_dtype, norm_w, eps, y);
+        p.cu_host = cu_seqlens_host;
+        return kda::launch_chunk_tc(p, K, V, chunk, st);
+    }
+    // fp32 path: o goes to y's buffer when o is not wanted, then the norm runs in place.
+    void *o_target = o ? o : y;
+    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o_target,
+                                   o_dtype, nullptr, cu_seqlens, N, T, H, scale, use_qk_l2norm,
+                                   nullptr, gate_dtype, norm_w, eps, nullptr);
+    s = kda::launch_chunk_fp32(p, K, V, chunk, nullptr, st);
+    if (s != KDA_OK || !gate || (int64_t)B * T == 0) return s;
+    return kda::launch_gated_rmsnorm(o_target, o_dtype == KDA_BF16, gate, gate_dtype == KDA_BF16,
+                                     norm_w, eps, y, o_dtype == KDA_BF16, (int64_t)B * T, H, V, st);
+}
+
+kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                             const float *g, const float *beta, const float *initial_state,
+                             float *final_state, void *o, kda_dtype o_dtype, float *states,
+                             const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                             int n_seqs, int B, int T, int H, int K, int V, float scale,
+                             int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                             const float *norm_w, float eps, void *y, void *stream) {
+    kda::g_err[0] = 0;
+    int N = 0;
+    kda_status s = check_seq_args("kda_recurrent_fwd", q, k, v, qkv_dtype, g, beta, initial_state,
+                                  final_state, o, o_dtype, cu_seqlens, cu_seqlens_host, n_seqs, B, T,
+                                  H, K, V, scale, gate, gate_dtype, norm_w, eps, y, N);
+    if (s != KDA_OK) return s;
+    KDA_REQUIRE(!states || aligned16(states), KDA_ERR_INVALID_ARG, "kda_recurrent_fwd: states must be 16-byte aligned");
+    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o, o_dtype,
+                                   states, cu_seqlens, N, T, H, scale, use_qk_l2norm, gate, gate_dtype,
+                                   norm_w, eps, y);
+    return kda::launch_recurrent(p, K, V, (cudaStream_t)stream);
+}
+
+kda_status kda_recurrent_step(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                              const float *g, const float *beta, const float *state_in,
+                              float *state_out, void *o, kda_dtype o_dtype, int B, int H, int K,
+                              int V, float scale, int use_qk_l2norm, const void *gate,
+                              kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
+                              void *stream) {
+    kda::g_err[0] = 0;
+    int N = 0;
+    KDA_REQUIRE(state_out, KDA_ERR_INVALID_ARG, "kda_recurrent_step: state_out must not be NULL");
+    kda_status s = check_seq_args("kda_recurrent_step", q, k, v, qkv_dtype, g, beta, state_in, state_out,
+                                  o, o_dtype, nullptr, nullptr, 0, B, 1, H, K, V, scale, gate,
+                                  gate_dtype, norm_w, eps, y, N);
+    if (s != KDA_OK) return s;
+    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, state_in, state_out, o, o_dtype,
+                                   nullptr, nullptr, N, 1, H, scale, use_qk_l2norm, gate, gate_dtype,
+                                   norm_w, eps, y);
+    return kda::launch_recurrent(p, K, V, (cudaStream_t)stream);
+}
+
+kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,
+                             kda_dtype gate_dtype, const float *w, float eps, void *y,
+                             kda_dtype y_dtype, int64_t rows, int H, int V, void *stream) {
+    kda::g_err[0] = 0;
+    KDA_REQUIRE(o && gate && w && y, KDA_ERR_INVALID_ARG, "kda_gated_rmsnorm: o, gate, w and y must not be NULL");
+    KDA_REQUIRE(dtype_ok(o_dtype) && dtype_ok(gate_dtype) && dtype_ok(y_dtype), KDA_ERR_UNSUPPORTED,
+                "kda_gated_rmsnorm: unsupported dtype");
+    KDA_REQUIRE(rows >= 0 && H > 0, KDA_ERR_INVALID_ARG, "kda_gated_rmsnorm: need rows >= 0 and H > 0");
+    KDA_REQUIRE(dim_ok(V), KDA_ERR_UNSUPPORTED, "kda_gated_rmsnorm: V=%d (supported: 32, 64, 128)", V);
+    KDA_REQUIRE(eps > 0.f && std::isfinite(eps), KDA_ERR_INVALID_ARG, "kda_gated_rmsnorm: eps must be > 0");
+    KDA_REQUIRE(aligned16(o) && aligned16(gate) && aligned16(w) && aligned16(y), KDA_ERR_INVALID_ARG,
+                "kda_gated_rmsnorm: every pointer must be 16-byte aligned");
+    KDA_REQUIRE(o != y || o_dtype == y_dtype, KDA_ERR_INVALID_ARG,
+                "kda_gated_rmsnorm: in place (o == y) needs o_dtype == y_dtype");
+    return kda::launch_gated_rmsnorm(o, o_dtype == KDA_BF16, gate, gate_dtype == KDA_BF16, w, eps, y,
+                                     y_dtype == KDA_BF16, rows, H, V, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,244 @@
+// kda_recurrent.cu -- the token-by-token KDA kernel (decode step and multi-token form).
+//
+// Pages: nnterp encyclopedia "Kimi-Linear", section 03 "Loading" (a decode step
+// runs the token-by-token kernel), section 03 "Kimi Delta Attention decays each
+// key channel" and section 04 (decay per key channel before each delta-rule
+// update; q, k L2-normalised in the kernel).  Kimi-K3 atlas "gate-project
+// (decode, P = 1000)" for the fused sigmoid-gated RMSNorm.
+//
+// One CTA per (sequence, head).  The fp32 state S[K][V] lives in registers for
+// the whole call: warp w owns rows [w*K/NW, (w+1)*K/NW), lane l owns columns
+// [l*V/32, (l+1)*V/32) of every one of them, so each row is read and written as
+// one coalesced 128-bit-per-lane transaction (V = 128).  Per token:
+//   S' = Diag(exp g) S           (each thread scales its own rows)
+//   u  = S'^T k^,  p = S'^T q^   (per-thread partials over rows, then a
+//                                 cross-warp sum in shared memory)
+//   D  = beta (v - u)
+//   o  = scale (p + (k^.q^) D)   = scale S^T q^ after the write
+//   S  = S' + k^ D^T
+// so the state crosses HBM exactly once in each direction per call.  For decode
+// (T = 1) that is the whole cost: 2 x 64 KiB per (sequence, head) at d = 128.
+#include <math.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+template <int VPL>
+struct VecF;
+template <>
+struct VecF<1> {
+    float x[1];
+};
+template <>
+struct VecF<2> {
+    float x[2];
+};
+template <>
+struct VecF<4> {
+    float x[4];
+};
+
+template <int VPL>
+__device__ __forceinline__ void ld_row(const float *p, float (&r)[VPL]) {
+    if constexpr (VPL == 4) {
+        float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
+        r[0] = t.x; r[1] = t.y; r[2] = t.z; r[3] = t.w;
+    } else if constexpr (VPL == 2) {
+        float2 t = __ldcs(reinterpret_cast<const float2 *>(p));
+        r[0] = t.x; r[1] = t.y;
+    } else {
+        r[0] = __ldcs(p);
+    }
+}
+
+template <int VPL>
+__device__ __forceinline__ void st_row(float *p, const float (&r)[VPL]) {
+    if constexpr (VPL == 4) {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(r[0], r[1], r[2], r[3]));
+    } else if constexpr (VPL == 2) {
+        __stcs(reinterpret_cast<float2 *>(p), make_float2(r[0], r[1]));
+    } else {
+        __stcs(p, r[0]);
+    }
+}
+
+template <int K, int V>
+__global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) {
+    constexpr int RPW = K / kWarps;  // rows per warp
+    constexpr int VPL = V / 32;      // columns per lane
+    static_assert(K % kWarps == 0 && V % 32 == 0 && K <= kThreads && V <= 128, "shape");
+
+    __shared__ float sq[K], sk[K], se[K];
+    __shared__ float sv[V], sd[V];
+    __shared__ float red_u[kWarps][V], red_q[kWarps][V];
+    __shared__ float misc[kWarps][4];
+
+    const int H = p.H;
+    const int unit = blockIdx.x;
+    const int n = unit / H, h = unit % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int bos, len;
+    seq_range(p, n, bos, len);
+
+    const size_t state_off = (size_t)unit * K * V;
+    float s[RPW][VPL];
+    // Issue every state load first so they are in flight during the q/k prologue.
+    if (p.s0) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+            ld_row<VPL>(p.s0 + state_off + (size_t)(warp * RPW + r) * V + lane * VPL, s[r]);
+    } else {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int c = 0; c < VPL; ++c) s[r][c] = 0.f;
+    }
+
+    for (int t = 0; t < len; ++t) {
+        const size_t row = (size_t)(bos + t);
+        const size_t hk = (row * H + h) * K, hv = (row * H + h) * V;
+        // -- prologue: load q, k, exp(g), v; partial norms
+        float pq = 0.f, pk = 0.f, pqk = 0.f;
+        if (tid < K) {
+            const float qv = ld_in(p.q, hk + tid, p.qkv_bf16);
+            const float kv = ld_in(p.k, hk + tid, p.qkv_bf16);
+            sq[tid] = qv;
+            sk[tid] = kv;
+            se[tid] = __expf(p.g[hk + tid]);
+            pq = qv * qv;
+            pk = kv * kv;
+            pqk = qv * kv;
+        }
+        if (tid >= kThreads - V) sv[tid - (kThreads - V)] = ld_in(p.v, hv + tid - (kThreads - V), p.qkv_bf16);
+        pq = warp_sum(pq);
+        pk = warp_sum(pk);
+        pqk = warp_sum(pqk);
+        if (lane == 0) {
+            misc[warp][0] = pq;
+            misc[warp][1] = pk;
+            misc[warp][2] = pqk;
+        }
+        __syncthreads();
+        float ssq = 0.f, ssk = 0.f, sqk = 0.f;
+#pragma unroll
+        for (int w = 0; w < (K + 31) / 32; ++w) {
+            ssq += misc[w][0];
+            ssk += misc[w][1];
+            sqk += misc[w][2];
+        }
+        const float rq = p.l2norm ? rsqrtf(ssq + 1e-6f) : 1.f;
+        const float rk = p.l2norm ? rsqrtf(ssk + 1e-6f) : 1.f;
+        const float kq = sqk * rq * rk;  // k^ . q^
+
+        // -- decay rows, partial u = S'^T k^ and p = S'^T q^
+        float pu[VPL], pp[VPL];
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) pu[c] = pp[c] = 0.f;
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const int i = warp * RPW + r;
+            const float e = se[i], ki = sk[i] * rk, qi = sq[i] * rq;
+#pragma unroll
+            for (int c = 0; c < VPL; ++c) {
+                s[r][c] *= e;
+                pu[c] = fmaf(ki, s[r][c], pu[c]);
+                pp[c] = fmaf(qi, s[r][c], pp[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) {
+            red_u[warp][lane * VPL + c] = pu[c];
+            red_q[warp][lane * VPL + c] = pp[c];
+        }
+        __syncthreads();
+
+        // -- delta and output, one thread per value column
+        float ov = 0.f;
+        if (tid < V) {
+            float u = 0.f, pv = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                u += red_u[w][tid];
+                pv += red_q[w][tid];
+            }
+            const float b = p.beta[row * H + h];
+            const float d = b * (sv[tid] - u);
+            sd[tid] = d;
+            ov = p.scale * fmaf(kq, d, pv);
+            if (p.o) st_out(p.o, hv + tid, ov, p.o_bf16);
+        }
+        if (p.gate) {
+            // sigmoid-gated RMSNorm over the V outputs of this head
+            float sq2 = warp_sum(tid < V ? ov * ov : 0.f);
+            if (lane == 0) misc[warp][3] = sq2;
+        }
+        __syncthreads();
+        if (p.gate && tid < V) {
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < V / 32; ++w) ss += misc[w][3];
+            const float inv = rsqrtf(ss / (float)V + p.eps);
+            const float gt = ld_in(p.gate, hv + tid, p.gate_bf16);
+            st_out(p.y, hv + tid, ov * inv * p.norm_w[tid] * sigmoidf_(gt), p.o_bf16);
+        }
+
+        // -- rank-one write
+        float dl[VPL];
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) dl[c] = sd[lane * VPL + c];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float ki = sk[warp * RPW + r] * rk;
+#pragma unroll
+            for (int c = 0; c < VPL; ++c) s[r][c] = fmaf(ki, dl[c], s[r][c]);
+        }
+        if (p.states) {
+            const size_t so = row * H * (size_t)K * V + (size_t)h * K * V;
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                st_row<VPL>(p.states + so + (size_t)(warp * RPW + r) * V + lane * VPL, s[r]);
+        }
+        __syncthreads();  // shared buffers are rewritten by the next token
+    }
+
+    if (p.sT) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+            st_row<VPL>(p.sT + state_off + (size_t)(warp * RPW + r) * V + lane * VPL, s[r]);
+    }
+}
+
+template <int K, int V>
+kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
+    const int units = p.N * p.H;
+    if (units == 0) return KDA_OK;
+    recurrent_kernel<K, V><<<units, kThreads, 0, st>>>(p);
+    note_launch();
+    return check_launch("recurrent_kernel");
+}
+
+}  // namespace
+
+kda_status launch_recurrent(const SeqParams &p, int K, int V, cudaStream_t st) {
+#define KDA_CASE(KK, VV) \
+    if (K == KK && V == VV) return launch_kv<KK, VV>(p, st);
+    KDA_CASE(128, 128)
+    KDA_CASE(64, 64)
+    KDA_CASE(32, 32)
+    KDA_CASE(128, 64)
+    KDA_CASE(64, 128)
+    KDA_CASE(128, 32)
+    KDA_CASE(32, 128)
+    KDA_CASE(64, 32)
+    KDA_CASE(32, 64)
+#undef KDA_CASE
+    set_error("recurrent: K=%d V=%d not built (K, V in {32, 64, 128})", K, V);
+    return KDA_ERR_UNSUPPORTED;
+}
+
+}  // namespace kda

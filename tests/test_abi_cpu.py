@@ -1,0 +1,155 @@
+"""CPU checks of the C ABI: libkda loads, exports every symbol include/*.h declares,
+and rejects bad arguments on the host with a defined status before launching
+anything.  No test here touches a GPU: the device pointers are fake aligned
+addresses that validation never dereferences."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+BF16, F32 = 0, 1
+FAKE = 0x10000000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kimi_delta_attention_gated_gb300 import build as b
+    b.build()
+    from kimi_delta_attention_gated_gb300 import _load
+    return _load()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names.update(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm"):
+        assert fn in names
+
+
+def test_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, f"libkda does not export {missing}"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.kda_version() >= 10000
+    lib.kda_status_string.restype = ctypes.c_char_p
+    assert lib.kda_status_string(0) == b"KDA_OK"
+    assert lib.kda_status_string(1) == b"KDA_ERR_INVALID_ARG"
+    assert lib.kda_status_string(99) == b"KDA_ERR_UNKNOWN"
+
+
+def chunk_call(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, qkv=BF16, g=FAKE, beta=FAKE, s0=None, sT=None, o=FAKE, odt=F32,
+             cu=None, cu_host=None, n_seqs=0, B=1, T=64, H=2, K=128, V=128, chunk=64, scale=0.088,
+             l2=1, gate=None, gdt=BF16, w=None, eps=1e-5, y=None, mode=0)
+    a.update(over)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["s0"], a["sT"], a["o"],
+                             a["odt"], a["cu"], a["cu_host"], a["n_seqs"], a["B"], a["T"], a["H"], a["K"],
+                             a["V"], a["chunk"], a["scale"], a["l2"], a["gate"], a["gdt"], a["w"], a["eps"],
+                             a["y"], a["mode"], None)
+
+
+def cu_host(values):
+    arr = np.asarray(values, np.int32)
+    return arr, arr.ctypes.data_as(ctypes.c_void_p)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), INVALID),
+    (dict(beta=None), INVALID),
+    (dict(o=None), INVALID),                       # o may be NULL only with the gated norm
+    (dict(K=100), UNSUPPORTED),
+    (dict(V=256), UNSUPPORTED),
+    (dict(chunk=48), UNSUPPORTED),
+    (dict(qkv=7), UNSUPPORTED),
+    (dict(odt=3), UNSUPPORTED),
+    (dict(q=FAKE + 4), INVALID),                   # misaligned
+    (dict(o=FAKE + 8), INVALID),
+    (dict(H=0), INVALID),
+    (dict(T=-1), INVALID),
+    (dict(B=0), INVALID),
+    (dict(mode=9), INVALID),
+    (dict(mode=1, K=32, V=32), UNSUPPORTED),       # tensor path only at K = V = 128
+    (dict(mode=1, chunk=32), UNSUPPORTED),
+    (dict(mode=1, qkv=F32), UNSUPPORTED),
+    (dict(gate=FAKE), INVALID),                    # gate without norm_w / y
+    (dict(gate=FAKE, w=FAKE, y=FAKE, eps=0.0), INVALID),
+    (dict(scale=float("nan")), INVALID),
+    (dict(cu=FAKE, n_seqs=0), INVALID),
+    (dict(cu=FAKE, n_seqs=2, B=2), INVALID),       # varlen needs B == 1
+    (dict(cu_host=FAKE), INVALID),                 # host copy without the device array
+])
+def test_chunk_fwd_rejects(lib, over, code):
+    assert chunk_call(lib, **over) == code
+    assert lib.kda_last_error()
+
+
+@pytest.mark.parametrize("values,T", [([0, 5, 3, 8], 8), ([1, 4, 8], 8), ([0, 4, 7], 8), ([0, -1, 8], 8)])
+def test_chunk_fwd_rejects_bad_cu_seqlens(lib, values, T):
+    arr, ptr = cu_host(values)
+    assert chunk_call(lib, cu=FAKE, cu_host=ptr, n_seqs=len(values) - 1, T=T) == INVALID
+    assert b"cu_seqlens" in lib.kda_last_error()
+
+
+def test_recurrent_step_rejects(lib):
+    f = lib.kda_recurrent_step
+    base = [FAKE, FAKE, FAKE, BF16, FAKE, FAKE, FAKE, FAKE, FAKE, F32, 4, 2, 128, 128, 0.088, 1, None, BF16,
+            None, 1e-5, None, None]
+    bad_state = list(base)
+    bad_state[7] = None  # state_out
+    assert f(*bad_state) == INVALID
+    bad_dim = list(base)
+    bad_dim[12] = 96
+    assert f(*bad_dim) == UNSUPPORTED
+    misaligned = list(base)
+    misaligned[6] = FAKE + 4
+    assert f(*misaligned) == INVALID
+
+
+def test_recurrent_fwd_rejects(lib):
+    f = lib.kda_recurrent_fwd
+    base = [FAKE, FAKE, FAKE, BF16, FAKE, FAKE, None, None, FAKE, F32, None, None, None, 0, 1, 16, 2, 64, 64,
+            0.125, 1, None, BF16, None, 1e-5, None, None]
+    bad_states = list(base)
+    bad_states[10] = FAKE + 4  # misaligned per-token states
+    assert f(*bad_states) == INVALID
+    no_v = list(base)
+    no_v[2] = None
+    assert f(*no_v) == INVALID
+
+
+def test_gated_rmsnorm_rejects(lib):
+    f = lib.kda_gated_rmsnorm
+    assert f(FAKE, F32, FAKE, BF16, FAKE, ctypes.c_float(1e-5), FAKE, F32, ctypes.c_int64(4), 2, 100, None) == UNSUPPORTED
+    assert f(FAKE, F32, FAKE, BF16, FAKE, ctypes.c_float(0.0), FAKE, F32, ctypes.c_int64(4), 2, 128, None) == INVALID
+    assert f(None, F32, FAKE, BF16, FAKE, ctypes.c_float(1e-5), FAKE, F32, ctypes.c_int64(4), 2, 128, None) == INVALID
+    # in place (o == y) with different element sizes would corrupt the buffer
+    assert f(FAKE, BF16, FAKE, BF16, FAKE, ctypes.c_float(1e-5), FAKE, F32, ctypes.c_int64(4), 2, 128, None) == INVALID
+
+
+def test_launch_count_starts_at_zero(lib):
+    assert lib.kda_launch_count() == 0
+
+
+def test_python_binding_fails_loudly_without_gpu():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    import kimi_delta_attention_gated_gb300 as kda
+    q = torch.zeros(1, 4, 1, 32, dtype=torch.bfloat16)
+    with pytest.raises(Exception):
+        kda.chunk_fwd(q, q, q, torch.zeros(1, 4, 1, 32), torch.zeros(1, 4, 1), chunk=16)
