@@ -237,7 +237,9 @@ kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,
                              kda_dtype gate_dtype, const float *w, float eps, void *y,
                              kda_dtype y_dtype, int64_t rows, int H, int V, void *stream) {
     kda::g_err[0] = 0;
-    KDA_REQUIRE(o && gate && w && y, KDA_ERR_INVALID_ARG, "kda_gated_rmsnorm: o, gate, w and y must not be NULL");
+    KDA_REQUIRE((o && gate && y) || rows == 0, KDA_ERR_INVALID_ARG,
+                "kda_gated_rmsnorm: o, gate and y must not be NULL");
+    KDA_REQUIRE(w, KDA_ERR_INVALID_ARG, "kda_gated_rmsnorm: w must not be NULL");
     KDA_REQUIRE(dtype_ok(o_dtype) && dtype_ok(gate_dtype) && dtype_ok(y_dtype), KDA_ERR_UNSUPPORTED,
                 "kda_gated_rmsnorm: unsupported dtype");
     KDA_REQUIRE(rows >= 0 && H > 0, KDA_ERR_INVALID_ARG, "kda_gated_rmsnorm: need rows >= 0 and H > 0");

@@ -10,38 +10,41 @@
 // Chunk algebra (derived from the recurrence, exact in real arithmetic).  For one
 // (sequence, head) and a chunk of C = 64 tokens entering with state S [K x V]:
 //   G_i = sum_{s<=i} g_s (inclusive, per key channel), gamma = G_{C-1}
-//   Kd = k^ exp(G), Qd = q^ exp(G), Kg = k^ exp(gamma - G), Km = k^ exp(-G)
+//   Kd = k^ exp(G), Qd = q^ exp(G), Km = k^ exp(-G), Kg = k^ exp(gamma - G)
 //   A = strict_lower(diag(beta) Kd Km^T),  P = lower(Qd Km^T)          (grams)
-//   T = (I + A)^-1,  W = T diag(beta) Kd,  U = T diag(beta) V          (WY/UT form)
-//   D = U - W S,  O = Qd S + P D,  S' = Diag(exp gamma) S + Kg^T D
-// Km carries exp(-G) >= 1: it stays finite while the chunk's decay range
-// max_c(-gamma[c]) <= 80.  Chunks beyond that (g near the -5 lower bound on many
-// tokens) compute A and P exactly on CUDA cores with pairwise exponentials instead.
+//   T = (I + A)^-1                                                    (UT transform)
+//   R = V - Kd S,  D = T diag(beta) R   (= U - W S of the WY form, reassociated)
+//   O = Qd S + P D,  S' = Diag(exp gamma) S + Kg^T D
+// Km carries exp(-G) >= 1 and stays finite while the chunk's decay range
+// max_c(-gamma[c]) <= 80.  Chunks beyond it (g near the -5 lower bound on many
+// tokens) compute A and P exactly on CUDA cores with pairwise exponentials.
 //
 // Precision: every contraction runs on the tensor cores with bf16 operands split
-// into hi + lo parts (x = hi + lo, three MMAs hi*hi + hi*lo + lo*hi, fp32
-// accumulation), about 16 significant bits per operand; U uses two MMAs because v
-// is an exact bf16 input.  Plain bf16 operands miss the 5e-3 max-error bound by an
-// order of magnitude, plain tf32 sits right at it.
+// into hi + lo parts (x = hi + lo, three products hi*hi + hi*lo + lo*hi, fp32
+// accumulation), about 16 significant bits per operand.  V enters R through an MMA
+// with a bf16 identity (exact).  Plain bf16 operands miss the 5e-3 max-error bound
+// by an order of magnitude; plain tf32 sits right at it.
 //
-// Mapping: one CTA of 16 warps per (sequence, head).  Everything is transposed so
-// that the value dimension (128) is the MMA M dimension and TMEM lane:
-//   TMEM columns   [0,128)  S^T fp32 accumulator (lane v, column c)
-//                [128,192)  S^T hi, packed bf16 pairs (A operand of the state MMAs)
-//                [192,256)  S^T lo
-//                [256,320)  D^T accumulator (U^T then - S^T W^T)
-//                [320,384)  O^T accumulator
-//                [384,448)  gram accumulator [A ; P] (lanes 0-63 / 64-127), then
-//                           D^T hi [384,416) and D^T lo [416,448)
-//                [448,512)  W^T accumulator (lane c, column i)
-//   per chunk:  gram     [Kd;Qd] Km^T           M=128 N=64  K=128
-//               W^T    = Kd^T (T diag beta)^T   M=128 N=64  K=64
-//               U^T    = V^T (T diag beta)^T    M=128 N=64  K=64   (V tile by TMA)
-//               D^T   += S^T (-W^T)             M=128 N=64  K=128  (A from TMEM)
-//               O^T    = S^T Qd^T               M=128 N=64  K=128  (A from TMEM)
-//               O^T   += D^T P^T                M=128 N=64  K=64   (A from TMEM)
-//               S^T    = S^T Diag(exp gamma) + D^T Kg   M=128 N=128 K=64
-// The triangular inverse runs on CUDA cores (blocked, 16 x 16 diagonal blocks).
+// Mapping: one CTA of 16 warps per (sequence, head); thread 0 issues the TMA and
+// every tcgen05.mma.  A dependent M=128 MMA costs about 100 cycles whatever its N up
+// to 128, so the products are stacked along N (fewer, wider instructions), and the
+// R/O product is issued while warps 1-15 run the triangular solve (thread 0's warp
+// stalls on the MMA queue meanwhile).  Everything is transposed so that the value
+// dimension (128) is the MMA M dimension and the TMEM lane:
+//   TMEM columns   [0,64)   R^T accumulator, then D^T hi [0,32) / lo [32,64)
+//                 [64,128)  O^T accumulator
+//                [128,256)  S^T fp32 accumulator (lane v, column c)
+//                [256,320)  S^T hi, packed bf16 pairs (A operand of the state MMAs)
+//                [320,384)  S^T lo
+//                [384,512)  gram accumulator: [hi*hi + lo*hi | hi*lo], then R^T hi
+//                           [384,416) / lo [416,448) and the D^T accumulator [448,512)
+//   per chunk:
+//     gram   [-Kd;Qd] [Km_hi;Km_lo]^T  M=128 N=128 K=128, + [-Kd;Qd]_lo Km_hi^T N=64
+//     R^T  = V^T I (N=64), then [R|O]^T += S^T [-Kd;Qd]^T   N=128 K=128 (S^T in TMEM)
+//       ... meanwhile on CUDA cores: gram pass, T = (I + A)^-1, T diag(beta) tile
+//     D^T  = R^T (T diag beta)^T                           N=64  K=64  (R^T in TMEM)
+//     [O|S]^T += D^T [P^T | Kg]  (S^T pre-scaled by exp(gamma))  N=192 K=64
+// The next chunk's q, k and g are loaded into registers while the current one runs.
 #include <cuda.h>
 #include <math.h>
 #include <string.h>
@@ -54,51 +57,47 @@ namespace {
 
 using namespace tc;
 
-constexpr int C = 64;         // tokens per chunk
-constexpr int DK = 128;       // key dim
-constexpr int DV = 128;       // value dim
-constexpr int kThreads = 512; // 16 warps = 4 warpgroups
+constexpr int C = 64;            // tokens per chunk
+constexpr int DK = 128;          // key dim
+constexpr int DV = 128;          // value dim
+constexpr int kThreads = 512;    // 16 warps = 4 warpgroups
+constexpr int kSolve = 480;      // warps 1-15 run the triangular solve
 constexpr float kRangeMax = 80.f;
 constexpr uint32_t kPolls = 1u << 26;  // bound on every mbarrier wait
 
 // TMEM columns
-constexpr uint32_t T_S = 0, T_SH = 128, T_SL = 192, T_D = 256, T_O = 320, T_G = 384, T_DH = 384, T_DL = 416,
-                   T_W = 448;
+constexpr uint32_t T_R = 0, T_DH = 0, T_DL = 32, T_O = 64, T_S = 128, T_SH = 256, T_SL = 320, T_G = 384,
+                   T_RH = 384, T_RL = 416, T_D = 448;
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t S_V = 0;             // V tile, two TMA boxes of 64 tokens x 64 values (16 KB)
-constexpr uint32_t S_KQH = 16384;       // [Kd ; Qd] hi, 128 rows x 128 (32 KB)
-constexpr uint32_t S_KQL = 49152;       // [Kd ; Qd] lo
-constexpr uint32_t S_KMH = 81920;       // Km hi (then Kg hi), 64 rows x 128 (16 KB)
-constexpr uint32_t S_KML = 98304;       // Km lo (then Kg lo)
-constexpr uint32_t S_TBH = 114688;      // T diag(beta) hi, 64 x 64 (8 KB)
-constexpr uint32_t S_TBL = 122880;
-constexpr uint32_t S_PH = 131072;       // P hi 64 x 64
-constexpr uint32_t S_PL = 139264;
-constexpr uint32_t S_WH = 147456;       // W, rows c x 64 i (16 KB)
-constexpr uint32_t S_WL = 163840;
+constexpr uint32_t S_KQH = 16384;       // [-Kd ; Qd] hi, 128 rows x 128 (32 KB)
+constexpr uint32_t S_KQL = 49152;       // [-Kd ; Qd] lo
+constexpr uint32_t S_KM = 81920;        // [Km hi ; Km lo], 128 rows x 128 (32 KB)
+constexpr uint32_t S_PKGH = 114688;     // [P^T | Kg] hi, 64 rows (j) x 192 (24 KB), MN-major B
+constexpr uint32_t S_PKGL = 139264;     // [P^T | Kg] lo
+constexpr uint32_t S_TBH = 163840;      // T diag(beta) hi, 64 x 64 (8 KB)
+constexpr uint32_t S_TBL = 172032;
+constexpr uint32_t S_ID = 180224;       // bf16 identity 64 x 64 (8 KB)
 constexpr int AP = 68;                  // fp32 pitch of A and T
-constexpr uint32_t S_A = 180224;        // A fp32 [64][AP] (17408 B)
+constexpr uint32_t S_A = 188416;        // A fp32 [64][AP] (17408 B)
 constexpr uint32_t S_T = S_A + 64 * AP * 4;  // T fp32 [64][AP]
 constexpr uint32_t S_SMALL = S_T + 64 * AP * 4;
 // small buffers (floats)
-constexpr uint32_t F_GEXP = 0;    // exp(gamma)   [128]
-constexpr uint32_t F_GNEG = 128;  // exp(-gamma)  [128]
-constexpr uint32_t F_GAM = 256;   // gamma        [128]
-constexpr uint32_t F_BETA = 384;  // beta         [64]
-constexpr uint32_t F_RQ = 448;    // q scale per token (norm * scale) [64]
-constexpr uint32_t F_RK = 512;    // k norm per token [64]
-constexpr uint32_t F_RED = 576;   // norm partials [4 wg][4 quarters][16]
-constexpr uint32_t F_END = 832;
-constexpr uint32_t S_BARS = S_SMALL + F_END * 4;   // 2 mbarriers + tmem slot + flags
+constexpr uint32_t F_BETA = 0;    // beta [64]
+constexpr uint32_t F_RQ = 64;     // q scale per token (norm * scale) [64]
+constexpr uint32_t F_RK = 128;    // k norm per token [64]
+constexpr uint32_t F_GEXP = 192;  // exp(gamma) [128]
+constexpr uint32_t F_RED = 320;   // norm partials [4 wg][4 quarters][16]
+constexpr uint32_t F_END = 576;
+constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 6 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = S_BARS + 64 + 1024;  // + alignment slack
 // scan scratch aliases T (free during prep): [16 warps][128] floats
 constexpr uint32_t S_SCAN = S_T;
-// fallback scratch (only for chunks beyond the decay range): G fp32 [64][128] in the
-// W tiles, raw q and k bf16 [64][128] in the T diag(beta) and Km hi tiles
-constexpr uint32_t S_FB_G = S_WH, S_FB_Q = S_TBH, S_FB_K = S_KMH;
+// fallback scratch: G fp32 [64][128] in the Km tile (Km is not used then)
+constexpr uint32_t S_FB_G = S_KM;
 
-static_assert(S_A % 16 == 0 && S_SMALL % 16 == 0, "alignment");
+static_assert(S_A % 1024 == 0 && S_SMALL % 16 == 0, "alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Set by a CTA whose bounded wait on the tensor core or the TMA gave up; that CTA
@@ -113,6 +112,9 @@ struct TcParams {
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// barrier over warps 1-15 (the triangular solve, while warp 0 issues MMAs)
+__device__ __forceinline__ void tbar() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
 
 // Writes 4 consecutive columns (col % 4 == 0) of one row of a SW128 tile as hi/lo.
 __device__ __forceinline__ void st_tile4(uint32_t hi_base, uint32_t lo_base, uint32_t rows, uint32_t row,
@@ -136,6 +138,105 @@ __device__ __forceinline__ void st_tile8(uint32_t hi_base, uint32_t lo_base, uin
     st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
 }
 
+// P[i][j] into the P^T block (rows j, columns i) of the [P^T | Kg] tiles, hi and lo.
+__device__ __forceinline__ void st_pt(uint8_t *sm, int i, int j, float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+    const uint32_t off = sw128_off(j, i, 64);
+    *reinterpret_cast<__nv_bfloat16 *>(sm + S_PKGH + off) = h;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + S_PKGL + off) = l;
+}
+
+// hi*hi, hi*lo, lo*hi: (A part, B part) of the three products of a split operand pair
+__device__ __forceinline__ int combo_a(int cb) { return cb == 2 ? 1 : 0; }
+__device__ __forceinline__ int combo_b(int cb) { return cb == 1 ? 1 : 0; }
+
+// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 at block distance D (I - J = D):
+// X = sum_{K=J}^{I-1} A_IK T_KJ (kept in A's unused upper block (J, I)), then
+// T_IJ = -T_II X.  Each 2 x 2 output tile is shared by S adjacent lanes that split
+// the inner sum and combine it with shuffles.
+template <int D>
+__device__ __forceinline__ void tri_level(float *Asm, float *Tsm, int ctid) {
+    constexpr int NP = 4 - D;
+    constexpr int S = D == 3 ? 4 : 2;
+    constexpr int ACTIVE = NP * 64 * S;
+    const int s = ctid % S, e = (ctid / S) & 63, pr = ctid / (S * 64);
+    const int I = D + pr, J = I - D, r = (e >> 3) * 2, cc = (e & 7) * 2;
+    if (ctid < ACTIVE) {
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+#pragma unroll
+        for (int st = 0; st < 16 * D / S; ++st) {
+            const int krow = 16 * J + s + S * st;
+            const float a0 = Asm[(16 * I + r) * AP + krow], a1 = Asm[(16 * I + r + 1) * AP + krow];
+            const float2 t = *reinterpret_cast<const float2 *>(Tsm + krow * AP + 16 * J + cc);
+            x00 = fmaf(a0, t.x, x00);
+            x01 = fmaf(a0, t.y, x01);
+            x10 = fmaf(a1, t.x, x10);
+            x11 = fmaf(a1, t.y, x11);
+        }
+#pragma unroll
+        for (int o = 1; o < S; o <<= 1) {
+            x00 += __shfl_xor_sync(0xffffffffu, x00, o);
+            x01 += __shfl_xor_sync(0xffffffffu, x01, o);
+            x10 += __shfl_xor_sync(0xffffffffu, x10, o);
+            x11 += __shfl_xor_sync(0xffffffffu, x11, o);
+        }
+        if (s == 0) {
+            *reinterpret_cast<float2 *>(Asm + (16 * J + r) * AP + 16 * I + cc) = make_float2(x00, x01);
+            *reinterpret_cast<float2 *>(Asm + (16 * J + r + 1) * AP + 16 * I + cc) = make_float2(x10, x11);
+        }
+    }
+    tbar();
+    if (ctid < ACTIVE) {
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll
+        for (int st = 0; st < 16 / S; ++st) {
+            const int t = s + S * st;
+            const float a0 = Tsm[(16 * I + r) * AP + 16 * I + t], a1 = Tsm[(16 * I + r + 1) * AP + 16 * I + t];
+            const float2 x = *reinterpret_cast<const float2 *>(Asm + (16 * J + t) * AP + 16 * I + cc);
+            y00 = fmaf(a0, x.x, y00);
+            y01 = fmaf(a0, x.y, y01);
+            y10 = fmaf(a1, x.x, y10);
+            y11 = fmaf(a1, x.y, y11);
+        }
+#pragma unroll
+        for (int o = 1; o < S; o <<= 1) {
+            y00 += __shfl_xor_sync(0xffffffffu, y00, o);
+            y01 += __shfl_xor_sync(0xffffffffu, y01, o);
+            y10 += __shfl_xor_sync(0xffffffffu, y10, o);
+            y11 += __shfl_xor_sync(0xffffffffu, y11, o);
+        }
+        if (s == 0) {
+            *reinterpret_cast<float2 *>(Tsm + (16 * I + r) * AP + 16 * J + cc) = make_float2(-y00, -y01);
+            *reinterpret_cast<float2 *>(Tsm + (16 * I + r + 1) * AP + 16 * J + cc) = make_float2(-y10, -y11);
+        }
+    }
+    tbar();
+}
+
+// Loads of one chunk's q, k, g for this thread's 4 tokens x 4 key channels.
+struct ChunkRegs {
+    float4 g[4];
+    uint2 q[4], k[4];
+};
+
+__device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, int bos, int t0, int cn, int h,
+                                           int warp, int l4) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = warp * 4 + r;
+        cr.g[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        cr.q[r] = make_uint2(0u, 0u);
+        cr.k[r] = make_uint2(0u, 0u);
+        if (i < cn) {
+            const size_t hk = ((size_t)(bos + t0 + i) * p.H + h) * DK + l4;
+            cr.g[r] = __ldg(reinterpret_cast<const float4 *>(p.g + hk));
+            cr.q[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + hk));
+            cr.k[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ TcParams tp) {
     const SeqParams &p = tp.p;
@@ -145,13 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *fs = reinterpret_cast<float *>(sm + S_SMALL);
     float *Asm = reinterpret_cast<float *>(sm + S_A);
     float *Tsm = reinterpret_cast<float *>(sm + S_T);
-    uint64_t *mma_bar = reinterpret_cast<uint64_t *>(sm + S_BARS);
-    uint64_t *tma_bar = mma_bar + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 16);
+    // one barrier per tensor-core group, each completing exactly once per chunk
+    uint64_t *bar_g = reinterpret_cast<uint64_t *>(sm + S_BARS);  // gram
+    uint64_t *bar_r = bar_g + 1;                                    // R and O
+    uint64_t *bar_d = bar_g + 2;                                    // D
+    uint64_t *bar_s = bar_g + 3;                                    // O and S updates
+    uint64_t *tma_bar = bar_g + 4;                                  // V tile
+    uint64_t *drain_bar = bar_g + 5;                                // drain after a failure
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wg = warp >> 2, wq = warp & 3;
     const int m = wq * 32 + lane;  // TMEM lane this thread reads/writes
+    const int l4 = lane * 4;       // this thread's 4 key channels in the prep phase
     const int H = p.H;
     int n = blockIdx.x / H;
     const int h = blockIdx.x % H;
@@ -159,31 +266,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int unit = n * H + h;
     int bos, len;
     seq_range(p, n, bos, len);
+    const int nchunks = (len + C - 1) / C;
+
+    // first chunk's inputs are in flight while the CTA sets up
+    ChunkRegs cr;
+    load_chunk(p, cr, bos, 0, min(C, len), h, warp, l4);
 
     if (tid == 0) {
-        mbar_init(mma_bar, 1);
-        mbar_init(tma_bar, 1);
+        for (int b = 0; b < 6; ++b) mbar_init(bar_g + b, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    // bf16 identity tile (K-major, rows i, columns j)
+    {
+        const int i = tid >> 3, j0 = (tid & 7) * 8;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (i >= j0 && i < j0 + 8) w[(i - j0) >> 1] = (i & 1) ? 0x3F800000u : 0x00003F80u;
+        st_shared_v4(sb + S_ID + sw128_off(i, j0, 64), w[0], w[1], w[2], w[3]);
+    }
+    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tb = *tmem_slot;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    uint32_t mma_phase = 0, tma_phase = 0;
-    bool failed = false;
 
-    // ---- initial state -> S^T accumulator and its hi/lo operand copy
-    {
+    auto issue_v = [&](int chunk) {
+        mbar_arrive_expect_tx(tma_bar, 16384);
+        tma_load_3d(sb + S_V, &tmap_v, tma_bar, 0, h, bos + chunk * C);
+        tma_load_3d(sb + S_V + 8192, &tmap_v, tma_bar, 64, h, bos + chunk * C);
+    };
+    if (tid == 0 && nchunks > 0) issue_v(0);
+
+    {  // initial state -> S^T accumulator and its hi/lo copy; O^T = 0
         const int c0 = wg * 32;
         float s[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-            s[c] = p.s0 ? p.s0[((size_t)unit * DK + c0 + c) * DV + m] : 0.f;
+        for (int c = 0; c < 32; ++c) s[c] = p.s0 ? p.s0[((size_t)unit * DK + c0 + c) * DV + m] : 0.f;
         uint32_t r[16], hi[16], lo[16];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -192,49 +314,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tb + lane_off + T_S + c0 + half * 16, r);
         }
 #pragma unroll
-        for (int c = 0; c < 16; ++c) split2(s[2 * c], s[2 * c + 1], hi[c], lo[c]);
+        for (int c = 0; c < 16; ++c) {
+            split2(s[2 * c], s[2 * c + 1], hi[c], lo[c]);
+            r[c] = 0u;
+        }
         tmem_st16(tb + lane_off + T_SH + c0 / 2, hi);
         tmem_st16(tb + lane_off + T_SL + c0 / 2, lo);
+        tmem_st16(tb + lane_off + T_O + wg * 16, r);
         tmem_wait_st();
     }
 
-    const int nchunks = (len + C - 1) / C;
-    auto issue_v = [&](int chunk) {
-        mbar_arrive_expect_tx(tma_bar, 16384);
-        tma_load_3d(sb + S_V, &tmap_v, tma_bar, 0, h, bos + chunk * C);
-        tma_load_3d(sb + S_V + 8192, &tmap_v, tma_bar, 64, h, bos + chunk * C);
-    };
-    if (tid == 0 && nchunks > 0) issue_v(0);
-
-    // all threads wait on the MMA barrier; a timeout marks the CTA failed
-    auto mma_wait = [&]() {
-        const bool ok = mbar_wait(mma_bar, mma_phase, kPolls);
-        mma_phase ^= 1;
+    auto wait_group = [&](uint64_t *bar, int parity) {
+        const bool ok = mbar_wait(bar, (uint32_t)parity, kPolls);
         fence_after_sync();
         return ok;
     };
 
-    for (int ch = 0; ch < nchunks && !failed; ++ch) {
+    int failed = 0;
+    for (int ch = 0; ch < nchunks; ++ch) {
+        const int par = ch & 1;
         const int t0 = ch * C;
         const int cn = min(C, len - t0);
-        // ================= prep: loads, norms, cumulative decay, operand tiles
-        const int l4 = lane * 4;  // this thread's 4 key channels
+        int out_of_range = 0;
+        // ================= prep: norms, cumulative decay, operand tiles
         float g4[4][4], q4[4][4], k4[4][4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int i = warp * 4 + r;
-            const bool valid = i < cn;
-            const size_t hk = ((size_t)(bos + t0 + i) * H + h) * DK + l4;
-            float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-            uint2 qv = make_uint2(0u, 0u), kv = make_uint2(0u, 0u);
-            if (valid) {
-                gv = __ldg(reinterpret_cast<const float4 *>(p.g + hk));
-                qv = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + hk));
-                kv = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
-            }
-            g4[r][0] = gv.x; g4[r][1] = gv.y; g4[r][2] = gv.z; g4[r][3] = gv.w;
-            q4[r][0] = bf16lo(qv.x); q4[r][1] = bf16hi(qv.x); q4[r][2] = bf16lo(qv.y); q4[r][3] = bf16hi(qv.y);
-            k4[r][0] = bf16lo(kv.x); k4[r][1] = bf16hi(kv.x); k4[r][2] = bf16lo(kv.y); k4[r][3] = bf16hi(kv.y);
+            g4[r][0] = cr.g[r].x; g4[r][1] = cr.g[r].y; g4[r][2] = cr.g[r].z; g4[r][3] = cr.g[r].w;
+            q4[r][0] = bf16lo(cr.q[r].x); q4[r][1] = bf16hi(cr.q[r].x);
+            q4[r][2] = bf16lo(cr.q[r].y); q4[r][3] = bf16hi(cr.q[r].y);
+            k4[r][0] = bf16lo(cr.k[r].x); k4[r][1] = bf16hi(cr.k[r].x);
+            k4[r][2] = bf16lo(cr.k[r].y); k4[r][3] = bf16hi(cr.k[r].y);
         }
         float rq[4], rk[4];
 #pragma unroll
@@ -256,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fs[F_RQ + i] = rq[lane];
             fs[F_RK + i] = rk[lane];
         }
-        // local inclusive prefix over the thread's 4 tokens; warp totals to the scan buffer
+        // inclusive prefix over the thread's 4 tokens; warp totals to the scan buffer
 #pragma unroll
         for (int r = 1; r < 4; ++r)
 #pragma unroll
@@ -264,320 +374,324 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *scan = reinterpret_cast<float *>(sm + S_SCAN);
         *reinterpret_cast<float4 *>(scan + warp * 128 + l4) = make_float4(g4[3][0], g4[3][1], g4[3][2], g4[3][3]);
         __syncthreads();
-        if (tid < 128) {  // exclusive scan of the 16 warp totals, per channel
-            float acc = 0.f;
+        float o4[4] = {0.f, 0.f, 0.f, 0.f}, gam[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int w = 0; w < 16; ++w) {
-                const float t = scan[w * 128 + tid];
-                scan[w * 128 + tid] = acc;
-                acc += t;
+        for (int w = 0; w < 16; ++w) {  // offset of this warp's tokens and the chunk total, per channel
+            const float4 t = *reinterpret_cast<const float4 *>(scan + w * 128 + l4);
+            const float tt[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (w < warp) o4[c] += tt[c];
+                gam[c] += tt[c];
             }
-            fs[F_GAM + tid] = acc;
-            fs[F_GEXP + tid] = __expf(acc);
-            fs[F_GNEG + tid] = __expf(-acc);
         }
-        const int fallback = __syncthreads_or(tid < 128 && -fs[F_GAM + tid] > kRangeMax ? 1 : 0);
-        // (the predicate above reads gamma written before the barrier by the same thread)
-        float kg[4][4];
-        {
-            const float4 off = *reinterpret_cast<const float4 *>(scan + warp * 128 + l4);
-            const float4 gam = *reinterpret_cast<const float4 *>(fs + F_GAM + l4);
-            const float4 gneg = *reinterpret_cast<const float4 *>(fs + F_GNEG + l4);
-            const float offs[4] = {off.x, off.y, off.z, off.w};
-            const float gams[4] = {gam.x, gam.y, gam.z, gam.w};
-            const float gnegs[4] = {gneg.x, gneg.y, gneg.z, gneg.w};
+        float egam[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = warp * 4 + r;
-                float kd[4], qd[4], km[4], G[4];
+        for (int c = 0; c < 4; ++c) {
+            egam[c] = __expf(gam[c]);
+            out_of_range |= (-gam[c] > kRangeMax);
+        }
+        if (warp == 0) *reinterpret_cast<float4 *>(fs + F_GEXP + l4) = make_float4(egam[0], egam[1], egam[2], egam[3]);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    G[c] = offs[c] + g4[r][c];
-                    const float eG = __expf(G[c]);
-                    const float kh = k4[r][c] * rk[r], qh = q4[r][c] * rq[r];
-                    kd[c] = kh * eG;
-                    qd[c] = qh * eG;
-                    kg[r][c] = kh * __expf(gams[c] - G[c]);
-                    km[c] = kg[r][c] * gnegs[c];
-                }
-                st_tile4(sb + S_KQH, sb + S_KQL, 128, i, l4, kd[0], kd[1], kd[2], kd[3]);
-                st_tile4(sb + S_KQH, sb + S_KQL, 128, 64 + i, l4, qd[0], qd[1], qd[2], qd[3]);
-                if (!fallback) {
-                    st_tile4(sb + S_KMH, sb + S_KML, 64, i, l4, km[0], km[1], km[2], km[3]);
-                } else {
-                    float *Gs = reinterpret_cast<float *>(sm + S_FB_G);
-                    *reinterpret_cast<float4 *>(Gs + i * 128 + l4) = make_float4(G[0], G[1], G[2], G[3]);
-                    __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(sm + S_FB_Q);
-                    __nv_bfloat16 *ks = reinterpret_cast<__nv_bfloat16 *>(sm + S_FB_K);
+        for (int r = 0; r < 4; ++r) {
+            const int i = warp * 4 + r;
+            float kd[4], qd[4], km[4], kg[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        qs[i * 128 + l4 + c] = __float2bfloat16_rn(q4[r][c]);  // exact: inputs are bf16
-                        ks[i * 128 + l4 + c] = __float2bfloat16_rn(k4[r][c]);
-                    }
-                }
+            for (int c = 0; c < 4; ++c) {
+                const float G = o4[c] + g4[r][c];
+                const float eG = __expf(G);
+                const float kh = k4[r][c] * rk[r];
+                kd[c] = -kh * eG;
+                qd[c] = q4[r][c] * rq[r] * eG;
+                km[c] = kh * __expf(-G);
+                kg[c] = km[c] * egam[c];
             }
+            st_tile4(sb + S_KQH, sb + S_KQL, 128, i, l4, kd[0], kd[1], kd[2], kd[3]);
+            st_tile4(sb + S_KQH, sb + S_KQL, 128, 64 + i, l4, qd[0], qd[1], qd[2], qd[3]);
+            {
+                uint32_t h0, l0, h1, l1;
+                split2(km[0], km[1], h0, l0);
+                split2(km[2], km[3], h1, l1);
+                st_shared_v2(sb + S_KM + sw128_off(i, l4, 128), h0, h1);
+                st_shared_v2(sb + S_KM + sw128_off(64 + i, l4, 128), l0, l1);
+            }
+            st_tile4(sb + S_PKGH, sb + S_PKGL, 64, i, 64 + l4, kg[0], kg[1], kg[2], kg[3]);
         }
         fence_async_smem();
-        __syncthreads();
+        fence_before_sync();  // the previous state pass (or the initial state) wrote TMEM
+        // ---- operand tiles of this chunk and S(n-1) are ready
+        const int fallback = __syncthreads_or(out_of_range);
 
-        // ================= grams A (strict lower, beta-scaled) and P (lower)
-        if (!fallback) {
-            if (tid == 0) {
-                fence_after_sync();
-                const uint32_t idesc = idesc_bf16(128, 64, false, false);
-                const uint32_t ah[2] = {sb + S_KQH, sb + S_KQL}, bh[2] = {sb + S_KMH, sb + S_KML};
-                const int combos[3][2] = {{0, 0}, {0, 1}, {1, 0}};
-                int first = 1;
-                for (int cb = 0; cb < 3; ++cb)
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t koff = (s >> 2) * 0u + (s & 3) * 32u;
-                        const uint64_t ad = sdesc(ah[combos[cb][0]] + (s >> 2) * 16384 + koff, 16, 1024);
-                        const uint64_t bd = sdesc(bh[combos[cb][1]] + (s >> 2) * 8192 + koff, 16, 1024);
-                        mma_ss(tb + T_G, ad, bd, idesc, first ? 0u : 1u);
-                        first = 0;
-                    }
-                mma_commit(mma_bar);
-            }
-            __syncwarp();
-            if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-            {
-                uint32_t r[16];
-                tmem_ld16(tb + lane_off + T_G + wg * 16, r);
-                tmem_wait_ld();
-                const int j0 = wg * 16;
-                if (m < 64) {
-                    const int i = m;
-                    const float b = fs[F_BETA + i];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        Asm[i * AP + j0 + c] = (j0 + c < i) ? b * __uint_as_float(r[c]) : 0.f;
-                } else {
-                    const int i = m - 64;
-                    float x[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] = (j0 + c <= i) ? __uint_as_float(r[c]) : 0.f;
-                    st_tile8(sb + S_PH, sb + S_PL, 64, i, j0, x);
-                    st_tile8(sb + S_PH, sb + S_PL, 64, i, j0 + 8, x + 8);
+        // ================= gram [-Kd;Qd] [Km_hi;Km_lo]^T (+ lo x hi)
+        if (tid == 0) {
+            fence_after_sync();
+            if (!fallback) {
+                const uint32_t id128 = idesc_bf16(128, 128, false, false);
+                const uint32_t id64 = idesc_bf16(128, 64, false, false);
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {  // [-Kd;Qd]_hi x [Km_hi;Km_lo]^T
+                    const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_ss(tb + T_G, sdesc(sb + S_KQH + koff, 16, 1024), sdesc(sb + S_KM + koff, 16, 1024), id128,
+                           s ? 1u : 0u);
                 }
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {  // [-Kd;Qd]_lo x Km_hi^T into the first half
+                    const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_ss(tb + T_G, sdesc(sb + S_KQL + koff, 16, 1024), sdesc(sb + S_KM + koff, 16, 1024), id64, 1u);
+                }
+            }
+            mma_commit(bar_g);  // an empty commit on fallback chunks
+        }
+        __syncwarp();
+        // start loading the next chunk while waiting for the gram
+        if (ch + 1 < nchunks) load_chunk(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
+        if (!wait_group(bar_g, par)) failed = 1;
+        if (!fallback) {
+            uint32_t r1[16], r2[16];
+            tmem_ld16(tb + lane_off + T_G + wg * 16, r1);
+            tmem_ld16(tb + lane_off + T_G + 64 + wg * 16, r2);
+            tmem_wait_ld();
+            const int j0 = wg * 16;
+            if (m < 64) {
+                const int i = m;
+                const float b = -fs[F_BETA + i];  // gram rows hold -Kd Km^T
+                float4 *dst = reinterpret_cast<float4 *>(Asm + i * AP + j0);
+#pragma unroll
+                for (int c = 0; c < 16; c += 4) {
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        x[e] = (j0 + c + e < i) ? b * (__uint_as_float(r1[c + e]) + __uint_as_float(r2[c + e])) : 0.f;
+                    dst[c / 4] = make_float4(x[0], x[1], x[2], x[3]);
+                }
+            } else {
+                const int i = m - 64;
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    st_pt(sm, i, j0 + c, (j0 + c <= i) ? __uint_as_float(r1[c]) + __uint_as_float(r2[c]) : 0.f);
             }
         } else {
             // exact grams with pairwise exponentials (decay range too wide for Km)
-            const float *Gs = reinterpret_cast<const float *>(sm + S_FB_G);
-            const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + S_FB_Q);
-            const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + S_FB_K);
+            float *Gs = reinterpret_cast<float *>(sm + S_FB_G);
+            const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(p.q);
+            const __nv_bfloat16 *kgl = reinterpret_cast<const __nv_bfloat16 *>(p.k);
+            if (tid < 128) {  // G for every token and channel, from the inputs again
+                float acc = 0.f;
+                for (int i = 0; i < C; ++i) {
+                    if (i < cn) acc += p.g[((size_t)(bos + t0 + i) * H + h) * DK + tid];
+                    Gs[i * 128 + tid] = acc;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {  // Kg from the exact G (the fast formula overflows here)
+                const int i = warp * 4 + r;
+                float kg[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float kv = i < cn ? __bfloat162float(kgl[((size_t)(bos + t0 + i) * H + h) * DK + l4 + c]) : 0.f;
+                    kg[c] = kv * fs[F_RK + i] * __expf(Gs[63 * 128 + l4 + c] - Gs[i * 128 + l4 + c]);
+                }
+                st_tile4(sb + S_PKGH, sb + S_PKGL, 64, i, 64 + l4, kg[0], kg[1], kg[2], kg[3]);
+            }
             float *Pf = Tsm;  // P in fp32, converted to the tile below
-            for (int pr = warp; pr < C * C; pr += 16) {
-                const int i = pr >> 6, j = pr & 63;
-                float a = 0.f, b = 0.f;
-                if (j <= i) {
-                    for (int c = lane; c < DK; c += 32) {
-                        const float e = __expf(Gs[i * 128 + c] - Gs[j * 128 + c]);
-                        const float kj = __bfloat162float(ks[j * 128 + c]) * e;
-                        a = fmaf(__bfloat162float(ks[i * 128 + c]), kj, a);
-                        b = fmaf(__bfloat162float(qs[i * 128 + c]), kj, b);
+            for (int i = warp; i < C; i += 16) {
+                const size_t ri = ((size_t)(bos + t0 + i) * H + h) * DK;
+                float qi[4], ki[4], gi[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int ch_ = lane + 32 * c;
+                    qi[c] = i < cn ? __bfloat162float(qg[ri + ch_]) : 0.f;
+                    ki[c] = i < cn ? __bfloat162float(kgl[ri + ch_]) : 0.f;
+                    gi[c] = Gs[i * 128 + ch_];
+                }
+                for (int j = 0; j <= i; ++j) {
+                    const size_t rj = ((size_t)(bos + t0 + j) * H + h) * DK;
+                    float a = 0.f, b = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int ch_ = lane + 32 * c;
+                        const float kj = (j < cn ? __bfloat162float(kgl[rj + ch_]) : 0.f) * __expf(gi[c] - Gs[j * 128 + ch_]);
+                        a = fmaf(ki[c], kj, a);
+                        b = fmaf(qi[c], kj, b);
                     }
                     a = warp_sum(a) * fs[F_RK + i] * fs[F_RK + j];
                     b = warp_sum(b) * fs[F_RQ + i] * fs[F_RK + j];
+                    if (lane == 0) {
+                        Asm[i * AP + j] = (j < i) ? fs[F_BETA + i] * a : 0.f;
+                        Pf[i * AP + j] = b;
+                    }
                 }
-                if (lane == 0) {
-                    Asm[i * AP + j] = (j < i) ? fs[F_BETA + i] * a : 0.f;
-                    Pf[i * AP + j] = (j <= i) ? b : 0.f;
-                }
+                if (lane == 0)
+                    for (int j = i + 1; j < C; ++j) {
+                        Asm[i * AP + j] = 0.f;
+                        Pf[i * AP + j] = 0.f;
+                    }
             }
             __syncthreads();
             {
                 const int i = tid >> 3, j0 = (tid & 7) * 8;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) st_pt(sm, i, j0 + c, Pf[i * AP + j0 + c]);
+            }
+        }
+        __syncthreads();
+
+        if (tid == 0) {
+            // ================= R^T = V^T I + S^T (-Kd)^T, O^T = S^T Qd^T (while warps 1-15 solve T)
+            if (!mbar_wait(tma_bar, (uint32_t)par, kPolls)) failed = 1;
+            fence_after_sync();
+            const uint32_t id_mn = idesc_bf16(128, 64, true, false);
+#pragma unroll 1
+            for (int s = 0; s < 4; ++s)
+                mma_ss(tb + T_R, sdesc(sb + S_V + s * 2048, 8192, 1024), sdesc(sb + S_ID + s * 32, 16, 1024), id_mn,
+                       s ? 1u : 0u);
+            const uint32_t id128 = idesc_bf16(128, 128, false, false);
+#pragma unroll
+            for (int cb = 0; cb < 3; ++cb)
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t a = tb + (combo_a(cb) ? T_SL : T_SH) + s * 8;
+                    const uint32_t bk = (combo_b(cb) ? sb + S_KQL : sb + S_KQH) + (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_ts(tb + T_R, a, sdesc(bk, 16, 1024), id128, 1u);
+                }
+            mma_commit(bar_r);
+        } else if (warp > 0) {
+            // ================= T = (I + A)^-1, blocked with 16 x 16 diagonal blocks (warps 1-15)
+            const int ctid = tid - 32;
+            if (tid >= kThreads - 64) {
+                const int t = tid - (kThreads - 64), b = t >> 4, c = t & 15, o = 16 * b;
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < i; ++j) acc = fmaf(Asm[(o + i) * AP + o + j], x[j], acc);
+                    x[i] = (i < c) ? 0.f : (i == c ? 1.f : -acc);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Tsm[(o + i) * AP + o + c] = x[i];
+            }
+            tbar();
+            tri_level<1>(Asm, Tsm, ctid);
+            tri_level<2>(Asm, Tsm, ctid);
+            tri_level<3>(Asm, Tsm, ctid);
+            for (int it = ctid; it < 64 * 8; it += kSolve) {  // T diag(beta) -> hi/lo tile (rows i, K = j)
+                const int i = it >> 3, j0 = (it & 7) * 8;
                 float x[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) x[c] = Pf[i * AP + j0 + c];
-                st_tile8(sb + S_PH, sb + S_PL, 64, i, j0, x);
+                for (int c = 0; c < 8; ++c) x[c] = (j0 + c <= i) ? Tsm[i * AP + j0 + c] * fs[F_BETA + j0 + c] : 0.f;
+                st_tile8(sb + S_TBH, sb + S_TBL, 64, i, j0, x);
             }
-            __syncthreads();
-        }
-        // Kg into the Km tiles (the gram that read Km has completed)
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            st_tile4(sb + S_KMH, sb + S_KML, 64, warp * 4 + r, lane * 4, kg[r][0], kg[r][1], kg[r][2], kg[r][3]);
-        __syncthreads();
-
-        // ================= T = (I + A)^-1, blocked with 16 x 16 diagonal blocks
-        if (tid < 64) {
-            const int b = tid >> 4, c = tid & 15, o = 16 * b;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 0; j < i; ++j) acc = fmaf(Asm[(o + i) * AP + o + j], x[j], acc);
-                x[i] = (i < c) ? 0.f : (i == c ? 1.f : -acc);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tsm[(o + i) * AP + o + c] = x[i];
-        }
-        __syncthreads();
-        for (int d = 1; d < 4; ++d) {
-            const int np = 4 - d;
-            for (int it = tid; it < np * 256; it += kThreads) {  // X = sum_K A_IK T_KJ -> A's upper block (J, I)
-                const int I = d + (it >> 8), J = I - d, e = it & 255, r = e >> 4, cc = e & 15;
-                float acc = 0.f;
-                for (int Kb = J; Kb < I; ++Kb)
-#pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        acc = fmaf(Asm[(16 * I + r) * AP + 16 * Kb + t], Tsm[(16 * Kb + t) * AP + 16 * J + cc], acc);
-                Asm[(16 * J + r) * AP + 16 * I + cc] = acc;
-            }
-            __syncthreads();
-            for (int it = tid; it < np * 256; it += kThreads) {  // T_IJ = -T_II X
-                const int I = d + (it >> 8), J = I - d, e = it & 255, r = e >> 4, cc = e & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    acc = fmaf(Tsm[(16 * I + r) * AP + 16 * I + t], Asm[(16 * J + t) * AP + 16 * I + cc], acc);
-                Tsm[(16 * I + r) * AP + 16 * J + cc] = -acc;
-            }
-            __syncthreads();
-        }
-        {  // T diag(beta) -> hi/lo tile (rows i, K = j)
-            const int i = tid >> 3, j0 = (tid & 7) * 8;
-            float x[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = (j0 + c <= i) ? Tsm[i * AP + j0 + c] * fs[F_BETA + j0 + c] : 0.f;
-            st_tile8(sb + S_TBH, sb + S_TBL, 64, i, j0, x);
-        }
-        fence_async_smem();
-        __syncthreads();
-
-        // ================= W^T = Kd^T (T diag beta)^T ; U^T = V^T (T diag beta)^T
-        if (tid == 0) {
-            const bool v_ok = mbar_wait(tma_bar, tma_phase, kPolls);
-            if (!v_ok) failed = true;
-            fence_after_sync();
-            const uint32_t idesc_w = idesc_bf16(128, 64, true, false);
-            const uint32_t kq[2] = {sb + S_KQH, sb + S_KQL}, tbt[2] = {sb + S_TBH, sb + S_TBL};
-            const int combos[3][2] = {{0, 0}, {0, 1}, {1, 0}};
-            int first = 1;
-            for (int cb = 0; cb < 3; ++cb)
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ad = sdesc(kq[combos[cb][0]] + s * 2048, 16384, 1024);
-                    const uint64_t bd = sdesc(tbt[combos[cb][1]] + s * 32, 16, 1024);
-                    mma_ss(tb + T_W, ad, bd, idesc_w, first ? 0u : 1u);
-                    first = 0;
-                }
-            first = 1;
-            for (int cb = 0; cb < 2; ++cb)
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ad = sdesc(sb + S_V + s * 2048, 8192, 1024);
-                    const uint64_t bd = sdesc(tbt[cb] + s * 32, 16, 1024);
-                    mma_ss(tb + T_D, ad, bd, idesc_w, first ? 0u : 1u);
-                    first = 0;
-                }
-            mma_commit(mma_bar);
-        }
-        tma_phase ^= 1;
-        __syncwarp();
-        if (__syncthreads_or(!mma_wait() || failed)) { failed = true; break; }
-        if (tid == 0 && ch + 1 < nchunks) issue_v(ch + 1);  // V tile is free again
-
-        // ================= W pass: W^T (lane c, column i) -> W tile (rows c, 64 i)
-        {
-            uint32_t r[16];
-            tmem_ld16(tb + lane_off + T_W + wg * 16, r);
-            tmem_wait_ld();
-            float x[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) x[c] = __uint_as_float(r[c]);
-            st_tile8(sb + S_WH, sb + S_WL, 128, m, wg * 16, x);
-            st_tile8(sb + S_WH, sb + S_WL, 128, m, wg * 16 + 8, x + 8);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-
-        // ================= D^T += S^T (-W^T) ; O^T = S^T Qd^T
-        if (tid == 0) {
-            fence_after_sync();
-            const uint32_t idesc_d = idesc_bf16(128, 64, false, true, false, true);  // B = W, MN-major, negated
-            const uint32_t idesc_o = idesc_bf16(128, 64, false, false);
-            const uint32_t sa[2] = {tb + T_SH, tb + T_SL};
-            const uint32_t wt[2] = {sb + S_WH, sb + S_WL}, kq[2] = {sb + S_KQH, sb + S_KQL};
-            const int combos[3][2] = {{0, 0}, {0, 1}, {1, 0}};
-            for (int cb = 0; cb < 3; ++cb)
-                for (int s = 0; s < 8; ++s) {
-                    const uint64_t bd = sdesc(wt[combos[cb][1]] + s * 2048, 8192, 1024);
-                    mma_ts(tb + T_D, sa[combos[cb][0]] + s * 8, bd, idesc_d, 1u);
-                }
-            int first = 1;
-            for (int cb = 0; cb < 3; ++cb)
-                for (int s = 0; s < 8; ++s) {
-                    const uint64_t bd = sdesc(kq[combos[cb][1]] + 8192 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-                    mma_ts(tb + T_O, sa[combos[cb][0]] + s * 8, bd, idesc_o, first ? 0u : 1u);
-                    first = 0;
-                }
-            mma_commit(mma_bar);
+            fence_async_smem();
         }
         __syncwarp();
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        __syncthreads();
 
-        // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
+        // ================= R pass: R^T (lane v, column j) -> hi/lo operand in TMEM
+        if (!wait_group(bar_r, par)) failed = 1;
+        if (tid == 0 && ch + 1 < nchunks) issue_v(ch + 1);  // the V tile has been read
         {
             uint32_t r[16], hi[8], lo[8];
-            tmem_ld16(tb + lane_off + T_D + wg * 16, r);
+            tmem_ld16(tb + lane_off + T_R + wg * 16, r);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
-            tmem_st8(tb + lane_off + T_DH + wg * 8, hi);
-            tmem_st8(tb + lane_off + T_DL + wg * 8, lo);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int c0 = wg * 32 + half * 16;
-                tmem_ld16(tb + lane_off + T_S + c0, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * fs[F_GEXP + c0 + c]);
-                tmem_st16(tb + lane_off + T_S + c0, r);
-            }
+            tmem_st8(tb + lane_off + T_RH + wg * 8, hi);
+            tmem_st8(tb + lane_off + T_RL + wg * 8, lo);
             tmem_wait_st();
         }
         fence_before_sync();
-        __syncthreads();
+        // ---- T diag(beta) tile and R^T hi/lo are ready
+        if (__syncthreads_or(failed)) break;
 
-        // ================= O^T += D^T P^T ; S^T += D^T Kg
+        // ================= D^T = R^T (T diag beta)^T
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t idesc_p = idesc_bf16(128, 64, false, false);
-            const uint32_t idesc_s = idesc_bf16(128, 128, false, true);
-            const uint32_t da[2] = {tb + T_DH, tb + T_DL};
-            const uint32_t pt[2] = {sb + S_PH, sb + S_PL}, kgt[2] = {sb + S_KMH, sb + S_KML};
-            const int combos[3][2] = {{0, 0}, {0, 1}, {1, 0}};
+            const uint32_t id64 = idesc_bf16(128, 64, false, false);
+#pragma unroll 1
             for (int cb = 0; cb < 3; ++cb)
-                for (int s = 0; s < 4; ++s) {
-                    mma_ts(tb + T_O, da[combos[cb][0]] + s * 8, sdesc(pt[combos[cb][1]] + s * 32, 16, 1024), idesc_p, 1u);
-                    mma_ts(tb + T_S, da[combos[cb][0]] + s * 8, sdesc(kgt[combos[cb][1]] + s * 2048, 8192, 1024),
-                           idesc_s, 1u);
-                }
-            mma_commit(mma_bar);
+#pragma unroll 1
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tb + T_D, tb + (combo_a(cb) ? T_RL : T_RH) + s * 8,
+                           sdesc((combo_b(cb) ? sb + S_TBL : sb + S_TBH) + s * 32, 16, 1024), id64,
+                           (cb | s) ? 1u : 0u);
+            mma_commit(bar_d);
         }
         __syncwarp();
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-
-        // ================= O pass (+ gated norm) and state pass
+        // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
+        if (!wait_group(bar_d, par)) failed = 1;
         {
-            uint32_t r[16];
-            tmem_ld16(tb + lane_off + T_O + wg * 16, r);
+        uint32_t r[16], s1[16], s2[16], hi[8], lo[8];
+            const int c0 = wg * 32;
+            tmem_ld16(tb + lane_off + T_D + wg * 16, r);
+            tmem_ld16(tb + lane_off + T_S + c0, s1);
+            tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
             tmem_wait_ld();
+    #pragma unroll
+            for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
+            tmem_st8(tb + lane_off + T_DH + wg * 8, hi);
+            tmem_st8(tb + lane_off + T_DL + wg * 8, lo);
+    #pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                s1[c] = __float_as_uint(__uint_as_float(s1[c]) * fs[F_GEXP + c0 + c]);
+                s2[c] = __float_as_uint(__uint_as_float(s2[c]) * fs[F_GEXP + c0 + 16 + c]);
+            }
+            tmem_st16(tb + lane_off + T_S + c0, s1);
+            tmem_st16(tb + lane_off + T_S + c0 + 16, s2);
+            tmem_wait_st();
+            fence_before_sync();
+    }
+        // ---- D^T hi/lo ready, S^T decayed
+        if (__syncthreads_or(failed)) break;
+
+        // ================= [O|S]^T += D^T [P^T | Kg]
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t id192 = idesc_bf16(128, 192, false, true);
+#pragma unroll 1
+            for (int cb = 0; cb < 3; ++cb)
+#pragma unroll 1
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tb + T_O, tb + (combo_a(cb) ? T_DL : T_DH) + s * 8,
+                           sdesc((combo_b(cb) ? sb + S_PKGL : sb + S_PKGH) + s * 2048, 8192, 1024), id192, 1u);
+            mma_commit(bar_s);
+        }
+        __syncwarp();
+        // ================= O pass (+ gated norm) and state pass
+        if (!wait_group(bar_s, par)) failed = 1;
+        {
+        uint32_t r[16];
+            const int c0 = wg * 32;
+            {
+                uint32_t s1[16], s2[16], hi[16], lo[16];
+                tmem_ld16(tb + lane_off + T_O + wg * 16, r);
+                tmem_ld16(tb + lane_off + T_S + c0, s1);
+                tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
+                tmem_wait_ld();
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    split2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]), hi[c], lo[c]);
+                    split2(__uint_as_float(s2[2 * c]), __uint_as_float(s2[2 * c + 1]), hi[8 + c], lo[8 + c]);
+                }
+                tmem_st16(tb + lane_off + T_SH + wg * 16, hi);
+                tmem_st16(tb + lane_off + T_SL + wg * 16, lo);
+                const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                tmem_st16(tb + lane_off + T_O + wg * 16, zero);  // O^T starts from zero next chunk
+            }
             const int v = m;
             const int i0 = wg * 16;
             if (p.gate) {
-                float* red = fs + F_RED;
-#pragma unroll
+                float *red = fs + F_RED;
+    #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float x = __uint_as_float(r[c]);
-                    const float s2 = warp_sum(x * x);
-                    if (lane == 0) red[(wg * 4 + wq) * 16 + c] = s2;
+                    const float s2v = warp_sum(x * x);
+                    if (lane == 0) red[(wg * 4 + wq) * 16 + c] = s2v;
                 }
                 __syncthreads();
                 const float w = p.norm_w[v];
-#pragma unroll
+    #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int i = i0 + c;
                     if (i < cn) {
@@ -592,46 +706,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else if (p.o) {
-#pragma unroll
+    #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int i = i0 + c;
                     if (i < cn) st_out(p.o, ((size_t)(bos + t0 + i) * H + h) * DV + v, __uint_as_float(r[c]), p.o_bf16);
                 }
             }
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld16(tb + lane_off + T_S + wg * 32 + half * 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[half * 8 + c], lo[half * 8 + c]);
-            }
-            tmem_st16(tb + lane_off + T_SH + wg * 16, hi);
-            tmem_st16(tb + lane_off + T_SL + wg * 16, lo);
             tmem_wait_st();
         }
-        fence_before_sync();
-        __syncthreads();
+        // the next chunk's first barrier (or the final one) orders the state pass before its use
     }
+    failed = __syncthreads_or(failed);
 
     if (failed) {
         if (tid == 0) {
             atomicAdd(&g_chunk_tc_timeouts, 1);
-            mma_commit(mma_bar);  // arrives once the tensor-core work already issued has drained
+            mma_commit(drain_bar);  // arrives once the tensor-core work already issued has drained
         }
-        mbar_wait(mma_bar, mma_phase, kPolls);
+        __syncthreads();
+        mbar_wait(drain_bar, 0, kPolls);
         if (p.sT)
             for (int e = tid; e < DK * DV; e += kThreads) p.sT[(size_t)unit * DK * DV + e] = __int_as_float(0x7fc00000);
     } else if (p.sT) {  // final state: S[c][v] from S^T (lane v, column c)
+        uint32_t s1[16], s2[16];
+        const int c0 = wg * 32;
+        tmem_ld16(tb + lane_off + T_S + c0, s1);
+        tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
+        tmem_wait_ld();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t r[16];
-            const int c0 = wg * 32 + half * 16;
-            tmem_ld16(tb + lane_off + T_S + c0, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) p.sT[((size_t)unit * DK + c0 + c) * DV + m] = __uint_as_float(r[c]);
+        for (int c = 0; c < 16; ++c) {
+            p.sT[((size_t)unit * DK + c0 + c) * DV + m] = __uint_as_float(s1[c]);
+            p.sT[((size_t)unit * DK + c0 + 16 + c) * DV + m] = __uint_as_float(s2[c]);
         }
     }
     fence_before_sync();
@@ -685,11 +790,11 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
     const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)p_in.H * DV * 2};
     const cuuint32_t box[3] = {64, 1, 64};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p_in.v), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) {
-        set_error("chunk_tc: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+    CUresult cres = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p_in.v), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cres != CUDA_SUCCESS) {
+        set_error("chunk_tc: cuTensorMapEncodeTiled failed (%d)", (int)cres);
         return KDA_ERR_CUDA;
     }
     TcParams tp;
