@@ -35,6 +35,26 @@ PREFILL_FLOP_PER_TH = 10 * 64 * 128 + 6 * 128 * 128 + (2 * 64 * 64) // 3  # 182,
 STATE_BYTES = 128 * 128 * 4
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256 + 512  # + gate bf16, y fp32
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work from one
+# ncu capture summarised under profiles/, valid only for the kernel source it was
+# taken on: `traffic` is reported as null as soon as that source file changes.
+MEASURED_TRAFFIC = {}
+
+
+def measured_traffic(kind: str, units: float, fixed: float = 0.0):
+    """Traffic of one launch scaled from the capture, or None if the kernel changed."""
+    import hashlib
+    m = MEASURED_TRAFFIC.get(kind)
+    if m is None:
+        return None
+    try:
+        with open(os.path.join(ROOT, m["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != m["sha256"]:
+                return None
+    except OSError:
+        return None
+    return m["bytes_per_unit"] * units + fixed
+
 
 def load_peaks():
     try:
@@ -169,15 +189,15 @@ def time_steps(fn, steps, warmup, world, clocks_index=None):
             "launches": launches, "clocks": sampler.summary() if sampler else None}
 
 
-def prefill_inputs(device):
+def prefill_inputs(device, T=None):
     from kimi_delta_attention_gated_gb300.inputs import make_inputs
-    return make_inputs("prefill", device=device)
+    return make_inputs("prefill", device=device, T=T)
 
 
 def bench_prefill(args, world, rank, peaks):
     import torch
     import kimi_delta_attention_gated_gb300 as kda
-    d = prefill_inputs("cuda")
+    d = prefill_inputs("cuda", args.prefill_T)
     B, T, H, K, V = d["B"], d["T"], d["H"], d["K"], d["V"]
     o = torch.empty((B, T, H, V), device="cuda", dtype=torch.float32)
     fs = torch.empty((B, H, K, V), device="cuda", dtype=torch.float32)
@@ -197,7 +217,7 @@ def bench_prefill(args, world, rank, peaks):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("prefill", th, B * H * STATE_BYTES),
                      "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
                      "peak_source": peaks["source"]},
         "roofline_tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -214,7 +234,7 @@ def bench_decode(args, world, peaks):
     import torch
     import kimi_delta_attention_gated_gb300 as kda
     from kimi_delta_attention_gated_gb300.inputs import make_inputs
-    d = make_inputs("decode", device="cuda")
+    d = make_inputs("decode", device="cuda", B=args.decode_B)
     sq = lambda t: t.squeeze(1).contiguous()
     q, k, v, g, beta, gate = (sq(d[n]) for n in ("q", "k", "v", "g", "beta", "gate"))
     state = d["initial_state"]
@@ -231,7 +251,7 @@ def bench_decode(args, world, peaks):
             "config": {"workload": f"decode B={B} H={H} d={K} fp32 state in place + fused sigmoid-gated RMSNorm",
                        "l2_flush": "state 1.61 GB > L2"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("decode", B * H),
                          "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
                          "peak_source": peaks["source"]}}
 
@@ -243,9 +263,11 @@ def bench_e2e(args, world, d):
     host = {n: d[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     B, T, H, V = d["B"], d["T"], d["H"], d["V"]
-    d2h = B * T * H * V * 4 + B * H * d["K"] * V * 4
+    o_h = torch.empty((B, T, H, V), dtype=torch.float32).pin_memory()
+    s_h = torch.empty((B, H, d["K"], V), dtype=torch.float32).pin_memory()
+    d2h = o_h.numel() * 4 + s_h.numel() * 4
     fn = lambda: kda.chunk_fwd(host["q"], host["k"], host["v"], host["g"], host["beta"], None, scale=d["scale"],
-                               chunk=64, mode=args.mode)
+                               chunk=64, mode=args.mode, o=o_h, final_state=s_h)
     steps = max(2, min(args.steps, 5))
     for _ in range(max(1, min(args.warmup, 2))):
         fn()
@@ -319,6 +341,10 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling runs: time one workload only")
+    ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
+    ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -335,11 +361,16 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
+    if args.only == "decode":
+        dec = bench_decode(args, world, peaks)
+        if rank == 0:
+            print(json.dumps(dec), flush=True)
+        return
     pre, d = bench_prefill(args, world, rank, peaks)
-    dec = None if args.no_decode else bench_decode(args, world, peaks)
-    e2e = None if args.no_e2e else bench_e2e(args, world, d)
+    dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
+    e2e = None if (args.no_e2e or args.only == "prefill") else bench_e2e(args, world, d)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
         cpu = cpu_baseline(d, args.cpu_heads)
     if rank != 0:
         return

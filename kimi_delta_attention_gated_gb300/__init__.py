@@ -125,10 +125,28 @@ def _cu(cu_seqlens, device):
     return dev, host, host.numel() - 1
 
 
-def _to_host(ts, host):
+def _to_host(ts, host, dests=None):
+    """Copy results back to the host: into the caller's host tensors when given
+    (asynchronously when they are pinned, then the stream is synchronised)."""
     if not host:
         return ts
-    return tuple(None if t is None else t.to("cpu") for t in ts)
+    out = []
+    for i, t in enumerate(ts):
+        dst = dests[i] if dests is not None else None
+        if t is None:
+            out.append(None)
+        elif dst is not None:
+            dst.copy_(t, non_blocking=dst.is_pinned())
+            out.append(dst)
+        else:
+            out.append(t.to("cpu"))
+    torch.cuda.current_stream().synchronize()
+    return tuple(out)
+
+
+def _dev_out(t):
+    """A caller-provided output on the host is computed on the device first."""
+    return None if (t is None or t.device.type != "cuda") else t
 
 
 def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use_qk_l2norm=True,
@@ -143,6 +161,9 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
     lib = _load()
     host = q.device.type != "cuda"
     dev = _device_of(q, k, v)
+    dests = (o, final_state, y) if host else None
+    if host:
+        o, final_state, y = _dev_out(o), _dev_out(final_state), _dev_out(y)
     q, k, v = _prep(q, dev), _prep(k, dev), _prep(v, dev)
     g, beta = _prep(g, dev, torch.float32), _prep(beta, dev, torch.float32)
     initial_state = _prep(initial_state, dev, torch.float32)
@@ -154,7 +175,7 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
         gate, norm_w = _prep(gate, dev), _prep(norm_w, dev, torch.float32)
         if y is None:
             y = torch.empty((B, T, H * V), device=dev, dtype=out_dtype)
-    if o is None and (return_o or gate is None):
+    if o is None and (return_o or (dests is not None and dests[0] is not None) or gate is None):
         o = torch.empty((B, T, H, V), device=dev, dtype=out_dtype)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, K, V), device=dev, dtype=torch.float32)
@@ -166,8 +187,8 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
         float(scale), int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16,
         _ptr(norm_w), float(eps), _ptr(y), _MODES[mode] if isinstance(mode, str) else int(mode), _stream()))
     if gate is not None:
-        return _to_host((o, final_state, y), host)
-    return _to_host((o, final_state), host)
+        return _to_host((o, final_state, y), host, dests)
+    return _to_host((o, final_state), host, dests)
 
 
 def recurrent_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, use_qk_l2norm=True,

@@ -151,66 +151,60 @@ __device__ __forceinline__ void st_pt(uint8_t *sm, int i, int j, float x) {
 __device__ __forceinline__ int combo_a(int cb) { return cb == 2 ? 1 : 0; }
 __device__ __forceinline__ int combo_b(int cb) { return cb == 1 ? 1 : 0; }
 
-// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 at block distance D (I - J = D):
-// X = sum_{K=J}^{I-1} A_IK T_KJ (kept in A's unused upper block (J, I)), then
-// T_IJ = -T_II X.  Each 2 x 2 output tile is shared by S adjacent lanes that split
-// the inner sum and combine it with shuffles.
-template <int D>
-__device__ __forceinline__ void tri_level(float *Asm, float *Tsm, int ctid) {
-    constexpr int NP = 4 - D;
-    constexpr int S = D == 3 ? 4 : 2;
-    constexpr int ACTIVE = NP * 64 * S;
-    const int s = ctid % S, e = (ctid / S) & 63, pr = ctid / (S * 64);
-    const int I = D + pr, J = I - D, r = (e >> 3) * 2, cc = (e & 7) * 2;
-    if (ctid < ACTIVE) {
-        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+// One 16 x 16 x 16 product of the triangular solve, 64 threads, each a 1 x 4 strip:
+// dst = (acc ? dst : 0) + sign * X Y, blocks addressed by their top-left element.
+// The whole row of X (4 x 16 B) and the strip of Y (16 x 16 B) are loaded up front.
+__device__ __forceinline__ void blk16(float *dst, const float *X, const float *Y, float sign, bool acc, int t) {
+    const int r = t >> 2, c4 = (t & 3) * 4;
+    float x[16];
 #pragma unroll
-        for (int st = 0; st < 16 * D / S; ++st) {
-            const int krow = 16 * J + s + S * st;
-            const float a0 = Asm[(16 * I + r) * AP + krow], a1 = Asm[(16 * I + r + 1) * AP + krow];
-            const float2 t = *reinterpret_cast<const float2 *>(Tsm + krow * AP + 16 * J + cc);
-            x00 = fmaf(a0, t.x, x00);
-            x01 = fmaf(a0, t.y, x01);
-            x10 = fmaf(a1, t.x, x10);
-            x11 = fmaf(a1, t.y, x11);
-        }
+    for (int k = 0; k < 16; k += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(X + r * AP + k);
+        x[k] = v.x; x[k + 1] = v.y; x[k + 2] = v.z; x[k + 3] = v.w;
+    }
+    float4 o = acc ? *reinterpret_cast<const float4 *>(dst + r * AP + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int o = 1; o < S; o <<= 1) {
-            x00 += __shfl_xor_sync(0xffffffffu, x00, o);
-            x01 += __shfl_xor_sync(0xffffffffu, x01, o);
-            x10 += __shfl_xor_sync(0xffffffffu, x10, o);
-            x11 += __shfl_xor_sync(0xffffffffu, x11, o);
-        }
-        if (s == 0) {
-            *reinterpret_cast<float2 *>(Asm + (16 * J + r) * AP + 16 * I + cc) = make_float2(x00, x01);
-            *reinterpret_cast<float2 *>(Asm + (16 * J + r + 1) * AP + 16 * I + cc) = make_float2(x10, x11);
-        }
+    for (int k = 0; k < 16; ++k) {
+        const float4 y = *reinterpret_cast<const float4 *>(Y + k * AP + c4);
+        s.x = fmaf(x[k], y.x, s.x);
+        s.y = fmaf(x[k], y.y, s.y);
+        s.z = fmaf(x[k], y.z, s.z);
+        s.w = fmaf(x[k], y.w, s.w);
+    }
+    o.x = fmaf(sign, s.x, o.x);
+    o.y = fmaf(sign, s.y, o.y);
+    o.z = fmaf(sign, s.z, o.z);
+    o.w = fmaf(sign, s.w, o.w);
+    *reinterpret_cast<float4 *>(dst + r * AP + c4) = o;
+}
+
+// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 from the diagonal inverses T_II:
+//   T_IJ = -T_II X_IJ,  X_IJ = sum_{K=J}^{I-1} A_IK T_KJ        (I > J)
+// The partial sums that need only diagonal blocks are formed first, so every phase
+// is a batch of independent K = 16 products.  X_IJ lives in A's unused upper block (J, I).
+__device__ __forceinline__ void tri_offdiag(float *Asm, float *Tsm, int ctid) {
+    auto A = [&](int i, int j) { return Asm + 16 * i * AP + 16 * j; };
+    auto T = [&](int i, int j) { return Tsm + 16 * i * AP + 16 * j; };
+    auto X = [&](int i, int j) { return Asm + 16 * j * AP + 16 * i; };  // upper block (j, i) of A
+    const int p = ctid >> 6, t = ctid & 63;
+    if (p < 6) {  // X10, X21, X32 and the first terms of X20, X31, X30: (I, J) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+        const int I = p < 3 ? p + 1 : (p == 3 ? 2 : 3), J = p < 3 ? p : (p == 4 ? 1 : 0);
+        blk16(X(I, J), A(I, J), T(J, J), 1.f, false, t);
     }
     tbar();
-    if (ctid < ACTIVE) {
-        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll
-        for (int st = 0; st < 16 / S; ++st) {
-            const int t = s + S * st;
-            const float a0 = Tsm[(16 * I + r) * AP + 16 * I + t], a1 = Tsm[(16 * I + r + 1) * AP + 16 * I + t];
-            const float2 x = *reinterpret_cast<const float2 *>(Asm + (16 * J + t) * AP + 16 * I + cc);
-            y00 = fmaf(a0, x.x, y00);
-            y01 = fmaf(a0, x.y, y01);
-            y10 = fmaf(a1, x.x, y10);
-            y11 = fmaf(a1, x.y, y11);
-        }
-#pragma unroll
-        for (int o = 1; o < S; o <<= 1) {
-            y00 += __shfl_xor_sync(0xffffffffu, y00, o);
-            y01 += __shfl_xor_sync(0xffffffffu, y01, o);
-            y10 += __shfl_xor_sync(0xffffffffu, y10, o);
-            y11 += __shfl_xor_sync(0xffffffffu, y11, o);
-        }
-        if (s == 0) {
-            *reinterpret_cast<float2 *>(Tsm + (16 * I + r) * AP + 16 * J + cc) = make_float2(-y00, -y01);
-            *reinterpret_cast<float2 *>(Tsm + (16 * I + r + 1) * AP + 16 * J + cc) = make_float2(-y10, -y11);
-        }
+    if (p < 3) blk16(T(p + 1, p), T(p + 1, p + 1), X(p + 1, p), -1.f, false, t);  // T10, T21, T32
+    tbar();
+    if (p < 3) {  // X20 += A21 T10, X31 += A32 T21, X30 += A31 T10: (I, J, K) = (2,0,1) (3,1,2) (3,0,1)
+        const int I = p == 0 ? 2 : 3, J = p == 1 ? 1 : 0, K = p == 1 ? 2 : 1;
+        blk16(X(I, J), A(I, K), T(K, J), 1.f, true, t);
     }
+    tbar();
+    if (p < 2) blk16(T(p + 2, p), T(p + 2, p + 2), X(p + 2, p), -1.f, false, t);  // T20, T31
+    tbar();
+    if (p == 0) blk16(X(3, 0), A(3, 2), T(2, 0), 1.f, true, t);  // X30 += A32 T20
+    tbar();
+    if (p == 0) blk16(T(3, 0), T(3, 3), X(3, 0), -1.f, false, t);  // T30
     tbar();
 }
 
@@ -363,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < 4) {
             const int i = warp * 4 + lane;
             fs[F_BETA + i] = (i < cn) ? p.beta[(size_t)(bos + t0 + i) * H + h] : 0.f;
-            fs[F_RQ + i] = rq[lane];
-            fs[F_RK + i] = rk[lane];
+            fs[F_RQ + i] = lane == 0 ? rq[0] : (lane == 1 ? rq[1] : (lane == 2 ? rq[2] : rq[3]));
+            fs[F_RK + i] = lane == 0 ? rk[0] : (lane == 1 ? rk[1] : (lane == 2 ? rk[2] : rk[3]));
         }
         // inclusive prefix over the thread's 4 tokens; warp totals to the scan buffer
 #pragma unroll
@@ -573,9 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i) Tsm[(o + i) * AP + o + c] = x[i];
             }
             tbar();
-            tri_level<1>(Asm, Tsm, ctid);
-            tri_level<2>(Asm, Tsm, ctid);
-            tri_level<3>(Asm, Tsm, ctid);
+            tri_offdiag(Asm, Tsm, ctid);
             for (int it = ctid; it < 64 * 8; it += kSolve) {  // T diag(beta) -> hi/lo tile (rows i, K = j)
                 const int i = it >> 3, j0 = (it & 7) * 8;
                 float x[8];
@@ -622,17 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
         if (!wait_group(bar_d, par)) failed = 1;
         {
-        uint32_t r[16], s1[16], s2[16], hi[8], lo[8];
+            uint32_t r[16], s1[16], s2[16], hi[8], lo[8];
             const int c0 = wg * 32;
             tmem_ld16(tb + lane_off + T_D + wg * 16, r);
             tmem_ld16(tb + lane_off + T_S + c0, s1);
             tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
             tmem_wait_ld();
-    #pragma unroll
+#pragma unroll
             for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
             tmem_st8(tb + lane_off + T_DH + wg * 8, hi);
             tmem_st8(tb + lane_off + T_DL + wg * 8, lo);
-    #pragma unroll
+#pragma unroll
             for (int c = 0; c < 16; ++c) {
                 s1[c] = __float_as_uint(__uint_as_float(s1[c]) * fs[F_GEXP + c0 + c]);
                 s2[c] = __float_as_uint(__uint_as_float(s2[c]) * fs[F_GEXP + c0 + 16 + c]);
@@ -641,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tb + lane_off + T_S + c0 + 16, s2);
             tmem_wait_st();
             fence_before_sync();
-    }
+        }
         // ---- D^T hi/lo ready, S^T decayed
         if (__syncthreads_or(failed)) break;
 
@@ -661,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
         {
-        uint32_t r[16];
+            uint32_t r[16];
             const int c0 = wg * 32;
             {
                 uint32_t s1[16], s2[16], hi[16], lo[16];
@@ -669,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld16(tb + lane_off + T_S + c0, s1);
                 tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
                 tmem_wait_ld();
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     split2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]), hi[c], lo[c]);
                     split2(__uint_as_float(s2[2 * c]), __uint_as_float(s2[2 * c + 1]), hi[8 + c], lo[8 + c]);
@@ -683,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i0 = wg * 16;
             if (p.gate) {
                 float *red = fs + F_RED;
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float x = __uint_as_float(r[c]);
                     const float s2v = warp_sum(x * x);
@@ -691,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncthreads();
                 const float w = p.norm_w[v];
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int i = i0 + c;
                     if (i < cn) {
@@ -706,10 +698,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else if (p.o) {
-    #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int i = i0 + c;
-                    if (i < cn) st_out(p.o, ((size_t)(bos + t0 + i) * H + h) * DV + v, __uint_as_float(r[c]), p.o_bf16);
+                // rows i0.. of this head: one base pointer, a constant row stride
+                const size_t base = ((size_t)(bos + t0 + i0) * H + h) * DV + v, stride = (size_t)H * DV;
+                if (!p.o_bf16 && i0 + 16 <= cn) {
+                    float *ob = reinterpret_cast<float *>(p.o) + base;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) ob[c * stride] = __uint_as_float(r[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        if (i0 + c < cn) st_out(p.o, base + c * stride, __uint_as_float(r[c]), p.o_bf16);
                 }
             }
             tmem_wait_st();

@@ -10,6 +10,8 @@
 //   3  A in TMEM (packed bf16 pairs, K = 64), B K-major smem (N = 64)
 //   4  case 0 with the second half of K accumulated with B negated
 //   5  A in TMEM (K = 64), B MN-major smem (N = 128)
+//   6  failure detection: a bounded wait on an mbarrier that nothing arrives on must
+//      give up, report it (err = 2) and leave the kernel and the context usable
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -85,6 +87,13 @@ __global__ void __launch_bounds__(128) probe_kernel(int which, const __nv_bfloat
     __syncthreads();
     fence_after_sync();
 
+    if (which == 6) {  // no MMA is issued and nothing arrives: the wait must run out
+        if (tid == 0 && !mbar_wait(&bar, 0, 4096)) atomicExch(err, 2);
+        fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(t0, 256);
+        return;
+    }
     if (tid == 0) {
         const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
         for (int s = 0; s < K / 16; ++s) {

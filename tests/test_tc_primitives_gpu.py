@@ -40,6 +40,20 @@ CASES = {  # which: (K, N, negate second half)
 }
 
 
+def test_bounded_wait_reports_timeout(probe):
+    """A wait on an mbarrier that nothing arrives on gives up after its poll bound and
+    reports it; the context stays usable (the next launch still computes correctly)."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    A = torch.zeros(128, 128, device="cuda", dtype=torch.bfloat16)
+    D = torch.zeros(128, 64, device="cuda")
+    rc = probe.tc_probe(6, A.data_ptr(), A.data_ptr(), D.data_ptr(), err.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(err.item()) == 2
+    test_tc_primitive(probe, 0)
+
+
 @pytest.mark.parametrize("which", sorted(CASES))
 def test_tc_primitive(probe, which):
     K, N, neg = CASES[which]
