@@ -38,7 +38,18 @@ DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256 + 512  # + gat
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work from one
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # B=1 T=2048 H=96 capture: (330.24 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
+                "sha256": "ccbfb420e83fed6b91d32833e3c9549ad036d7e6470f521a6a048e86be61d4e3",
+                "bytes_per_unit": (330.24e6 - 6.29e6) / (2048 * 96),
+                "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
+    # B=64 capture: 757.3 MB / (64 * 96) (sequence, head) units
+    "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
+               "sha256": "0691f03b03e90ea0ee70519ef2406d711739f838c832ffdc89a8050a1db954f4",
+               "bytes_per_unit": 757.3e6 / (64 * 96),
+               "capture": "profiles/recurrent_kernel_decode_B64.md"},
+}
 
 
 def measured_traffic(kind: str, units: float, fixed: float = 0.0):
