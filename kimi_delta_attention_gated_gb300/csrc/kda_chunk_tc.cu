@@ -44,7 +44,9 @@
 //       ... meanwhile on CUDA cores: gram pass, T = (I + A)^-1, T diag(beta) tile
 //     D^T  = R^T (T diag beta)^T                           N=64  K=64  (R^T in TMEM)
 //     [O|S]^T += D^T [P^T | Kg]  (S^T pre-scaled by exp(gamma))  N=192 K=64
-// The next chunk's q, k and g are loaded into registers while the current one runs.
+// The next chunk's q, k and g are loaded into registers while the current one runs,
+// and its CUDA-core preparation (norms, cumulative decay, operand tiles) is done while
+// this chunk's D and [O|S] products run on the tensor cores.
 #include <cuda.h>
 #include <math.h>
 #include <string.h>
@@ -324,97 +326,132 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ok;
     };
 
-    int failed = 0;
-    for (int ch = 0; ch < nchunks; ++ch) {
-        const int par = ch & 1;
-        const int t0 = ch * C;
-        const int cn = min(C, len - t0);
-        int out_of_range = 0;
-        // ================= prep: norms, cumulative decay, operand tiles
-        float g4[4][4], q4[4][4], k4[4][4];
+    float *scan = reinterpret_cast<float *>(sm + S_SCAN);
+
+    // ---- preparation of a chunk, first half: per-token norm scales and beta into the
+    // small buffers, each warp's decay totals per key channel into the scan buffer.
+    // The 8 sums of squares of a warp's 4 tokens are reduced with a reduce-scatter
+    // (9 shuffles); lanes 4v..4v+3 end with sum v (q of tokens 0-3, then k).
+    auto prep_norms = [&](const ChunkRegs &c, int t0n, int cnn) {
+        float a[8];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            g4[r][0] = cr.g[r].x; g4[r][1] = cr.g[r].y; g4[r][2] = cr.g[r].z; g4[r][3] = cr.g[r].w;
-            q4[r][0] = bf16lo(cr.q[r].x); q4[r][1] = bf16hi(cr.q[r].x);
-            q4[r][2] = bf16lo(cr.q[r].y); q4[r][3] = bf16hi(cr.q[r].y);
-            k4[r][0] = bf16lo(cr.k[r].x); k4[r][1] = bf16hi(cr.k[r].x);
-            k4[r][2] = bf16lo(cr.k[r].y); k4[r][3] = bf16hi(cr.k[r].y);
+            const float q0 = bf16lo(c.q[r].x), q1 = bf16hi(c.q[r].x), q2 = bf16lo(c.q[r].y), q3 = bf16hi(c.q[r].y);
+            const float k0 = bf16lo(c.k[r].x), k1 = bf16hi(c.k[r].x), k2 = bf16lo(c.k[r].y), k3 = bf16hi(c.k[r].y);
+            a[r] = fmaf(q0, q0, fmaf(q1, q1, fmaf(q2, q2, q3 * q3)));
+            a[4 + r] = fmaf(k0, k0, fmaf(k1, k1, fmaf(k2, k2, k3 * k3)));
         }
-        float rq[4], rk[4];
+        const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+        float b[4], d2[2];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            float aq = 0.f, ak = 0.f;
+        for (int j = 0; j < 4; ++j)
+            b[j] = (u16 ? a[j + 4] : a[j]) + __shfl_xor_sync(0xffffffffu, u16 ? a[j] : a[j + 4], 16);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                aq = fmaf(q4[r][c], q4[r][c], aq);
-                ak = fmaf(k4[r][c], k4[r][c], ak);
-            }
-            aq = warp_sum(aq);
-            ak = warp_sum(ak);
-            rq[r] = (p.l2norm ? rsqrtf(aq + 1e-6f) : 1.f) * p.scale;
-            rk[r] = p.l2norm ? rsqrtf(ak + 1e-6f) : 1.f;
+        for (int j = 0; j < 2; ++j)
+            d2[j] = (u8 ? b[j + 2] : b[j]) + __shfl_xor_sync(0xffffffffu, u8 ? b[j] : b[j + 2], 8);
+        float d = (u4 ? d2[1] : d2[0]) + __shfl_xor_sync(0xffffffffu, u4 ? d2[0] : d2[1], 4);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        if ((lane & 3) == 0) {
+            const int v = lane >> 2;
+            const float sc = p.l2norm ? rsqrtf(d + 1e-6f) : 1.f;
+            if (v < 4)
+                fs[F_RQ + warp * 4 + v] = sc * p.scale;
+            else
+                fs[F_RK + warp * 4 + v - 4] = sc;
         }
         if (lane < 4) {
             const int i = warp * 4 + lane;
-            fs[F_BETA + i] = (i < cn) ? p.beta[(size_t)(bos + t0 + i) * H + h] : 0.f;
-            fs[F_RQ + i] = lane == 0 ? rq[0] : (lane == 1 ? rq[1] : (lane == 2 ? rq[2] : rq[3]));
-            fs[F_RK + i] = lane == 0 ? rk[0] : (lane == 1 ? rk[1] : (lane == 2 ? rk[2] : rk[3]));
+            fs[F_BETA + i] = (i < cnn) ? p.beta[(size_t)(bos + t0n + i) * H + h] : 0.f;
         }
-        // inclusive prefix over the thread's 4 tokens; warp totals to the scan buffer
+        float4 t = c.g[0];
 #pragma unroll
-        for (int r = 1; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) g4[r][c] += g4[r - 1][c];
-        float *scan = reinterpret_cast<float *>(sm + S_SCAN);
-        *reinterpret_cast<float4 *>(scan + warp * 128 + l4) = make_float4(g4[3][0], g4[3][1], g4[3][2], g4[3][3]);
-        __syncthreads();
+        for (int r = 1; r < 4; ++r) {
+            t.x += c.g[r].x; t.y += c.g[r].y; t.z += c.g[r].z; t.w += c.g[r].w;
+        }
+        *reinterpret_cast<float4 *>(scan + warp * 128 + l4) = t;
+    };
+
+    // ---- preparation, second half (after a barrier): cumulative decay, exp(gamma),
+    // the [-Kd ; Qd] and Km operand tiles; Kg is returned in registers because its
+    // tile may still be in use.  Returns 1 if the chunk's decay range is too wide.
+    auto prep_tiles = [&](const ChunkRegs &c, float (&kgv)[4][4]) -> int {
         float o4[4] = {0.f, 0.f, 0.f, 0.f}, gam[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < 16; ++w) {  // offset of this warp's tokens and the chunk total, per channel
             const float4 t = *reinterpret_cast<const float4 *>(scan + w * 128 + l4);
             const float tt[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (w < warp) o4[c] += tt[c];
-                gam[c] += tt[c];
+            for (int e = 0; e < 4; ++e) {
+                if (w < warp) o4[e] += tt[e];
+                gam[e] += tt[e];
             }
         }
         float egam[4];
+        int oor = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            egam[c] = __expf(gam[c]);
-            out_of_range |= (-gam[c] > kRangeMax);
+        for (int e = 0; e < 4; ++e) {
+            egam[e] = __expf(gam[e]);
+            oor |= (-gam[e] > kRangeMax);
         }
         if (warp == 0) *reinterpret_cast<float4 *>(fs + F_GEXP + l4) = make_float4(egam[0], egam[1], egam[2], egam[3]);
+        const float4 rq4 = *reinterpret_cast<const float4 *>(fs + F_RQ + warp * 4);
+        const float4 rk4 = *reinterpret_cast<const float4 *>(fs + F_RK + warp * 4);
+        const float rq[4] = {rq4.x, rq4.y, rq4.z, rq4.w}, rk[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = warp * 4 + r;
-            float kd[4], qd[4], km[4], kg[4];
+            const float gr[4] = {c.g[r].x, c.g[r].y, c.g[r].z, c.g[r].w};
+            const float qv[4] = {bf16lo(c.q[r].x), bf16hi(c.q[r].x), bf16lo(c.q[r].y), bf16hi(c.q[r].y)};
+            const float kv[4] = {bf16lo(c.k[r].x), bf16hi(c.k[r].x), bf16lo(c.k[r].y), bf16hi(c.k[r].y)};
+            float kd[4], qd[4], km[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float G = o4[c] + g4[r][c];
-                const float eG = __expf(G);
-                const float kh = k4[r][c] * rk[r];
-                kd[c] = -kh * eG;
-                qd[c] = q4[r][c] * rq[r] * eG;
-                km[c] = kh * __expf(-G);
-                kg[c] = km[c] * egam[c];
+            for (int e = 0; e < 4; ++e) {
+                o4[e] += gr[e];  // inclusive cumulative decay G of token i
+                const float eG = __expf(o4[e]);
+                const float kh = kv[e] * rk[r];
+                kd[e] = -kh * eG;
+                qd[e] = qv[e] * rq[r] * eG;
+                km[e] = kh * __expf(-o4[e]);
+                kgv[r][e] = km[e] * egam[e];
             }
             st_tile4(sb + S_KQH, sb + S_KQL, 128, i, l4, kd[0], kd[1], kd[2], kd[3]);
             st_tile4(sb + S_KQH, sb + S_KQL, 128, 64 + i, l4, qd[0], qd[1], qd[2], qd[3]);
-            {
-                uint32_t h0, l0, h1, l1;
-                split2(km[0], km[1], h0, l0);
-                split2(km[2], km[3], h1, l1);
-                st_shared_v2(sb + S_KM + sw128_off(i, l4, 128), h0, h1);
-                st_shared_v2(sb + S_KM + sw128_off(64 + i, l4, 128), l0, l1);
-            }
-            st_tile4(sb + S_PKGH, sb + S_PKGL, 64, i, 64 + l4, kg[0], kg[1], kg[2], kg[3]);
+            uint32_t h0, l0, h1, l1;
+            split2(km[0], km[1], h0, l0);
+            split2(km[2], km[3], h1, l1);
+            st_shared_v2(sb + S_KM + sw128_off(i, l4, 128), h0, h1);
+            st_shared_v2(sb + S_KM + sw128_off(64 + i, l4, 128), l0, l1);
         }
+        return oor;
+    };
+
+    auto st_kg = [&](const float (&kgv)[4][4]) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            st_tile4(sb + S_PKGH, sb + S_PKGL, 64, warp * 4 + r, 64 + l4, kgv[r][0], kgv[r][1], kgv[r][2], kgv[r][3]);
+    };
+
+    // ---- first chunk's preparation (later chunks are prepared inside the previous
+    // chunk's tensor-core waits)
+    int oor_next = 0;
+    if (nchunks > 0) {
+        prep_norms(cr, 0, min(C, len));
+        __syncthreads();
+        float kgv[4][4];
+        oor_next = prep_tiles(cr, kgv);
+        st_kg(kgv);
+    }
+
+    int failed = 0;
+    for (int ch = 0; ch < nchunks; ++ch) {
+        const int par = ch & 1;
+        const int t0 = ch * C;
+        const int cn = min(C, len - t0);
         fence_async_smem();
         fence_before_sync();  // the previous state pass (or the initial state) wrote TMEM
         // ---- operand tiles of this chunk and S(n-1) are ready
-        const int fallback = __syncthreads_or(out_of_range);
+        const int fallback = __syncthreads_or(oor_next);
 
         // ================= gram [-Kd;Qd] [Km_hi;Km_lo]^T (+ lo x hi)
         if (tid == 0) {
@@ -611,6 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar_d);
         }
         __syncwarp();
+        // while D runs: the next chunk's norms, beta and decay totals
+        if (ch + 1 < nchunks) prep_norms(cr, t0 + C, min(C, len - t0 - C));
         // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
         if (!wait_group(bar_d, par)) failed = 1;
         {
@@ -650,8 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar_s);
         }
         __syncwarp();
+        // while O and S update: the next chunk's operand tiles (its Kg waits for this MMA)
+        float kgv[4][4];
+        if (ch + 1 < nchunks) oor_next = prep_tiles(cr, kgv);
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
+        if (ch + 1 < nchunks) st_kg(kgv);  // the Kg tile has been read
         {
             uint32_t r[16];
             const int c0 = wg * 32;
@@ -712,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
         }
-        // the next chunk's first barrier (or the final one) orders the state pass before its use
+        // the next chunk's first barrier (or the final one) orders these writes before their use
     }
     failed = __syncthreads_or(failed);
 
