@@ -38,7 +38,7 @@
 //                [320,384)  S^T lo
 //                [384,512)  gram accumulator: [hi*hi + lo*hi | hi*lo], then R^T hi
 //                           [384,416) / lo [416,448) and the D^T accumulator [448,512)
-//   per chunk:
+//   per chunk (B operands in shared memory are K-major unless noted):
 //     gram   [-Kd;Qd] [Km_hi;Km_lo]^T  M=128 N=128 K=128, + [-Kd;Qd]_lo Km_hi^T N=64
 //     R^T  = V^T I (N=64), then [R|O]^T += S^T [-Kd;Qd]^T   N=128 K=128 (S^T in TMEM)
 //       ... meanwhile on CUDA cores: gram pass, T = (I + A)^-1, T diag(beta) tile
@@ -76,8 +76,8 @@ constexpr uint32_t S_V = 0;             // V tile, two TMA boxes of 64 tokens x 
 constexpr uint32_t S_KQH = 16384;       // [-Kd ; Qd] hi, 128 rows x 128 (32 KB)
 constexpr uint32_t S_KQL = 49152;       // [-Kd ; Qd] lo
 constexpr uint32_t S_KM = 81920;        // [Km hi ; Km lo], 128 rows x 128 (32 KB)
-constexpr uint32_t S_PKGH = 114688;     // [P^T | Kg] hi, 64 rows (j) x 192 (24 KB), MN-major B
-constexpr uint32_t S_PKGL = 139264;     // [P^T | Kg] lo
+constexpr uint32_t S_PKGH = 114688;     // [P ; Kg^T] hi, 192 rows (i, then c) x 64 (j) (24 KB), K-major B
+constexpr uint32_t S_PKGL = 139264;     // [P ; Kg^T] lo
 constexpr uint32_t S_TBH = 163840;      // T diag(beta) hi, 64 x 64 (8 KB)
 constexpr uint32_t S_TBL = 172032;
 constexpr uint32_t S_ID = 180224;       // bf16 identity 64 x 64 (8 KB)
@@ -118,17 +118,6 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 // barrier over warps 1-15 (the triangular solve, while warp 0 issues MMAs)
 __device__ __forceinline__ void tbar() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
 
-// Writes 4 consecutive columns (col % 4 == 0) of one row of a SW128 tile as hi/lo.
-__device__ __forceinline__ void st_tile4(uint32_t hi_base, uint32_t lo_base, uint32_t rows, uint32_t row,
-                                         uint32_t col, float a, float b, float c, float d) {
-    uint32_t h0, l0, h1, l1;
-    split2(a, b, h0, l0);
-    split2(c, d, h1, l1);
-    const uint32_t off = sw128_off(row, col, rows);
-    st_shared_v2(hi_base + off, h0, h1);
-    st_shared_v2(lo_base + off, l0, l1);
-}
-
 // Writes 8 consecutive columns (col % 8 == 0) of one row as hi/lo.
 __device__ __forceinline__ void st_tile8(uint32_t hi_base, uint32_t lo_base, uint32_t rows, uint32_t row,
                                          uint32_t col, const float *x) {
@@ -140,13 +129,18 @@ __device__ __forceinline__ void st_tile8(uint32_t hi_base, uint32_t lo_base, uin
     st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
 }
 
-// P[i][j] into the P^T block (rows j, columns i) of the [P^T | Kg] tiles, hi and lo.
-__device__ __forceinline__ void st_pt(uint8_t *sm, int i, int j, float x) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
-    const uint32_t off = sw128_off(j, i, 64);
-    *reinterpret_cast<__nv_bfloat16 *>(sm + S_PKGH + off) = h;
-    *reinterpret_cast<__nv_bfloat16 *>(sm + S_PKGL + off) = l;
+// Kg^T rows c..c+3 (one per key channel) at columns j0..j0+3 (4 tokens) of the
+// [P ; Kg^T] tiles, hi and lo: x[t][e] is token j0 + t, channel c + e.
+__device__ __forceinline__ void st_kgt(uint32_t sb, int c, int j0, const float (&x)[4][4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        uint32_t h0, l0, h1, l1;
+        split2(x[0][e], x[1][e], h0, l0);
+        split2(x[2][e], x[3][e], h1, l1);
+        const uint32_t off = sw128_off(64 + c + e, j0, 192);
+        st_shared_v2(sb + S_PKGH + off, h0, h1);
+        st_shared_v2(sb + S_PKGL + off, l0, l1);
+    }
 }
 
 // hi*hi, hi*lo, lo*hi: (A part, B part) of the three products of a split operand pair
@@ -214,6 +208,7 @@ __device__ __forceinline__ void tri_offdiag(float *Asm, float *Tsm, int ctid) {
 struct ChunkRegs {
     float4 g[4];
     uint2 q[4], k[4];
+    float beta;  // token warp * 4 + lane, lanes 0-3
 };
 
 __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, int bos, int t0, int cn, int h,
@@ -231,6 +226,10 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
             cr.k[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
         }
     }
+    // beta of token warp * 4 + lane (lanes 0-3); the address stays inside the chunk for every lane
+    const int ib = warp * 4 + ((l4 >> 2) & 3);
+    const bool okb = l4 < 16 && ib < cn;
+    cr.beta = okb ? __ldg(p.beta + (size_t)(bos + t0 + (okb ? ib : 0)) * p.H + h) : 0.f;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -295,7 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sb + S_V, &tmap_v, tma_bar, 0, h, bos + chunk * C);
         tma_load_3d(sb + S_V + 8192, &tmap_v, tma_bar, 64, h, bos + chunk * C);
     };
-    if (tid == 0 && nchunks > 0) issue_v(0);
+    int v_pending = -1;  // chunk whose V tile is in flight (thread 0 only)
+    if (tid == 0 && nchunks > 0) {
+        issue_v(0);
+        v_pending = 0;
+    }
 
     {  // initial state -> S^T accumulator and its hi/lo copy; O^T = 0
         const int c0 = wg * 32;
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // small buffers, each warp's decay totals per key channel into the scan buffer.
     // The 8 sums of squares of a warp's 4 tokens are reduced with a reduce-scatter
     // (9 shuffles); lanes 4v..4v+3 end with sum v (q of tokens 0-3, then k).
-    auto prep_norms = [&](const ChunkRegs &c, int t0n, int cnn) {
+    auto prep_norms = [&](const ChunkRegs &c) {
         float a[8];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -360,10 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 fs[F_RK + warp * 4 + v - 4] = sc;
         }
-        if (lane < 4) {
-            const int i = warp * 4 + lane;
-            fs[F_BETA + i] = (i < cnn) ? p.beta[(size_t)(bos + t0n + i) * H + h] : 0.f;
-        }
+        if (lane < 4) fs[F_BETA + warp * 4 + lane] = c.beta;
         float4 t = c.g[0];
 #pragma unroll
         for (int r = 1; r < 4; ++r) {
@@ -415,28 +415,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 km[e] = kh * __expf(-o4[e]);
                 kgv[r][e] = km[e] * egam[e];
             }
-            st_tile4(sb + S_KQH, sb + S_KQL, 128, i, l4, kd[0], kd[1], kd[2], kd[3]);
-            st_tile4(sb + S_KQH, sb + S_KQL, 128, 64 + i, l4, qd[0], qd[1], qd[2], qd[3]);
+            // rows i and 64 + i of the 128-row tiles share the swizzle phase, 8 KB apart
+            const uint32_t off = sw128_off(i, l4, 128);
             uint32_t h0, l0, h1, l1;
+            split2(kd[0], kd[1], h0, l0);
+            split2(kd[2], kd[3], h1, l1);
+            st_shared_v2(sb + S_KQH + off, h0, h1);
+            st_shared_v2(sb + S_KQL + off, l0, l1);
+            split2(qd[0], qd[1], h0, l0);
+            split2(qd[2], qd[3], h1, l1);
+            st_shared_v2(sb + S_KQH + off + 8192, h0, h1);
+            st_shared_v2(sb + S_KQL + off + 8192, l0, l1);
             split2(km[0], km[1], h0, l0);
             split2(km[2], km[3], h1, l1);
-            st_shared_v2(sb + S_KM + sw128_off(i, l4, 128), h0, h1);
-            st_shared_v2(sb + S_KM + sw128_off(64 + i, l4, 128), l0, l1);
+            st_shared_v2(sb + S_KM + off, h0, h1);
+            st_shared_v2(sb + S_KM + off + 8192, l0, l1);
         }
         return oor;
     };
 
-    auto st_kg = [&](const float (&kgv)[4][4]) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            st_tile4(sb + S_PKGH, sb + S_PKGL, 64, warp * 4 + r, 64 + l4, kgv[r][0], kgv[r][1], kgv[r][2], kgv[r][3]);
-    };
+    auto st_kg = [&](const float (&kgv)[4][4]) { st_kgt(sb, l4, warp * 4, kgv); };
 
     // ---- first chunk's preparation (later chunks are prepared inside the previous
     // chunk's tensor-core waits)
     int oor_next = 0;
     if (nchunks > 0) {
-        prep_norms(cr, 0, min(C, len));
+        prep_norms(cr);
         __syncthreads();
         float kgv[4][4];
         oor_next = prep_tiles(cr, kgv);
@@ -497,9 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const int i = m - 64;
+                float x[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    st_pt(sm, i, j0 + c, (j0 + c <= i) ? __uint_as_float(r1[c]) + __uint_as_float(r2[c]) : 0.f);
+                for (int c = 0; c < 16; ++c) x[c] = (j0 + c <= i) ? __uint_as_float(r1[c]) + __uint_as_float(r2[c]) : 0.f;
+                st_tile8(sb + S_PKGH, sb + S_PKGL, 192, i, j0, x);
+                st_tile8(sb + S_PKGH, sb + S_PKGL, 192, i, j0 + 8, x + 8);
             }
         } else {
             // exact grams with pairwise exponentials (decay range too wide for Km)
@@ -514,16 +520,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncthreads();
+            {  // Kg from the exact G (the fast formula overflows here)
+                float kg[4][4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {  // Kg from the exact G (the fast formula overflows here)
-                const int i = warp * 4 + r;
-                float kg[4];
+                for (int r = 0; r < 4; ++r) {
+                    const int i = warp * 4 + r;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float kv = i < cn ? __bfloat162float(kgl[((size_t)(bos + t0 + i) * H + h) * DK + l4 + c]) : 0.f;
-                    kg[c] = kv * fs[F_RK + i] * __expf(Gs[63 * 128 + l4 + c] - Gs[i * 128 + l4 + c]);
+                    for (int c = 0; c < 4; ++c) {
+                        const float kv = i < cn ? __bfloat162float(kgl[((size_t)(bos + t0 + i) * H + h) * DK + l4 + c]) : 0.f;
+                        kg[r][c] = kv * fs[F_RK + i] * __expf(Gs[63 * 128 + l4 + c] - Gs[i * 128 + l4 + c]);
+                    }
                 }
-                st_tile4(sb + S_PKGH, sb + S_PKGL, 64, i, 64 + l4, kg[0], kg[1], kg[2], kg[3]);
+                st_kgt(sb, l4, warp * 4, kg);
             }
             float *Pf = Tsm;  // P in fp32, converted to the tile below
             for (int i = warp; i < C; i += 16) {
@@ -562,15 +570,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncthreads();
             {
                 const int i = tid >> 3, j0 = (tid & 7) * 8;
+                float x[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) st_pt(sm, i, j0 + c, Pf[i * AP + j0 + c]);
+                for (int c = 0; c < 8; ++c) x[c] = Pf[i * AP + j0 + c];
+                st_tile8(sb + S_PKGH, sb + S_PKGL, 192, i, j0, x);
             }
         }
         __syncthreads();
 
         if (tid == 0) {
             // ================= R^T = V^T I + S^T (-Kd)^T, O^T = S^T Qd^T (while warps 1-15 solve T)
-            if (!mbar_wait(tma_bar, (uint32_t)par, kPolls)) failed = 1;
+            if (mbar_wait(tma_bar, (uint32_t)par, kPolls))
+                v_pending = -1;
+            else
+                failed = 1;
             fence_after_sync();
             const uint32_t id_mn = idesc_bf16(128, 64, true, false);
 #pragma unroll 1
@@ -619,7 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ================= R pass: R^T (lane v, column j) -> hi/lo operand in TMEM
         if (!wait_group(bar_r, par)) failed = 1;
-        if (tid == 0 && ch + 1 < nchunks) issue_v(ch + 1);  // the V tile has been read
+        if (tid == 0 && ch + 1 < nchunks && !failed) {  // the V tile has been read
+            issue_v(ch + 1);
+            v_pending = ch + 1;
+        }
         {
             uint32_t r[16], hi[8], lo[8];
             tmem_ld16(tb + lane_off + T_R + wg * 16, r);
@@ -649,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // while D runs: the next chunk's norms, beta and decay totals
-        if (ch + 1 < nchunks) prep_norms(cr, t0 + C, min(C, len - t0 - C));
+        if (ch + 1 < nchunks) prep_norms(cr);
         // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
         if (!wait_group(bar_d, par)) failed = 1;
         {
@@ -663,10 +679,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
             tmem_st8(tb + lane_off + T_DH + wg * 8, hi);
             tmem_st8(tb + lane_off + T_DL + wg * 8, lo);
+            const float4 *ge = reinterpret_cast<const float4 *>(fs + F_GEXP + c0);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                s1[c] = __float_as_uint(__uint_as_float(s1[c]) * fs[F_GEXP + c0 + c]);
-                s2[c] = __float_as_uint(__uint_as_float(s2[c]) * fs[F_GEXP + c0 + 16 + c]);
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const float4 a = ge[c4], b = ge[4 + c4];
+                s1[4 * c4 + 0] = __float_as_uint(__uint_as_float(s1[4 * c4 + 0]) * a.x);
+                s1[4 * c4 + 1] = __float_as_uint(__uint_as_float(s1[4 * c4 + 1]) * a.y);
+                s1[4 * c4 + 2] = __float_as_uint(__uint_as_float(s1[4 * c4 + 2]) * a.z);
+                s1[4 * c4 + 3] = __float_as_uint(__uint_as_float(s1[4 * c4 + 3]) * a.w);
+                s2[4 * c4 + 0] = __float_as_uint(__uint_as_float(s2[4 * c4 + 0]) * b.x);
+                s2[4 * c4 + 1] = __float_as_uint(__uint_as_float(s2[4 * c4 + 1]) * b.y);
+                s2[4 * c4 + 2] = __float_as_uint(__uint_as_float(s2[4 * c4 + 2]) * b.z);
+                s2[4 * c4 + 3] = __float_as_uint(__uint_as_float(s2[4 * c4 + 3]) * b.w);
             }
             tmem_st16(tb + lane_off + T_S + c0, s1);
             tmem_st16(tb + lane_off + T_S + c0 + 16, s2);
@@ -679,13 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= [O|S]^T += D^T [P^T | Kg]
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t id192 = idesc_bf16(128, 192, false, true);
+            const uint32_t id192 = idesc_bf16(128, 192, false, false);
 #pragma unroll 1
             for (int cb = 0; cb < 3; ++cb)
 #pragma unroll 1
                 for (int s = 0; s < 4; ++s)
                     mma_ts(tb + T_O, tb + (combo_a(cb) ? T_DL : T_DH) + s * 8,
-                           sdesc((combo_b(cb) ? sb + S_PKGL : sb + S_PKGH) + s * 2048, 8192, 1024), id192, 1u);
+                           sdesc((combo_b(cb) ? sb + S_PKGL : sb + S_PKGH) + s * 32, 16, 1024), id192, 1u);
             mma_commit(bar_s);
         }
         __syncwarp();
@@ -763,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             atomicAdd(&g_chunk_tc_timeouts, 1);
             mma_commit(drain_bar);  // arrives once the tensor-core work already issued has drained
+            if (v_pending >= 0) mbar_wait(tma_bar, (uint32_t)(v_pending & 1), kPolls);  // V copy in flight
         }
         __syncthreads();
         mbar_wait(drain_bar, 0, kPolls);
