@@ -57,6 +57,11 @@ def _load():
                 P, P, P, ctypes.c_double, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
             ]
             lib.kda_oracle_gated_rmsnorm.restype = ctypes.c_int
+            lib.kda_oracle_short_conv.argtypes = [
+                P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int,
+            ]
+            lib.kda_oracle_short_conv.restype = ctypes.c_int
             lib.kda_oracle_version.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -138,6 +143,45 @@ def gated_rmsnorm(o, gate, w, eps=1e-5):
     if rc != 0:
         raise RuntimeError(f"kda_oracle_gated_rmsnorm failed with {rc}")
     return y
+
+
+def short_conv(x, weight, bias=None, conv_state=None, *, cu_seqlens=None, activation="silu"):
+    """Causal depthwise convolution along the sequence (+ SiLU), fp64.
+
+    x [B,T,D] (or [T,D] packed varlen), weight [D,W], bias [D] or None, conv_state
+    [N,W-1,D] or None (the W-1 inputs before each sequence, oldest first).
+    Returns ``(y [.., T, D] float64, final_state [N, W-1, D] float64)``.
+    Formula and page citations: ``kda_oracle_short_conv`` in kda_oracle.c.
+    """
+    x = _f32(x)
+    if x.ndim == 2:
+        x = x[None]
+    B, T, D = x.shape
+    w = _f64(weight)
+    if w.ndim != 2 or w.shape[0] != D:
+        raise ValueError("weight must be [D, W]")
+    W = w.shape[1]
+    b = None if bias is None else _f64(bias)
+    if b is not None and b.shape != (D,):
+        raise ValueError("bias must be [D]")
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+        if B != 1 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+            raise ValueError("varlen needs batch 1 and cu_seqlens from 0 to T, non-decreasing")
+        N = cu.shape[0] - 1
+    else:
+        cu, N = None, B
+    s0 = None if conv_state is None else _f64(conv_state)
+    if s0 is not None and s0.shape != (N, W - 1, D):
+        raise ValueError(f"conv_state must be {(N, W - 1, D)}")
+    y = np.zeros((B, T, D), dtype=np.float64)
+    sf = np.zeros((N, W - 1, D), dtype=np.float64)
+    act = {"silu": 1, "swish": 1, None: 0, "none": 0, "identity": 0}[activation]
+    rc = _load().kda_oracle_short_conv(_ptr(x), _ptr(w), _ptr(b), _ptr(s0), _ptr(y), _ptr(sf), _ptr(cu),
+                                       N if cu is not None else 0, B, T, D, W, act)
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_short_conv failed with {rc}")
+    return y, sf
 
 
 def version() -> int:

@@ -304,3 +304,65 @@ int kda_oracle_gated_rmsnorm(const double *o, const float *gate, const float *w,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Short convolution                                                          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Causal depthwise convolution along the sequence with an optional SiLU, the
+ * preprocessing of q, k and v.
+ *
+ * nnterp encyclopedia "Kimi-Linear", section "Printout": the layer's conv1d is
+ * Conv1d(12288, 12288, kernel_size=(4,), stride=(1,), padding=(3,), groups=12288,
+ * bias=False) -- one filter of 4 taps per channel, padded by 3 positions before
+ * the first token; the first T outputs are the causal ones.  Kimi-K3 atlas
+ * "gate-project (decode, P = 1000)", section "Code": q_conv1d, k_conv1d and
+ * v_conv1d are ShortConvolution(hidden_size, kernel_size=short_conv_kernel_size,
+ * activation='silu'), with short_conv_kernel_size = 4 in the config.
+ *
+ * For each sequence and channel c (cross-correlation, as Conv1d computes it):
+ *   y[t][c] = act( bias[c] + sum_{w=0}^{W-1} weight[c][w] * x[t - (W-1) + w][c] )
+ * A position before the sequence start takes its input from the conv state (the
+ * W-1 inputs before the sequence, oldest first) or zero; act(z) = z / (1 + e^-z)
+ * (SiLU) or z.  The state afterwards holds the last W-1 inputs, oldest first.
+ *
+ *   x         [B, T, D] float (bf16 values widened); varlen: B = 1, n_seqs > 0
+ *   weight    [D, W] double        bias [D] double or NULL
+ *   state_in  [N, W-1, D] double or NULL      state_out [N, W-1, D] double or NULL
+ *   y         [B, T, D] double
+ */
+int kda_oracle_short_conv(const float *x, const double *weight, const double *bias,
+                          const double *state_in, double *y, double *state_out,
+                          const int64_t *cu_seqlens, int n_seqs, int B, int T, int D, int W, int act) {
+    if (!weight || D <= 0 || W < 1 || W > 64 || B < 0 || T < 0) return -1;
+    const int N = cu_seqlens ? n_seqs : B;
+    double hist[64];
+    for (int n = 0; n < N; ++n) {
+        int64_t bos, len;
+        if (cu_seqlens) {
+            bos = cu_seqlens[n];
+            len = cu_seqlens[n + 1] - cu_seqlens[n];
+        } else {
+            bos = (int64_t)n * T;
+            len = T;
+        }
+        if (len < 0) return -2;
+        for (int c = 0; c < D; ++c) {
+            for (int w = 0; w < W - 1; ++w)
+                hist[w] = state_in ? state_in[((size_t)n * (W - 1) + w) * D + c] : 0.0;
+            for (int64_t t = 0; t < len; ++t) {
+                const double xt = (double)x[(size_t)(bos + t) * D + c];
+                double z = bias ? bias[c] : 0.0;
+                for (int w = 0; w < W - 1; ++w) z += weight[(size_t)c * W + w] * hist[w];
+                z += weight[(size_t)c * W + W - 1] * xt;
+                y[(size_t)(bos + t) * D + c] = act ? z / (1.0 + exp(-z)) : z;
+                for (int w = 0; w + 1 < W - 1; ++w) hist[w] = hist[w + 1];
+                if (W > 1) hist[W - 2] = xt;
+            }
+            if (state_out)
+                for (int w = 0; w < W - 1; ++w) state_out[((size_t)n * (W - 1) + w) * D + c] = hist[w];
+        }
+    }
+    return 0;
+}
