@@ -180,6 +180,44 @@ kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,
                              kda_dtype gate_dtype, const float *w, float eps, void *y,
                              kda_dtype y_dtype, int64_t rows, int H, int V, void *stream);
 
+/*
+ * kda_short_conv_fwd -- causal depthwise short convolution along the sequence,
+ * with an optional SiLU: the preprocessing of q, k and v before the delta rule.
+ *
+ * Pages: nnterp encyclopedia "Kimi-Linear", section "Printout" (the layer's conv1d
+ * is Conv1d(12288, 12288, kernel_size=(4,), padding=(3,), groups=12288,
+ * bias=False): one filter per channel, padded by 3 before the first token, the
+ * first T outputs kept); Kimi-K3 atlas "gate-project (decode, P = 1000)", section
+ * "Code" (q_conv1d, k_conv1d, v_conv1d = ShortConvolution(hidden_size,
+ * kernel_size=short_conv_kernel_size = 4, activation='silu')).
+ *
+ *   y[t][c] = act( bias[c] + sum_{w<W} weight[c][w] * x[t - (W-1) + w][c] )
+ *
+ * Positions before a sequence read its conv state (the W-1 inputs before it,
+ * oldest first) or zero; act is SiLU (z / (1 + e^-z)) when activation = 1, the
+ * identity when 0.
+ *
+ * Dense mode (cu_seqlens == NULL): N = B sequences of T tokens.
+ *   x       [B, T, D] x_dtype      y [B, T, D] y_dtype (must not overlap x)
+ *   weight  [D, W] float (the Conv1d weight [D, 1, W] without its middle axis)
+ *   bias    [D] float or NULL
+ *   conv_state_in  [N, W-1, D] float or NULL (zero history)
+ *   conv_state_out [N, W-1, D] float or NULL: the last W-1 inputs of each
+ *                  sequence, oldest first (a sequence shorter than W-1 keeps part
+ *                  of its old state).  It may be the same buffer as
+ *                  conv_state_in only for a decode step (dense, T = 1); otherwise
+ *                  the two must not overlap.
+ * Varlen mode: as kda_chunk_fwd (B = 1, T packed, cu_seqlens device int32
+ *   [n_seqs + 1], optional host copy cu_seqlens_host, which is then checked).
+ * A decode step is T = 1 with both states given.  Supported: W in {2, 3, 4},
+ * D a multiple of 8, B * T < 65535 * 64.  Returns a kda_status.
+ */
+kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *weight, const float *bias,
+                              const float *conv_state_in, float *conv_state_out, void *y,
+                              kda_dtype y_dtype, const int32_t *cu_seqlens,
+                              const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int D, int W,
+                              int activation, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "recurrent_fwd", "recurrent_step", "gated_rmsnorm", "launch_count",
+__all__ = ["chunk_fwd", "recurrent_fwd", "recurrent_step", "gated_rmsnorm", "short_conv", "launch_count",
            "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -64,7 +64,9 @@ def _load():
         lib.kda_recurrent_step.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, F,
                                            P, P]
         lib.kda_gated_rmsnorm.argtypes = [P, I, P, I, P, F, P, I, ctypes.c_int64, I, I, P]
-        for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm"):
+        lib.kda_short_conv_fwd.argtypes = [P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P]
+        for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
+                   "kda_short_conv_fwd"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_launch_count.restype = ctypes.c_uint64
@@ -272,3 +274,39 @@ def gated_rmsnorm(o, gate, w, eps=1e-5, *, out_dtype=torch.float32, y=None):
     _check(lib.kda_gated_rmsnorm(_ptr(o), _dt(o), _ptr(gate), _dt(gate), _ptr(w), float(eps), _ptr(y), _dt(y),
                                  rows, H, V, _stream()))
     return _to_host((y,), host)[0]
+
+
+def short_conv(x, weight, bias=None, conv_state=None, *, cu_seqlens=None, activation="silu",
+               output_final_state=True, out_dtype=None, y=None, final_state=None):
+    """Causal depthwise short convolution (+ SiLU) along the sequence.
+
+    x [B,T,D] (bf16 or fp32); weight [D,W] (or the Conv1d weight [D,1,W]); bias [D] or
+    None; conv_state [N,W-1,D] fp32 or None (the W-1 inputs before each sequence,
+    oldest first).  With ``cu_seqlens`` B must be 1.  A decode step is T = 1;
+    ``final_state=conv_state`` then updates the state in place.
+    Returns (y [B,T,D], final_state [N,W-1,D] or None)."""
+    lib = _load()
+    host = x.device.type != "cuda"
+    dev = _device_of(x, conv_state)
+    dests = (y, final_state) if host else None
+    if host:
+        y, final_state = _dev_out(y), _dev_out(final_state)
+    x = _prep(x, dev)
+    if weight.dim() == 3:
+        weight = weight[:, 0, :]
+    weight = _prep(weight, dev, torch.float32)
+    bias = _prep(bias, dev, torch.float32)
+    conv_state = _prep(conv_state, dev, torch.float32)
+    B, T, D = x.shape
+    W = weight.shape[1]
+    cu_d, cu_h, n_seqs = _cu(cu_seqlens, dev)
+    N = n_seqs if cu_d is not None else B
+    if y is None:
+        y = torch.empty((B, T, D), device=dev, dtype=out_dtype or x.dtype)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, W - 1, D), device=dev, dtype=torch.float32)
+    act = {"silu": 1, "swish": 1, None: 0, "none": 0, "identity": 0}[activation]
+    _check(lib.kda_short_conv_fwd(
+        _ptr(x), _dt(x), _ptr(weight), _ptr(bias), _ptr(conv_state), _ptr(final_state), _ptr(y), _dt(y),
+        _ptr(cu_d), _ptr(cu_h), n_seqs, B, T, D, W, act, _stream()))
+    return _to_host((y, final_state), host, dests)

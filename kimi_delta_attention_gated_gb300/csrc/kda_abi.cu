@@ -253,4 +253,54 @@ kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,
                                      y_dtype == KDA_BF16, rows, H, V, (cudaStream_t)stream);
 }
 
+kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *weight, const float *bias,
+                              const float *conv_state_in, float *conv_state_out, void *y,
+                              kda_dtype y_dtype, const int32_t *cu_seqlens,
+                              const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int D, int W,
+                              int activation, void *stream) {
+    kda::g_err[0] = 0;
+    const char *fn = "kda_short_conv_fwd";
+    const int64_t rows = (int64_t)B * T;
+    KDA_REQUIRE(B > 0 && T >= 0 && D > 0, KDA_ERR_INVALID_ARG, "%s: need B > 0, T >= 0, D > 0", fn);
+    KDA_REQUIRE(rows == 0 || (x && y), KDA_ERR_INVALID_ARG, "%s: x and y must not be NULL", fn);
+    KDA_REQUIRE(weight, KDA_ERR_INVALID_ARG, "%s: weight must not be NULL", fn);
+    KDA_REQUIRE(dtype_ok(x_dtype) && dtype_ok(y_dtype), KDA_ERR_UNSUPPORTED, "%s: unsupported dtype", fn);
+    KDA_REQUIRE(W >= 2 && W <= 4, KDA_ERR_UNSUPPORTED, "%s: W=%d (supported: 2, 3, 4)", fn, W);
+    KDA_REQUIRE(D % 8 == 0, KDA_ERR_UNSUPPORTED, "%s: D=%d must be a multiple of 8", fn, D);
+    KDA_REQUIRE(activation == 0 || activation == 1, KDA_ERR_INVALID_ARG, "%s: activation must be 0 or 1", fn);
+    KDA_REQUIRE(rows <= (int64_t)65535 * 64, KDA_ERR_UNSUPPORTED, "%s: B*T=%lld too large", fn, (long long)rows);
+    const void *ptrs[] = {x, weight, bias, conv_state_in, conv_state_out, y, cu_seqlens};
+    for (const void *ptr : ptrs)
+        KDA_REQUIRE(!ptr || aligned16(ptr), KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);
+    const size_t xbytes = (size_t)rows * D * (x_dtype == KDA_BF16 ? 2 : 4);
+    const size_t ybytes = (size_t)rows * D * (y_dtype == KDA_BF16 ? 2 : 4);
+    KDA_REQUIRE(rows == 0 || (const char *)y + ybytes <= (const char *)x || (const char *)x + xbytes <= (const char *)y,
+                KDA_ERR_INVALID_ARG, "%s: y must not overlap x", fn);
+    int N = B;
+    if (cu_seqlens) {
+        KDA_REQUIRE(B == 1 && n_seqs > 0, KDA_ERR_INVALID_ARG, "%s: varlen needs B == 1 and n_seqs > 0", fn);
+        if (cu_seqlens_host) {
+            KDA_REQUIRE(cu_seqlens_host[0] == 0, KDA_ERR_INVALID_ARG, "%s: cu_seqlens[0] must be 0", fn);
+            for (int i = 0; i < n_seqs; ++i)
+                KDA_REQUIRE(cu_seqlens_host[i + 1] >= cu_seqlens_host[i], KDA_ERR_INVALID_ARG,
+                            "%s: cu_seqlens must not decrease (entry %d)", fn, i + 1);
+            KDA_REQUIRE(cu_seqlens_host[n_seqs] == T, KDA_ERR_INVALID_ARG, "%s: cu_seqlens[n_seqs] = %d but T = %d",
+                        fn, cu_seqlens_host[n_seqs], T);
+        }
+        N = n_seqs;
+    } else {
+        KDA_REQUIRE(!cu_seqlens_host, KDA_ERR_INVALID_ARG, "%s: cu_seqlens_host given without cu_seqlens", fn);
+    }
+    if (conv_state_in && conv_state_out) {
+        const size_t sbytes = (size_t)N * (W - 1) * D * sizeof(float);
+        const char *a = (const char *)conv_state_in, *b = (const char *)conv_state_out;
+        const bool overlap = a < b + sbytes && b < a + sbytes;
+        KDA_REQUIRE(!overlap || (a == b && !cu_seqlens && T == 1), KDA_ERR_INVALID_ARG,
+                    "%s: conv_state_out may alias conv_state_in only for a decode step (dense, T = 1)", fn);
+    }
+    return kda::launch_short_conv(x, x_dtype == KDA_BF16, weight, bias, conv_state_in, conv_state_out, y,
+                                  y_dtype == KDA_BF16, cu_seqlens, N, rows, T, D, W, activation,
+                                  (cudaStream_t)stream);
+}
+
 }  // extern "C"

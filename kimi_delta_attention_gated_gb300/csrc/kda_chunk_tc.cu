@@ -817,20 +817,22 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
+EncodeTiledFn encode_fn() { return reinterpret_cast<EncodeTiledFn>(tensor_map_encoder()); }
+
+}  // namespace
+
+void *tensor_map_encoder() {
+    static void *fn = nullptr;
     if (!fn) {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+            fn = ptr;
     }
     return fn;
 }
-
-}  // namespace
 
 bool chunk_tc_supported(int K, int V, int chunk) { return K == DK && V == DV && chunk == C; }
 

@@ -87,6 +87,13 @@ kda_status launch_chunk_tc(const SeqParams &p, int K, int V, int chunk, cudaStre
 kda_status launch_gated_rmsnorm(const void *o, int o_bf16, const void *gate, int gate_bf16,
                                 const float *w, float eps, void *y, int y_bf16, int64_t rows,
                                 int H, int V, cudaStream_t st);
+kda_status launch_short_conv(const void *x, int x_bf16, const float *w, const float *bias, const float *s0,
+                             float *sT, void *y, int y_bf16, const int32_t *cu, int N, int64_t rows, int T,
+                             int D, int W, int act, cudaStream_t st);
 bool chunk_tc_supported(int K, int V, int chunk);
+// cuTensorMapEncodeTiled from the driver (no link against libcuda), or null.
+void *tensor_map_encoder();
+// Streaming multiprocessors of the current device.
+int sm_count();
 
 }  // namespace kda

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const void *o, 
     }
 }
 
+}  // namespace
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -55,8 +57,6 @@ int sm_count() {
     }
     return n;
 }
-
-}  // namespace
 
 kda_status launch_gated_rmsnorm(const void *o, int o_bf16, const void *gate, int gate_bf16,
                                 const float *w, float eps, void *y, int y_bf16, int64_t rows,

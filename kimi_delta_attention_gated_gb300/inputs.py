@@ -17,6 +17,13 @@ Workloads (names used by the tests and the benchmark):
   decode    B=256 one token each, H=96, d=128, state N(0, 0.02^2),
             gate logits N(0,1), norm weight 1 + N(0, 0.1^2), eps 1e-5
   long      B=2  T=65536  H=96  d=128  chunk 64, zero initial state, gated norm
+
+Short-convolution inputs (make_conv_inputs): x is the q, k and v projections side by
+side, D = 3 * 96 * 128 = 36864 channels of N(0, 1) values in bf16; the filter is
+Conv1d's default initialisation for a depthwise filter of 4 taps, U(-1/2, 1/2)
+(bound 1/sqrt(fan_in), fan_in = 4); the conv state N(0, 1) (earlier inputs).
+  conv_prefill  B=1   T=8192  D=36864  W=4, zero state
+  conv_decode   B=256 T=1     D=36864  W=4, state given (updated in place)
 """
 from __future__ import annotations
 
@@ -125,3 +132,35 @@ def make_inputs(w: Workload | str, device="cpu", *, T: int | None = None, H: int
         out["gate"] = torch.randn((B, T, H, V), generator=gen, device=device).to(torch.bfloat16)
         out["norm_w"] = 1.0 + 0.1 * torch.randn((V,), generator=gen, device=device)
     return out
+
+
+CONV_WORKLOADS = {
+    "conv_prefill": dict(seed=5, B=1, T=8192, D=3 * 96 * 128, W=4, state=False),
+    "conv_decode": dict(seed=6, B=256, T=1, D=3 * 96 * 128, W=4, state=True),
+}
+
+
+def make_conv_inputs(w: str | None = None, device="cpu", *, B: int | None = None, T: int | None = None,
+                     D: int | None = None, W: int | None = None, lengths: list | None = None,
+                     state: bool | None = None, bias: bool = False, seed: int | None = None) -> dict:
+    """Seeded inputs for the short convolution: x [B,T,D] bf16, weight [D,W] fp32,
+    bias [D] or None, conv_state [N,W-1,D] fp32 or None, cu_seqlens (host int32) for varlen."""
+    cfg = dict(CONV_WORKLOADS[w]) if w else dict(seed=7, B=1, T=64, D=256, W=4, state=False)
+    B = cfg["B"] if B is None else B
+    T = cfg["T"] if T is None else T
+    D = cfg["D"] if D is None else D
+    W = cfg["W"] if W is None else W
+    state = cfg["state"] if state is None else state
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg["seed"] if seed is None else seed)
+    cu = None
+    N = B
+    if lengths is not None:
+        cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+        B, T, N = 1, int(cu[-1]), len(lengths)
+    x = torch.randn((B, T, D), generator=gen, device=device).to(torch.bfloat16)
+    weight = torch.empty((D, W), device=device).uniform_(-W ** -0.5, W ** -0.5, generator=gen)
+    b = torch.empty((D,), device=device).uniform_(-W ** -0.5, W ** -0.5, generator=gen) if bias else None
+    s0 = torch.randn((N, W - 1, D), generator=gen, device=device) if state else None
+    return dict(x=x, weight=weight, bias=b, conv_state=s0, cu_seqlens=cu, B=B, T=T, D=D, W=W, N=N)

@@ -35,7 +35,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = declared_symbols()
-    for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm"):
+    for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
+               "kda_short_conv_fwd"):
         assert fn in names
 
 
@@ -153,3 +154,38 @@ def test_python_binding_fails_loudly_without_gpu():
     q = torch.zeros(1, 4, 1, 32, dtype=torch.bfloat16)
     with pytest.raises(Exception):
         kda.chunk_fwd(q, q, q, torch.zeros(1, 4, 1, 32), torch.zeros(1, 4, 1), chunk=16)
+
+
+def conv_call(lib, **over):
+    a = dict(x=FAKE, xdt=BF16, w=FAKE, b=None, s0=None, sT=None, y=FAKE + (1 << 24), ydt=BF16, cu=None,
+             cu_host=None, n_seqs=0, B=1, T=64, D=256, W=4, act=1)
+    a.update(over)
+    return lib.kda_short_conv_fwd(a["x"], a["xdt"], a["w"], a["b"], a["s0"], a["sT"], a["y"], a["ydt"], a["cu"],
+                                  a["cu_host"], a["n_seqs"], a["B"], a["T"], a["D"], a["W"], a["act"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(x=None), INVALID),
+    (dict(w=None), INVALID),
+    (dict(W=5), UNSUPPORTED),
+    (dict(W=1), UNSUPPORTED),
+    (dict(D=100), UNSUPPORTED),                     # D must be a multiple of 8
+    (dict(D=0), INVALID),
+    (dict(xdt=5), UNSUPPORTED),
+    (dict(act=2), INVALID),
+    (dict(x=FAKE + 4), INVALID),                    # misaligned
+    (dict(y=FAKE), INVALID),                        # y overlaps x
+    (dict(s0=FAKE + (1 << 26), sT=FAKE + (1 << 26)), INVALID),   # in place only for a decode step
+    (dict(cu=FAKE, n_seqs=0), INVALID),
+    (dict(cu=FAKE, n_seqs=2, B=2), INVALID),
+    (dict(cu_host=FAKE), INVALID),
+    (dict(B=70000, T=64), UNSUPPORTED),             # grid limit
+])
+def test_short_conv_rejects(lib, over, code):
+    assert conv_call(lib, **over) == code
+    assert lib.kda_last_error()
+
+
+def test_short_conv_rejects_bad_cu_seqlens(lib):
+    arr, ptr = cu_host([0, 9, 4, 64])
+    assert conv_call(lib, cu=FAKE, cu_host=ptr, n_seqs=3) == INVALID
