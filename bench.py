@@ -267,6 +267,40 @@ def bench_decode(args, world, peaks):
                          "peak_source": peaks["source"]}}
 
 
+def bench_short_conv(args, world, peaks):
+    """The q/k/v short convolution (causal depthwise, 4 taps, SiLU): one 8192-token prompt
+    (state out) and one decode step of 256 sequences (state updated in place), each over
+    the 3 x 12288 channels of q, k and v side by side."""
+    import torch
+    import kimi_delta_attention_gated_gb300 as kda
+    from kimi_delta_attention_gated_gb300.inputs import make_conv_inputs
+    out = {}
+    for name in ("conv_prefill", "conv_decode"):
+        d = make_conv_inputs(name, device="cuda")
+        B, T, D, W, N = d["B"], d["T"], d["D"], d["W"], d["N"]
+        y = torch.empty_like(d["x"])
+        st = d["conv_state"]
+        sf = st if st is not None else torch.empty((N, W - 1, D), device="cuda")
+        fn = lambda: kda.short_conv(d["x"], d["weight"], None, st, y=y, final_state=sf)
+        steps = max(args.steps, 20)
+        r = time_steps(fn, steps, args.warmup, world)
+        kernel_ms = r["call_ms"] / max(1, r["launches"] // steps)
+        state_bytes = N * (W - 1) * D * 4 * (2 if st is not None else 1)
+        algo_bytes = B * T * D * (2 + 2) + state_bytes + D * W * 4
+        achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+        out[name] = {
+            "metric": "short-conv tokens/s", "value": world * B * T / (r["ms_per_step"] * 1e-3), "unit": "tokens/s",
+            "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
+            "config": {"workload": f"{name} B={B} T={T} D={D} (q, k, v) W={W} SiLU bf16 in/out",
+                       "l2_flush": "inputs + outputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": measured_traffic(name, B * T * D),
+                         "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
+                         "peak_source": peaks["source"]}}
+    return out
+
+
 def bench_e2e(args, world, d):
     """Same prefill through the public call with pinned host inputs and host outputs."""
     import torch
@@ -352,12 +386,13 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -372,13 +407,14 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only == "decode":
-        dec = bench_decode(args, world, peaks)
+    if args.only in ("decode", "conv"):
+        res = bench_decode(args, world, peaks) if args.only == "decode" else bench_short_conv(args, world, peaks)
         if rank == 0:
-            print(json.dumps(dec), flush=True)
+            print(json.dumps(res), flush=True)
         return
     pre, d = bench_prefill(args, world, rank, peaks)
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
+    conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
     e2e = None if (args.no_e2e or args.only == "prefill") else bench_e2e(args, world, d)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
@@ -392,6 +428,7 @@ def main():
         "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": pre["config"],
         "roofline": pre["roofline"], "roofline_tensor": pre["roofline_tensor"], "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
+        "short_conv": conv,
         "gpu": torch.cuda.get_device_name(),
     }
     print(json.dumps(line), flush=True)

@@ -43,7 +43,7 @@ constexpr int kCh = 256;     // channels per tile (the TMA box width)
 constexpr int kVec = 4;      // channels per thread
 constexpr int kTokPer = 16;  // tokens per thread: 64 channel groups x 4 token quarters = 256 threads
 constexpr uint32_t kPolls = 1u << 24;  // bound on the tile's mbarrier wait
-static_assert((kCh / kVec) * (kTile / kTokPer) == kThreads, "thread map");
+static_assert((kCh / kVec) * (kTile / kTokPer) == kThreads && kVec == 4, "thread map");
 
 // Set by a CTA whose wait for its TMA tile gave up (its outputs are then NaN).
 __device__ int g_short_conv_timeouts = 0;
@@ -157,16 +157,79 @@ __device__ __forceinline__ void load_filter(const ConvParams &p, int c0, float (
     for (int e = 0; e < kVec; ++e) bv[e] = p.bias ? __ldg(p.bias + c0 + e) : 0.f;
 }
 
-template <int W>
+// SiLU as z / (1 + e^-z) with the fast divide: for z below about -88 the
+// denominator is infinite and the result is -0, the correctly rounded limit.
+template <int W, bool ACT>
 __device__ __forceinline__ void conv_point(const float (&wv)[W][kVec], const float (&bv)[kVec],
-                                           const float (&win)[W - 1][kVec], const float (&xv)[kVec], int act,
+                                           const float (&win)[W - 1][kVec], const float (&xv)[kVec],
                                            float (&z)[kVec]) {
 #pragma unroll
     for (int e = 0; e < kVec; ++e) {
         float a = fmaf(wv[W - 1][e], xv[e], bv[e]);
 #pragma unroll
         for (int j = 0; j < W - 1; ++j) a = fmaf(wv[j][e], win[j][e], a);
-        z[e] = act ? a / (1.f + __expf(-a)) : a;
+        z[e] = ACT ? __fdividef(a, 1.f + __expf(-a)) : a;
+    }
+}
+
+// The tokens [ta, tb) of one tile for this thread's kVec channels: the window of the
+// W-1 previous inputs slides in registers; sequence boundaries are counted down.
+template <int W, bool XB, bool YB, bool ACT>
+__device__ __forceinline__ void conv_tokens(const ConvParams &p, const uint8_t *tile, int64_t t0, int64_t ta,
+                                            int64_t tb, int ch, int c0) {
+    constexpr int NH = W - 1;
+    constexpr int ES = XB ? 2 : 4, YS = YB ? 2 : 4;
+    const size_t D = (size_t)p.D;
+    float wv[W][kVec], bv[kVec];
+    load_filter<W>(p, c0, wv, bv);
+    int n;
+    int64_t bos, eos;
+    seq_of(p, ta, n, bos, eos);
+    float win[NH][kVec];
+    auto start_window = [&](int64_t t) {  // inputs t-NH .. t-1 of sequence n
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            const int64_t src = t - NH + j;
+            if (src >= bos) {
+                lds_vec<XB>(tile, (size_t)(src - (t0 - NH)) * kCh + ch, win[j]);
+            } else if (p.s0) {
+                ld_state(p.s0, ((size_t)n * NH + (NH - (bos - src))) * D + c0, win[j]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) win[j][e] = 0.f;
+            }
+        }
+    };
+    start_window(ta);
+    const uint8_t *xs = tile + ((size_t)(ta - (t0 - NH)) * kCh + ch) * ES;
+    uint8_t *yp = reinterpret_cast<uint8_t *>(p.y) + ((size_t)ta * D + c0) * YS;
+    const size_t ystride = D * YS;
+    int left = (int)(eos - ta < kTile + 1 ? eos - ta : kTile + 1);  // tokens until the sequence ends
+    const int cnt = (int)(tb - ta);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+        if (left == 0) {  // a sequence starts inside the tile
+            const int64_t t = ta + k;
+            seq_of(p, t, n, bos, eos);
+            start_window(t);
+            left = (int)(eos - t < kTile + 1 ? eos - t : kTile + 1);
+        }
+        float xv[kVec], z[kVec];
+        lds_vec<XB>(xs, 0, xv);
+        xs += kCh * ES;
+        conv_point<W, ACT>(wv, bv, win, xv, z);
+        st_vec<YB>(yp, 0, z);
+        yp += ystride;
+#pragma unroll
+        for (int j = 0; j + 1 < NH; ++j)
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) win[j][e] = win[j + 1][e];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) win[NH - 1][e] = xv[e];
+        if (--left == 0 && p.sT) {
+#pragma unroll
+            for (int j = 0; j < NH; ++j) st_state(p.sT, ((size_t)n * NH + j) * D + c0, win[j]);
+        }
     }
 }
 
@@ -240,50 +303,14 @@ __global__ void __launch_bounds__(kThreads) short_conv_tile_kernel(const __grid_
         const int64_t t1 = t0 + kTile < p.rows ? t0 + kTile : p.rows;
         const int64_t tb = ta + kTokPer < t1 ? ta + kTokPer : t1;
         if (c0 < p.D && ta < tb) {
-            float wv[W][kVec], bv[kVec];
-            load_filter<W>(p, c0, wv, bv);
-            int n;
-            int64_t bos, eos;
-            seq_of(p, ta, n, bos, eos);
-            float win[NH][kVec];
-            auto start_window = [&](int64_t t) {  // inputs t-NH .. t-1 of sequence n
-#pragma unroll
-                for (int j = 0; j < NH; ++j) {
-                    const int64_t src = t - NH + j;
-                    if (src >= bos) {
-                        lds_vec<XB>(tile, (size_t)(src - (t0 - NH)) * kCh + ch, win[j]);
-                    } else if (p.s0) {
-                        ld_state(p.s0, ((size_t)n * NH + (NH - (bos - src))) * D + c0, win[j]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < kVec; ++e) win[j][e] = 0.f;
-                    }
-                }
-            };
-            start_window(ta);
-#pragma unroll 4
-            for (int64_t t = ta; t < tb; ++t) {
-                if (t >= eos) {  // a sequence starts inside the tile
-                    seq_of(p, t, n, bos, eos);
-                    start_window(t);
-                }
-                float xv[kVec], z[kVec];
-                lds_vec<XB>(tile, (size_t)(t - (t0 - NH)) * kCh + ch, xv);
-                conv_point<W>(wv, bv, win, xv, p.act, z);
-                if (!tile_ok)
-#pragma unroll
-                    for (int e = 0; e < kVec; ++e) z[e] = __int_as_float(0x7fc00000);
-                st_vec<YB>(p.y, (size_t)t * D + c0, z);
-#pragma unroll
-                for (int j = 0; j + 1 < NH; ++j)
-#pragma unroll
-                    for (int e = 0; e < kVec; ++e) win[j][e] = win[j + 1][e];
-#pragma unroll
-                for (int e = 0; e < kVec; ++e) win[NH - 1][e] = xv[e];
-                if (t == eos - 1 && p.sT) {
-#pragma unroll
-                    for (int j = 0; j < NH; ++j) st_state(p.sT, ((size_t)n * NH + j) * D + c0, win[j]);
-                }
+            if (!tile_ok) {  // the tile never arrived: make the failure visible
+                const float nan4[kVec] = {__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                          __int_as_float(0x7fc00000), __int_as_float(0x7fc00000)};
+                for (int64_t t = ta; t < tb; ++t) st_vec<YB>(p.y, (size_t)t * D + c0, nan4);
+            } else if (p.act) {
+                conv_tokens<W, XB, YB, true>(p, tile, t0, ta, tb, ch, c0);
+            } else {
+                conv_tokens<W, XB, YB, false>(p, tile, t0, ta, tb, ch, c0);
             }
         }
         ok = __syncthreads_and(ok);  // every thread is done with buffer b; a timeout anywhere stops the CTA
@@ -318,7 +345,10 @@ __global__ void __launch_bounds__(256) short_conv_step_kernel(const ConvParams p
     }
     ld_vec<XB>(p.x, (size_t)n * D + c0, xv);
     load_filter<W>(p, c0, wv, bv);
-    conv_point<W>(wv, bv, win, xv, p.act, z);
+    if (p.act)
+        conv_point<W, true>(wv, bv, win, xv, z);
+    else
+        conv_point<W, false>(wv, bv, win, xv, z);
     st_vec<YB>(p.y, (size_t)n * D + c0, z);
     if (p.sT) {
 #pragma unroll
