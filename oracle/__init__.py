@@ -57,6 +57,9 @@ def _load():
                 P, P, P, ctypes.c_double, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
             ]
             lib.kda_oracle_gated_rmsnorm.restype = ctypes.c_int
+            lib.kda_oracle_gates.argtypes = [P, P, P, ctypes.c_double, P, P, P, ctypes.c_int64, ctypes.c_int,
+                                             ctypes.c_int]
+            lib.kda_oracle_gates.restype = ctypes.c_int
             lib.kda_oracle_short_conv.argtypes = [
                 P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int,
@@ -92,7 +95,8 @@ def recurrent(q, k, v, g, beta, initial_state=None, *, scale=None, use_qk_l2norm
     the leading dimension is 1 (or absent) and initial_state is [n_seqs,H,K,V].
     Returns ``(o [.., T, H, V] float64, final_state [N,H,K,V] float64[, states])``.
     """
-    q, k, v, g, beta = _f32(q), _f32(k), _f32(v), _f32(g), _f32(beta)
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    g, beta = _f64(g), _f64(beta)  # exact for fp32 inputs; fp64 gates from gates() pass unrounded
     if q.ndim == 3:  # [T,H,K] packed varlen without batch dim
         q, k, v, g, beta = q[None], k[None], v[None], g[None], beta[None]
     B, T, H, K = q.shape
@@ -143,6 +147,27 @@ def gated_rmsnorm(o, gate, w, eps=1e-5):
     if rc != 0:
         raise RuntimeError(f"kda_oracle_gated_rmsnorm failed with {rc}")
     return y
+
+
+def gates(z, A_log, b, dt_bias=None, lower_bound=None):
+    """g [.., H, K] and beta [.., H] (fp64) from the decay logits z [.., H, K], A_log [H],
+    dt_bias [H, K] (or [H*K]) or None, the write-strength logits b [.., H] and an optional
+    lower bound.  Formula and page citations: ``kda_oracle_gates`` in kda_oracle.c."""
+    z = _f32(z)
+    b = _f32(b)
+    H, K = z.shape[-2], z.shape[-1]
+    A_log = _f32(A_log).reshape(H)
+    dtb = None if dt_bias is None else _f32(dt_bias).reshape(H, K)
+    if b.shape != z.shape[:-1]:
+        raise ValueError("b must be z without its last axis")
+    rows = int(np.prod(z.shape[:-2]))
+    g = np.zeros(z.shape, dtype=np.float64)
+    beta = np.zeros(b.shape, dtype=np.float64)
+    lb = -np.inf if lower_bound is None else float(lower_bound)
+    rc = _load().kda_oracle_gates(_ptr(z), _ptr(A_log), _ptr(dtb), lb, _ptr(b), _ptr(g), _ptr(beta), rows, H, K)
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_gates failed with {rc}")
+    return g, beta
 
 
 def short_conv(x, weight, bias=None, conv_state=None, *, cu_seqlens=None, activation="silu"):

@@ -58,7 +58,8 @@ int kda_oracle_version(void) { return KDA_ORACLE_VERSION; }
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-    const float *q, *k, *v, *g, *beta;   /* token-major inputs, see kda_oracle_recurrent */
+    const float *q, *k, *v;               /* token-major inputs, see kda_oracle_recurrent */
+    const double *g, *beta;               /* log decay and write strength (fp64) */
     const double *initial_state;          /* [N,H,K,V] or NULL (zero state) */
     double *o;                            /* [tokens,H,V] */
     double *final_state;                  /* [N,H,K,V] or NULL */
@@ -92,8 +93,8 @@ static void rec_unit(const rec_job *J, int64_t unit, double *S, double *qh, doub
         const float *qt = J->q + ((size_t)row * H + h) * K;
         const float *kt = J->k + ((size_t)row * H + h) * K;
         const float *vt = J->v + ((size_t)row * H + h) * V;
-        const float *gt = J->g + ((size_t)row * H + h) * K;
-        const double bt = (double)J->beta[(size_t)row * H + h];
+        const double *gt = J->g + ((size_t)row * H + h) * K;
+        const double bt = J->beta[(size_t)row * H + h];
 
         /* L2 normalisation of query and key over key_dim (optional). */
         double sq = 0.0, sk = 0.0;
@@ -187,8 +188,8 @@ static void *rec_worker(void *arg) {
  * [cu_seqlens[n], cu_seqlens[n+1]) and rows = cu_seqlens[n_seqs].
  * Returns 0 on success, -1 on a bad argument, -2 on an allocation failure.
  */
-int kda_oracle_recurrent(const float *q, const float *k, const float *v, const float *g,
-                         const float *beta, const double *initial_state, double *o,
+int kda_oracle_recurrent(const float *q, const float *k, const float *v, const double *g,
+                         const double *beta, const double *initial_state, double *o,
                          double *final_state, double *states, const int64_t *cu_seqlens,
                          int n_seqs, int B, int T, int H, int K, int V, double scale,
                          int use_qk_l2norm, double l2_eps, int n_threads) {
@@ -362,6 +363,49 @@ int kda_oracle_short_conv(const float *x, const double *weight, const double *bi
             }
             if (state_out)
                 for (int w = 0; w < W - 1; ++w) state_out[((size_t)n * (W - 1) + w) * D + c] = hist[w];
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decay and write strength from their logits                                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The layer's gate parameters, from the logits the projections produce.
+ *
+ * Kimi-K3 atlas "gate-project (decode, P = 1000)", section "Code" (the layer
+ * holds A_log = log U(1, 16), one per head; f_a_proj / f_b_proj, the rank-128
+ * pair producing one decay logit per key channel of each head; dt_bias, one bias
+ * per such logit; b_proj, one write-strength logit per head; gate_lower_bound);
+ * nnterp encyclopedia "Kimi-Linear", section 03 (g is per key channel, float32
+ * and non-positive; beta is the sigmoid of b_proj).  The pages omit the line that
+ * combines them; the reading used here (the plainest one the parameters support):
+ *
+ *   g[t][h][c] = max(lower_bound, -exp(A_log[h]) * softplus(z[t][h][c] + dt_bias[h][c]))
+ *   beta[t][h] = 1 / (1 + exp(-b[t][h]))
+ *
+ * with softplus(x) = log(1 + e^x), evaluated as max(x, 0) + log1p(e^-|x|).
+ *
+ *   z       [rows, H, K] float (bf16 values widened)     A_log [H] float
+ *   dt_bias [H, K] float or NULL (zero)                  lower_bound: -INFINITY for none
+ *   b       [rows, H] float                              g [rows, H, K], beta [rows, H] double (written)
+ */
+int kda_oracle_gates(const float *z, const float *A_log, const float *dt_bias, double lower_bound,
+                     const float *b, double *g, double *beta, int64_t rows, int H, int K) {
+    if (!z || !A_log || !b || !g || !beta || rows < 0 || H <= 0 || K <= 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const double a = exp((double)A_log[h]);
+            for (int c = 0; c < K; ++c) {
+                const size_t i = ((size_t)r * H + h) * K + c;
+                const double x = (double)z[i] + (dt_bias ? (double)dt_bias[(size_t)h * K + c] : 0.0);
+                const double sp = (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+                const double gv = -a * sp;
+                g[i] = gv > lower_bound ? gv : lower_bound;
+            }
+            beta[(size_t)r * H + h] = 1.0 / (1.0 + exp(-(double)b[(size_t)r * H + h]));
         }
     }
     return 0;
