@@ -34,6 +34,7 @@ PREFILL_BYTES_PER_TH = 3 * 256 + 512 + 4 + 512   # q,k,v bf16 + g fp32 + beta + 
 PREFILL_FLOP_PER_TH = 10 * 64 * 128 + 6 * 128 * 128 + (2 * 64 * 64) // 3  # 182,955 at C=64, d=128
 STATE_BYTES = 128 * 128 * 4
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256 + 512  # + gate bf16, y fp32
+PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits bf16 + beta logit bf16 + o fp32
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work from one
 # ncu capture summarised under profiles/, valid only for the kernel source it was
@@ -267,6 +268,34 @@ def bench_decode(args, world, peaks):
                          "peak_source": peaks["source"]}}
 
 
+def bench_prefill_logits(args, world, peaks):
+    """The same prefill with g and beta computed in the kernel from bf16 logits
+    (kda_chunk_fwd_logits), sharing the prefill's shapes and q, k, v."""
+    import torch
+    import kimi_delta_attention_gated_gb300 as kda
+    from kimi_delta_attention_gated_gb300.inputs import make_logit_inputs
+    d = make_logit_inputs("prefill", device="cuda", T=args.prefill_T)
+    B, T, H, K, V = d["B"], d["T"], d["H"], d["K"], d["V"]
+    o = torch.empty((B, T, H, V), device="cuda", dtype=torch.float32)
+    fs = torch.empty((B, H, K, V), device="cuda", dtype=torch.float32)
+    fn = lambda: kda.chunk_fwd_logits(d["q"], d["k"], d["v"], d["g_logits"], d["beta_logits"], d["A_log"], None,
+                                      dt_bias=d["dt_bias"], g_lower_bound=d["g_lower_bound"], scale=d["scale"],
+                                      mode=args.mode, o=o, final_state=fs)
+    r = time_steps(fn, args.steps, args.warmup, world)
+    kernel_ms = r["call_ms"] / max(1, r["launches"] // args.steps)
+    th = B * T * H
+    algo_bytes = th * PREFILL_LOGITS_BYTES_PER_TH + B * H * STATE_BYTES
+    achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+    return {"metric": "KDA prefill tokens/s, gates from logits", "value": world * B * T / (r["ms_per_step"] * 1e-3),
+            "unit": "tokens/s", "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
+            "config": {"workload": f"prefill B={B} T={T} H={H} d={K}, bf16 g/beta logits + A_log + dt_bias, "
+                                   "lower bound -5", "l2_flush": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
+                         "peak_source": peaks["source"]}}
+
+
 def bench_short_conv(args, world, peaks):
     """The q/k/v short convolution (causal depthwise, 4 taps, SiLU): one 8192-token prompt
     (state out) and one decode step of 256 sequences (state updated in place), each over
@@ -393,6 +422,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--no-logits", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -415,6 +445,7 @@ def main():
     pre, d = bench_prefill(args, world, rank, peaks)
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
     conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
+    logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
     e2e = None if (args.no_e2e or args.only == "prefill") else bench_e2e(args, world, d)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
@@ -428,7 +459,7 @@ def main():
         "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": pre["config"],
         "roofline": pre["roofline"], "roofline_tensor": pre["roofline_tensor"], "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
-        "short_conv": conv,
+        "short_conv": conv, "prefill_gate_logits": logits,
         "gpu": torch.cuda.get_device_name(),
     }
     print(json.dumps(line), flush=True)

@@ -126,6 +126,36 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype 
                          const float *norm_w, float eps, void *y, int mode, void *stream);
 
 /*
+ * kda_chunk_fwd_logits -- kda_chunk_fwd with the decay and the write strength
+ * computed inside the kernels from the logits the layer's projections produce,
+ * instead of read as fp32 g and beta (halves the g traffic with bf16 logits).
+ *
+ * Pages: Kimi-K3 atlas "gate-project (decode, P = 1000)", section "Code" (the
+ * layer holds A_log = log U(1, 16) per head, f_a_proj / f_b_proj producing one
+ * decay logit per key channel of each head, dt_bias with one bias per such logit,
+ * b_proj with one write-strength logit per head, gate_lower_bound); nnterp
+ * encyclopedia "Kimi-Linear", section 03 (g per key channel, fp32, non-positive;
+ * beta = sigmoid(b_proj)).  The line combining them is not on the pages; this
+ * library reads it as
+ *     g[t][h][c] = max(g_lower_bound, -exp(A_log[h]) * softplus(g_logits[t][h][c] + dt_bias[h][c]))
+ *     beta[t][h] = sigmoid(beta_logits[t][h])
+ *
+ *   g_logits    [B, T, H, K] g_logits_dtype     A_log [H] float
+ *   dt_bias     [H, K] float or NULL (zero)     g_lower_bound <= 0; -INFINITY for none
+ *   beta_logits [B, T, H] beta_logits_dtype
+ * Everything else as kda_chunk_fwd.
+ */
+kda_status kda_chunk_fwd_logits(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                kda_dtype beta_logits_dtype, const float *initial_state, float *final_state,
+                                void *o, kda_dtype o_dtype, const int32_t *cu_seqlens,
+                                const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int H, int K, int V,
+                                int chunk, float scale, int use_qk_l2norm, const void *gate,
+                                kda_dtype gate_dtype, const float *norm_w, float eps, void *y, int mode,
+                                void *stream);
+
+/*
  * kda_recurrent_fwd -- the token-by-token form over T tokens (fp32 arithmetic).
  *
  * Pages: nnterp "Kimi-Linear" section 03 "Loading" (the token-by-token kernel;
@@ -165,6 +195,20 @@ kda_status kda_recurrent_step(const void *q, const void *k, const void *v, kda_d
                               int V, float scale, int use_qk_l2norm, const void *gate,
                               kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
                               void *stream);
+
+/*
+ * kda_recurrent_step_logits -- kda_recurrent_step with g and beta computed from
+ * their logits, as kda_chunk_fwd_logits defines them:
+ *   g_logits [B, H, K] g_logits_dtype, A_log [H], dt_bias [H, K] or NULL,
+ *   g_lower_bound, beta_logits [B, H] beta_logits_dtype.
+ */
+kda_status kda_recurrent_step_logits(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                     const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                     const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                     kda_dtype beta_logits_dtype, const float *state_in, float *state_out,
+                                     void *o, kda_dtype o_dtype, int B, int H, int K, int V, float scale,
+                                     int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                                     const float *norm_w, float eps, void *y, void *stream);
 
 /*
  * kda_gated_rmsnorm -- the head-wise sigmoid-gated RMSNorm on its own.

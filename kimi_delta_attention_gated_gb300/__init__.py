@@ -22,7 +22,8 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "recurrent_fwd", "recurrent_step", "gated_rmsnorm", "short_conv", "launch_count",
+__all__ = ["chunk_fwd", "chunk_fwd_logits", "recurrent_fwd", "recurrent_step", "recurrent_step_logits",
+           "gated_rmsnorm", "short_conv", "launch_count",
            "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -65,8 +66,12 @@ def _load():
                                            P, P]
         lib.kda_gated_rmsnorm.argtypes = [P, I, P, I, P, F, P, I, ctypes.c_int64, I, I, P]
         lib.kda_short_conv_fwd.argtypes = [P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P]
+        lib.kda_chunk_fwd_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, P, P, I, I, I, I, I, I,
+                                             I, F, I, P, I, P, F, P, I, P]
+        lib.kda_recurrent_step_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, I, I, I, I, F, I,
+                                                  P, I, P, F, P, P]
         for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
-                   "kda_short_conv_fwd"):
+                   "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_launch_count.restype = ctypes.c_uint64
@@ -160,6 +165,34 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
     y [B,T,H*V] is the sigmoid-gated RMSNorm of o (o is None when return_o=False).
     Preallocated outputs may be passed as o / y / final_state (final_state may be
     initial_state itself for an in-place update)."""
+    return _chunk(q, k, v, (g, beta), None, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens,
+                  output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y, final_state)
+
+
+def chunk_fwd_logits(q, k, v, g_logits, beta_logits, A_log, initial_state=None, *, dt_bias=None,
+                     g_lower_bound=-5.0, scale=None, chunk=64, use_qk_l2norm=True, cu_seqlens=None,
+                     output_final_state=True, gate=None, norm_w=None, eps=1e-5, out_dtype=torch.float32,
+                     mode="auto", return_o=True, o=None, y=None, final_state=None):
+    """chunk_fwd with g = max(g_lower_bound, -exp(A_log[h]) * softplus(g_logits + dt_bias)) and
+    beta = sigmoid(beta_logits) computed inside the kernels.  g_logits [B,T,H,K] and
+    beta_logits [B,T,H] in bf16 or fp32; A_log [H]; dt_bias [H,K] (or [H*K]) or None;
+    g_lower_bound None for no floor."""
+    lb = float("-inf") if g_lower_bound is None else float(g_lower_bound)
+    return _chunk(q, k, v, None, (g_logits, beta_logits, A_log, dt_bias, lb), initial_state, scale, chunk,
+                  use_qk_l2norm, cu_seqlens, output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y,
+                  final_state)
+
+
+def _logit_args(lg, dev):
+    z, b, A_log, dt_bias, lb = lg
+    z, b = _prep(z, dev), _prep(b, dev)
+    A_log = _prep(A_log, dev, torch.float32)
+    dt_bias = _prep(dt_bias, dev, torch.float32)
+    return z, b, A_log, dt_bias, lb
+
+
+def _chunk(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens, output_final_state, gate,
+           norm_w, eps, out_dtype, mode, return_o, o, y, final_state):
     lib = _load()
     host = q.device.type != "cuda"
     dev = _device_of(q, k, v)
@@ -167,7 +200,6 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
     if host:
         o, final_state, y = _dev_out(o), _dev_out(final_state), _dev_out(y)
     q, k, v = _prep(q, dev), _prep(k, dev), _prep(v, dev)
-    g, beta = _prep(g, dev, torch.float32), _prep(beta, dev, torch.float32)
     initial_state = _prep(initial_state, dev, torch.float32)
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -183,11 +215,17 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
         final_state = torch.empty((N, H, K, V), device=dev, dtype=torch.float32)
     if scale is None:
         scale = K ** -0.5
-    _check(lib.kda_chunk_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(final_state),
-        _ptr(o), _dt(o if o is not None else y), _ptr(cu_d), _ptr(cu_h), n_seqs, B, T, H, K, V, int(chunk),
-        float(scale), int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16,
-        _ptr(norm_w), float(eps), _ptr(y), _MODES[mode] if isinstance(mode, str) else int(mode), _stream()))
+    tail = (_ptr(initial_state), _ptr(final_state), _ptr(o), _dt(o if o is not None else y), _ptr(cu_d), _ptr(cu_h),
+            n_seqs, B, T, H, K, V, int(chunk), float(scale), int(bool(use_qk_l2norm)), _ptr(gate),
+            _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y),
+            _MODES[mode] if isinstance(mode, str) else int(mode), _stream())
+    if lg is None:
+        g, beta = _prep(gb[0], dev, torch.float32), _prep(gb[1], dev, torch.float32)
+        _check(lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), *tail))
+    else:
+        z, b, A_log, dt_bias, lb = _logit_args(lg, dev)
+        _check(lib.kda_chunk_fwd_logits(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(z), _dt(z), _ptr(A_log),
+                                        _ptr(dt_bias), lb, _ptr(b), _dt(b), *tail))
     if gate is not None:
         return _to_host((o, final_state, y), host, dests)
     return _to_host((o, final_state), host, dests)
@@ -234,11 +272,25 @@ def recurrent_step(q, k, v, g, beta, state, *, scale=None, use_qk_l2norm=True, g
     """One decode token per sequence.  q, k [B,H,K]; v [B,H,V]; g [B,H,K]; beta [B,H];
     state [B,H,K,V] fp32 (or None).  ``state_out=state`` updates the state in place.
     Returns (o, state_out[, y])."""
+    return _step(q, k, v, (g, beta), None, state, scale, use_qk_l2norm, gate, norm_w, eps, out_dtype, state_out,
+                 return_o, o, y)
+
+
+def recurrent_step_logits(q, k, v, g_logits, beta_logits, A_log, state, *, dt_bias=None, g_lower_bound=-5.0,
+                          scale=None, use_qk_l2norm=True, gate=None, norm_w=None, eps=1e-5, out_dtype=torch.float32,
+                          state_out=None, return_o=True, o=None, y=None):
+    """recurrent_step with g and beta computed from their logits (see chunk_fwd_logits):
+    g_logits [B,H,K], beta_logits [B,H]."""
+    lb = float("-inf") if g_lower_bound is None else float(g_lower_bound)
+    return _step(q, k, v, None, (g_logits, beta_logits, A_log, dt_bias, lb), state, scale, use_qk_l2norm, gate,
+                 norm_w, eps, out_dtype, state_out, return_o, o, y)
+
+
+def _step(q, k, v, gb, lg, state, scale, use_qk_l2norm, gate, norm_w, eps, out_dtype, state_out, return_o, o, y):
     lib = _load()
     host = q.device.type != "cuda"
     dev = _device_of(q, k, v, state)
     q, k, v = _prep(q, dev), _prep(k, dev), _prep(v, dev)
-    g, beta = _prep(g, dev, torch.float32), _prep(beta, dev, torch.float32)
     state = _prep(state, dev, torch.float32)
     B, H, K = q.shape
     V = v.shape[-1]
@@ -252,10 +304,16 @@ def recurrent_step(q, k, v, g, beta, state, *, scale=None, use_qk_l2norm=True, g
         o = torch.empty((B, H, V), device=dev, dtype=out_dtype)
     if scale is None:
         scale = K ** -0.5
-    _check(lib.kda_recurrent_step(
-        _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(state), _ptr(state_out), _ptr(o),
-        _dt(o if o is not None else y), B, H, K, V, float(scale), int(bool(use_qk_l2norm)), _ptr(gate),
-        _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y), _stream()))
+    tail = (_ptr(state), _ptr(state_out), _ptr(o), _dt(o if o is not None else y), B, H, K, V, float(scale),
+            int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps),
+            _ptr(y), _stream())
+    if lg is None:
+        g, beta = _prep(gb[0], dev, torch.float32), _prep(gb[1], dev, torch.float32)
+        _check(lib.kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), *tail))
+    else:
+        z, b, A_log, dt_bias, lb = _logit_args(lg, dev)
+        _check(lib.kda_recurrent_step_logits(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(z), _dt(z), _ptr(A_log),
+                                             _ptr(dt_bias), lb, _ptr(b), _dt(b), *tail))
     if gate is not None:
         return _to_host((o, state_out, y), host)
     return _to_host((o, state_out), host)

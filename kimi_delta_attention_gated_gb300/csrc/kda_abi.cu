@@ -117,6 +117,13 @@ kda::SeqParams make_params(const void *q, const void *k, const void *v, int qkv_
     p.states = states;
     p.cu_seqlens = cu;
     p.cu_host = nullptr;
+    p.K = 0;
+    p.g_logits = nullptr;
+    p.A_log = nullptr;
+    p.dt_bias = nullptr;
+    p.beta_logits = nullptr;
+    p.g_lower = -INFINITY;
+    p.g_logits_bf16 = p.beta_logits_bf16 = 0;
     p.gate = gate;
     p.norm_w = norm_w;
     p.y = y;
@@ -130,6 +137,104 @@ kda::SeqParams make_params(const void *q, const void *k, const void *v, int qkv_
     p.o_bf16 = o_dtype == KDA_BF16;
     p.gate_bf16 = gate_dtype == KDA_BF16;
     return p;
+}
+
+// The decay / write-strength logits of the *_logits entry points.
+struct GateLogits {
+    const void *z;
+    int z_dtype;
+    const float *A_log, *dt_bias;
+    float lower;
+    const void *b;
+    int b_dtype;
+};
+
+kda_status check_logits(const char *fn, const GateLogits &gl, bool no_tokens) {
+    KDA_REQUIRE(gl.A_log, KDA_ERR_INVALID_ARG, "%s: A_log must not be NULL", fn);
+    KDA_REQUIRE(no_tokens || (gl.z && gl.b), KDA_ERR_INVALID_ARG, "%s: g_logits and beta_logits must not be NULL", fn);
+    KDA_REQUIRE(dtype_ok(gl.z_dtype) && dtype_ok(gl.b_dtype), KDA_ERR_UNSUPPORTED, "%s: unsupported logits dtype", fn);
+    KDA_REQUIRE(!std::isnan(gl.lower) && gl.lower <= 0.f, KDA_ERR_INVALID_ARG,
+                "%s: g_lower_bound must be <= 0 (-INFINITY for none)", fn);
+    const void *ptrs[] = {gl.z, gl.A_log, gl.dt_bias, gl.b};
+    for (const void *ptr : ptrs)
+        KDA_REQUIRE(!ptr || aligned16(ptr), KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);
+    return KDA_OK;
+}
+
+void set_logits(kda::SeqParams &p, const GateLogits *gl, int K) {
+    p.K = K;
+    p.g_logits = gl ? gl->z : nullptr;
+    p.A_log = gl ? gl->A_log : nullptr;
+    p.dt_bias = gl ? gl->dt_bias : nullptr;
+    p.beta_logits = gl ? gl->b : nullptr;
+    p.g_lower = gl ? gl->lower : -INFINITY;
+    p.g_logits_bf16 = gl && gl->z_dtype == KDA_BF16;
+    p.beta_logits_bf16 = gl && gl->b_dtype == KDA_BF16;
+}
+
+kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                      const float *g, const float *beta, const GateLogits *gl, const float *initial_state,
+                      float *final_state, void *o, kda_dtype o_dtype, const int32_t *cu_seqlens,
+                      const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int H, int K, int V, int chunk,
+                      float scale, int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                      const float *norm_w, float eps, void *y, int mode, void *stream) {
+    kda::g_err[0] = 0;
+    int N = 0;
+    // with logits, g / beta are checked through them (the recurrence never reads g / beta then)
+    const float *gchk = gl ? reinterpret_cast<const float *>(gl->z) : g;
+    const float *bchk = gl ? reinterpret_cast<const float *>(gl->b) : beta;
+    kda_status s = check_seq_args(fn, q, k, v, qkv_dtype, gchk, bchk, initial_state, final_state, o, o_dtype,
+                                  cu_seqlens, cu_seqlens_host, n_seqs, B, T, H, K, V, scale, gate, gate_dtype,
+                                  norm_w, eps, y, N);
+    if (s != KDA_OK) return s;
+    if (gl && (s = check_logits(fn, *gl, (int64_t)B * T == 0)) != KDA_OK) return s;
+    KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, KDA_ERR_UNSUPPORTED, "%s: chunk=%d (supported: 16, 32, 64)",
+                fn, chunk);
+    KDA_REQUIRE(mode == KDA_MODE_AUTO || mode == KDA_MODE_TENSOR || mode == KDA_MODE_FP32, KDA_ERR_INVALID_ARG,
+                "%s: unknown mode %d", fn, mode);
+    const bool tc_ok = kda::chunk_tc_supported(K, V, chunk) && qkv_dtype == KDA_BF16;
+    KDA_REQUIRE(mode != KDA_MODE_TENSOR || tc_ok, KDA_ERR_UNSUPPORTED,
+                "%s: the tensor path needs bf16 q/k/v, K = V = 128 and chunk = 64", fn);
+    cudaStream_t st = (cudaStream_t)stream;
+    // an empty prompt only hands the state through: the fp32 path does that without a tensor map
+    const bool use_tc = tc_ok && mode != KDA_MODE_FP32 && T > 0;
+    if (use_tc) {
+        kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o, o_dtype, nullptr,
+                                       cu_seqlens, N, T, H, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y);
+        p.cu_host = cu_seqlens_host;
+        set_logits(p, gl, K);
+        return kda::launch_chunk_tc(p, K, V, chunk, st);
+    }
+    // fp32 path: o goes to y's buffer when o is not wanted, then the norm runs in place.
+    void *o_target = o ? o : y;
+    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o_target, o_dtype,
+                                   nullptr, cu_seqlens, N, T, H, scale, use_qk_l2norm, nullptr, gate_dtype, norm_w,
+                                   eps, nullptr);
+    set_logits(p, gl, K);
+    s = kda::launch_chunk_fp32(p, K, V, chunk, nullptr, st);
+    if (s != KDA_OK || !gate || (int64_t)B * T == 0) return s;
+    return kda::launch_gated_rmsnorm(o_target, o_dtype == KDA_BF16, gate, gate_dtype == KDA_BF16, norm_w, eps, y,
+                                     o_dtype == KDA_BF16, (int64_t)B * T, H, V, st);
+}
+
+kda_status step_impl(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                     const float *g, const float *beta, const GateLogits *gl, const float *state_in,
+                     float *state_out, void *o, kda_dtype o_dtype, int B, int H, int K, int V, float scale,
+                     int use_qk_l2norm, const void *gate, kda_dtype gate_dtype, const float *norm_w, float eps,
+                     void *y, void *stream) {
+    kda::g_err[0] = 0;
+    int N = 0;
+    KDA_REQUIRE(state_out, KDA_ERR_INVALID_ARG, "%s: state_out must not be NULL", fn);
+    const float *gchk = gl ? reinterpret_cast<const float *>(gl->z) : g;
+    const float *bchk = gl ? reinterpret_cast<const float *>(gl->b) : beta;
+    kda_status s = check_seq_args(fn, q, k, v, qkv_dtype, gchk, bchk, state_in, state_out, o, o_dtype, nullptr,
+                                  nullptr, 0, B, 1, H, K, V, scale, gate, gate_dtype, norm_w, eps, y, N);
+    if (s != KDA_OK) return s;
+    if (gl && (s = check_logits(fn, *gl, false)) != KDA_OK) return s;
+    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, state_in, state_out, o, o_dtype, nullptr, nullptr, N,
+                                   1, H, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y);
+    set_logits(p, gl, K);
+    return kda::launch_recurrent(p, K, V, (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -160,38 +265,24 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype 
                          int B, int T, int H, int K, int V, int chunk, float scale,
                          int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
                          const float *norm_w, float eps, void *y, int mode, void *stream) {
-    kda::g_err[0] = 0;
-    int N = 0;
-    kda_status s = check_seq_args("kda_chunk_fwd", q, k, v, qkv_dtype, g, beta, initial_state,
-                                  final_state, o, o_dtype, cu_seqlens, cu_seqlens_host, n_seqs, B, T,
-                                  H, K, V, scale, gate, gate_dtype, norm_w, eps, y, N);
-    if (s != KDA_OK) return s;
-    KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, KDA_ERR_UNSUPPORTED,
-                "kda_chunk_fwd: chunk=%d (supported: 16, 32, 64)", chunk);
-    KDA_REQUIRE(mode == KDA_MODE_AUTO || mode == KDA_MODE_TENSOR || mode == KDA_MODE_FP32,
-                KDA_ERR_INVALID_ARG, "kda_chunk_fwd: unknown mode %d", mode);
-    const bool tc_ok = kda::chunk_tc_supported(K, V, chunk) && qkv_dtype == KDA_BF16;
-    KDA_REQUIRE(mode != KDA_MODE_TENSOR || tc_ok, KDA_ERR_UNSUPPORTED,
-                "kda_chunk_fwd: the tensor path needs bf16 q/k/v, K = V = 128 and chunk = 64");
-    cudaStream_t st = (cudaStream_t)stream;
-    // an empty prompt only hands the state through: the fp32 path does that without a tensor map
-    const bool use_tc = tc_ok && mode != KDA_MODE_FP32 && T > 0;
-    if (use_tc) {
-        kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o,
-                                       o_dtype, nullptr, cu_seqlens, N, T, H, scale, use_qk_l2norm,
-                                       gate, gate_dtype, norm_w, eps, y);
-        p.cu_host = cu_seqlens_host;
-        return kda::launch_chunk_tc(p, K, V, chunk, st);
-    }
-    // fp32 path: o goes to y's buffer when o is not wanted, then the norm runs in place.
-    void *o_target = o ? o : y;
-    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o_target,
-                                   o_dtype, nullptr, cu_seqlens, N, T, H, scale, use_qk_l2norm,
-                                   nullptr, gate_dtype, norm_w, eps, nullptr);
-    s = kda::launch_chunk_fp32(p, K, V, chunk, nullptr, st);
-    if (s != KDA_OK || !gate || (int64_t)B * T == 0) return s;
-    return kda::launch_gated_rmsnorm(o_target, o_dtype == KDA_BF16, gate, gate_dtype == KDA_BF16,
-                                     norm_w, eps, y, o_dtype == KDA_BF16, (int64_t)B * T, H, V, st);
+    return chunk_impl("kda_chunk_fwd", q, k, v, qkv_dtype, g, beta, nullptr, initial_state, final_state, o, o_dtype,
+                      cu_seqlens, cu_seqlens_host, n_seqs, B, T, H, K, V, chunk, scale, use_qk_l2norm, gate,
+                      gate_dtype, norm_w, eps, y, mode, stream);
+}
+
+kda_status kda_chunk_fwd_logits(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                kda_dtype beta_logits_dtype, const float *initial_state, float *final_state,
+                                void *o, kda_dtype o_dtype, const int32_t *cu_seqlens,
+                                const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int H, int K, int V,
+                                int chunk, float scale, int use_qk_l2norm, const void *gate,
+                                kda_dtype gate_dtype, const float *norm_w, float eps, void *y, int mode,
+                                void *stream) {
+    const GateLogits gl{g_logits, g_logits_dtype, A_log, dt_bias, g_lower_bound, beta_logits, beta_logits_dtype};
+    return chunk_impl("kda_chunk_fwd_logits", q, k, v, qkv_dtype, nullptr, nullptr, &gl, initial_state, final_state,
+                      o, o_dtype, cu_seqlens, cu_seqlens_host, n_seqs, B, T, H, K, V, chunk, scale, use_qk_l2norm,
+                      gate, gate_dtype, norm_w, eps, y, mode, stream);
 }
 
 kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
@@ -211,6 +302,7 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, kda_dt
     kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o, o_dtype,
                                    states, cu_seqlens, N, T, H, scale, use_qk_l2norm, gate, gate_dtype,
                                    norm_w, eps, y);
+    set_logits(p, nullptr, K);
     return kda::launch_recurrent(p, K, V, (cudaStream_t)stream);
 }
 
@@ -220,17 +312,20 @@ kda_status kda_recurrent_step(const void *q, const void *k, const void *v, kda_d
                               int V, float scale, int use_qk_l2norm, const void *gate,
                               kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
                               void *stream) {
-    kda::g_err[0] = 0;
-    int N = 0;
-    KDA_REQUIRE(state_out, KDA_ERR_INVALID_ARG, "kda_recurrent_step: state_out must not be NULL");
-    kda_status s = check_seq_args("kda_recurrent_step", q, k, v, qkv_dtype, g, beta, state_in, state_out,
-                                  o, o_dtype, nullptr, nullptr, 0, B, 1, H, K, V, scale, gate,
-                                  gate_dtype, norm_w, eps, y, N);
-    if (s != KDA_OK) return s;
-    kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, state_in, state_out, o, o_dtype,
-                                   nullptr, nullptr, N, 1, H, scale, use_qk_l2norm, gate, gate_dtype,
-                                   norm_w, eps, y);
-    return kda::launch_recurrent(p, K, V, (cudaStream_t)stream);
+    return step_impl("kda_recurrent_step", q, k, v, qkv_dtype, g, beta, nullptr, state_in, state_out, o, o_dtype, B,
+                     H, K, V, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y, stream);
+}
+
+kda_status kda_recurrent_step_logits(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                     const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                     const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                     kda_dtype beta_logits_dtype, const float *state_in, float *state_out,
+                                     void *o, kda_dtype o_dtype, int B, int H, int K, int V, float scale,
+                                     int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                                     const float *norm_w, float eps, void *y, void *stream) {
+    const GateLogits gl{g_logits, g_logits_dtype, A_log, dt_bias, g_lower_bound, beta_logits, beta_logits_dtype};
+    return step_impl("kda_recurrent_step_logits", q, k, v, qkv_dtype, nullptr, nullptr, &gl, state_in, state_out, o,
+                     o_dtype, B, H, K, V, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y, stream);
 }
 
 kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,

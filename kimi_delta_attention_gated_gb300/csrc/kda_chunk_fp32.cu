@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) chunk_fp32_kernel(const SeqParams p,
                 if (i < cn) {
                     qv = ld_in(p.q, hk + c, p.qkv_bf16);
                     kv = ld_in(p.k, hk + c, p.qkv_bf16);
-                    gv = p.g[hk + c];
+                    gv = load_g(p, hk + c, h, c);
                 }
                 qh[i * KP + c] = qv;
                 kh[i * KP + c] = kv;
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) chunk_fp32_kernel(const SeqParams p,
                 qh[i * KP + c] *= rq;
                 kh[i * KP + c] *= rk;
             }
-            if (lane == 0) bet[i] = i < cn ? p.beta[row * H + h] : 0.f;
+            if (lane == 0) bet[i] = i < cn ? load_beta(p, row * H + h) : 0.f;
         }
         __syncthreads();
         // -- inclusive cumulative decay G (one thread per key channel)

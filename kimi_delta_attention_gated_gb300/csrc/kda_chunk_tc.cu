@@ -206,9 +206,9 @@ __device__ __forceinline__ void tri_offdiag(float *Asm, float *Tsm, int ctid) {
 
 // Loads of one chunk's q, k, g for this thread's 4 tokens x 4 key channels.
 struct ChunkRegs {
-    float4 g[4];
+    float4 g[4];  // g, or its raw logits (fp32, or bf16 bits in .x/.y) until the chunk is prepared
     uint2 q[4], k[4];
-    float beta;  // token warp * 4 + lane, lanes 0-3
+    float beta;   // token warp * 4 + lane, lanes 0-3 (or its logit until prepared)
 };
 
 __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, int bos, int t0, int cn, int h,
@@ -221,7 +221,14 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
         cr.k[r] = make_uint2(0u, 0u);
         if (i < cn) {
             const size_t hk = ((size_t)(bos + t0 + i) * p.H + h) * DK + l4;
-            cr.g[r] = __ldg(reinterpret_cast<const float4 *>(p.g + hk));
+            if (!p.g_logits) {
+                cr.g[r] = __ldg(reinterpret_cast<const float4 *>(p.g + hk));
+            } else if (p.g_logits_bf16) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.g_logits) + hk));
+                cr.g[r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), 0.f, 0.f);
+            } else {
+                cr.g[r] = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.g_logits) + hk));
+            }
             cr.q[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + hk));
             cr.k[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
         }
@@ -229,7 +236,8 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
     // beta of token warp * 4 + lane (lanes 0-3); the address stays inside the chunk for every lane
     const int ib = warp * 4 + ((l4 >> 2) & 3);
     const bool okb = l4 < 16 && ib < cn;
-    cr.beta = okb ? __ldg(p.beta + (size_t)(bos + t0 + (okb ? ib : 0)) * p.H + h) : 0.f;
+    const size_t bi = (size_t)(bos + t0 + (okb ? ib : 0)) * p.H + h;
+    cr.beta = !okb ? 0.f : (p.beta_logits ? ld_in(p.beta_logits, bi, p.beta_logits_bf16) : __ldg(p.beta + bi));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -335,7 +343,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // small buffers, each warp's decay totals per key channel into the scan buffer.
     // The 8 sums of squares of a warp's 4 tokens are reduced with a reduce-scatter
     // (9 shuffles); lanes 4v..4v+3 end with sum v (q of tokens 0-3, then k).
-    auto prep_norms = [&](const ChunkRegs &c) {
+    auto prep_norms = [&](ChunkRegs &c, int cnn) {
+        if (p.g_logits) {  // g from its logits; tokens past the chunk's end keep g = 0
+            const float a_h = __expf(__ldg(p.A_log + h));
+            const float4 db = p.dt_bias ? __ldg(reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * DK + l4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float z[4];
+                if (p.g_logits_bf16) {
+                    const uint32_t ux = __float_as_uint(c.g[r].x), uy = __float_as_uint(c.g[r].y);
+                    z[0] = bf16lo(ux); z[1] = bf16hi(ux); z[2] = bf16lo(uy); z[3] = bf16hi(uy);
+                } else {
+                    z[0] = c.g[r].x; z[1] = c.g[r].y; z[2] = c.g[r].z; z[3] = c.g[r].w;
+                }
+                const bool live = warp * 4 + r < cnn;
+                c.g[r] = make_float4(live ? gate_of_logit(z[0] + db.x, a_h, p.g_lower) : 0.f,
+                                     live ? gate_of_logit(z[1] + db.y, a_h, p.g_lower) : 0.f,
+                                     live ? gate_of_logit(z[2] + db.z, a_h, p.g_lower) : 0.f,
+                                     live ? gate_of_logit(z[3] + db.w, a_h, p.g_lower) : 0.f);
+            }
+        }
+        if (p.beta_logits && lane < 4) c.beta = warp * 4 + lane < cnn ? beta_of_logit(c.beta) : 0.f;
         float a[8];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -440,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's tensor-core waits)
     int oor_next = 0;
     if (nchunks > 0) {
-        prep_norms(cr);
+        prep_norms(cr, min(C, len));
         __syncthreads();
         float kgv[4][4];
         oor_next = prep_tiles(cr, kgv);
@@ -515,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid < 128) {  // G for every token and channel, from the inputs again
                 float acc = 0.f;
                 for (int i = 0; i < C; ++i) {
-                    if (i < cn) acc += p.g[((size_t)(bos + t0 + i) * H + h) * DK + tid];
+                    if (i < cn) acc += load_g(p, ((size_t)(bos + t0 + i) * H + h) * DK + tid, h, tid);
                     Gs[i * 128 + tid] = acc;
                 }
             }
@@ -665,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // while D runs: the next chunk's norms, beta and decay totals
-        if (ch + 1 < nchunks) prep_norms(cr);
+        if (ch + 1 < nchunks) prep_norms(cr, min(C, len - t0 - C));
         // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
         if (!wait_group(bar_d, par)) failed = 1;
         {

@@ -37,9 +37,18 @@ struct SeqParams {
     const float *norm_w;         // [V]
     void *y;                     // [rows, H * V]
     int N, T, H;                 // sequences, tokens per sequence (dense) / packed tokens (varlen), heads
+    int K;                       // key dim (indexes dt_bias)
     float scale, eps;
     int l2norm;                  // 0 / 1
     int qkv_bf16, o_bf16, gate_bf16;  // storage dtypes (1 = bf16, 0 = fp32)
+    // Gates from their logits (then g / beta are not read):
+    //   g = max(g_lower, -exp(A_log[h]) * softplus(g_logits + dt_bias[h][c])), beta = sigmoid(beta_logits)
+    const void *g_logits;        // [rows, H, K] or null
+    const float *A_log;          // [H]
+    const float *dt_bias;        // [H, K] or null
+    const void *beta_logits;     // [rows, H] or null
+    float g_lower;               // -inf: no floor
+    int g_logits_bf16, beta_logits_bf16;
 };
 
 // Token range of sequence n, clamped to [0, T] so a bad cu_seqlens cannot
@@ -70,6 +79,28 @@ __device__ __forceinline__ void st_out(void *base, size_t idx, float x, int is_b
 }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+// softplus(x) = log(1 + e^x) as max(x, 0) + log(1 + e^-|x|); below x = -16.6 the second
+// term rounds to 0 (absolute error under 6e-8).
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x))); }
+
+// g of one key channel from its logit z (bias not yet added); a_h = exp(A_log[h]).
+__device__ __forceinline__ float gate_of_logit(float x, float a_h, float lower) { return fmaxf(lower, -a_h * softplus_f(x)); }
+
+__device__ __forceinline__ float beta_of_logit(float b) { return __fdividef(1.f, 1.f + __expf(-b)); }
+
+// g[idx] of head h, key channel c: given directly or from its logit.
+__device__ __forceinline__ float load_g(const SeqParams &p, size_t idx, int h, int c) {
+    if (!p.g_logits) return p.g[idx];
+    const float x = ld_in(p.g_logits, idx, p.g_logits_bf16) + (p.dt_bias ? __ldg(p.dt_bias + (size_t)h * p.K + c) : 0.f);
+    return gate_of_logit(x, __expf(__ldg(p.A_log + h)), p.g_lower);
+}
+
+// beta[idx]: given directly or the sigmoid of its logit.
+__device__ __forceinline__ float load_beta(const SeqParams &p, size_t idx) {
+    if (!p.beta_logits) return p.beta[idx];
+    return beta_of_logit(ld_in(p.beta_logits, idx, p.beta_logits_bf16));
+}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

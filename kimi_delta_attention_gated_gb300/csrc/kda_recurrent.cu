@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
             const float kv = ld_in(p.k, hk + tid, p.qkv_bf16);
             sq[tid] = qv;
             sk[tid] = kv;
-            se[tid] = __expf(p.g[hk + tid]);
+            se[tid] = __expf(load_g(p, hk + tid, h, tid));
             pq = qv * qv;
             pk = kv * kv;
             pqk = qv * kv;
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
                 u += red_u[w][tid];
                 pv += red_q[w][tid];
             }
-            const float b = p.beta[row * H + h];
+            const float b = load_beta(p, row * H + h);
             const float d = b * (sv[tid] - u);
             sd[tid] = d;
             ov = p.scale * fmaf(kq, d, pv);

@@ -134,6 +134,29 @@ def make_inputs(w: Workload | str, device="cpu", *, T: int | None = None, H: int
     return out
 
 
+def make_logit_inputs(w: Workload | str, device="cpu", *, T: int | None = None, H: int | None = None,
+                      B: int | None = None, lengths: list | None = None, seed: int | None = None,
+                      z_mean: float = -4.0, logits_dtype=torch.bfloat16) -> dict:
+    """make_inputs(...) with the decay and write strength given as the layer's logits
+    instead of g and beta: g_logits [B,T,H,K] ~ N(z_mean, 1), beta_logits [B,T,H] ~ N(0, 1)
+    (both in ``logits_dtype``), A_log [H] = log U(1, 16), dt_bias [H,K] ~ U(-1/2, 1/2),
+    lower bound -5.  q, k, v, the states and the norm inputs are drawn as in make_inputs
+    (the same seed gives the same q, k, v)."""
+    d = make_inputs(w, device, T=T, H=H, B=B, lengths=lengths, seed=seed)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(10_000 + (WORKLOADS[w].seed if isinstance(w, str) else w.seed) + (seed or 0))
+    Bq, Tq, Hq, K = d["q"].shape
+    z = torch.randn((Bq, Tq, Hq, K), generator=gen, device=device) + z_mean
+    b = torch.randn((Bq, Tq, Hq), generator=gen, device=device)
+    d.pop("g")
+    d.pop("beta")
+    d.update(g_logits=z.to(logits_dtype).contiguous(), beta_logits=b.to(logits_dtype).contiguous(),
+             A_log=torch.log(torch.empty(Hq, device=device).uniform_(1.0, 16.0, generator=gen)),
+             dt_bias=torch.empty((Hq, K), device=device).uniform_(-0.5, 0.5, generator=gen),
+             g_lower_bound=GATE_LOWER_BOUND)
+    return d
+
+
 CONV_WORKLOADS = {
     "conv_prefill": dict(seed=5, B=1, T=8192, D=3 * 96 * 128, W=4, state=False),
     "conv_decode": dict(seed=6, B=256, T=1, D=3 * 96 * 128, W=4, state=True),
