@@ -604,6 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 8; ++c) x[c] = Pf[i * AP + j0 + c];
                 st_tile8(sb + S_PKGH, sb + S_PKGL, 192, i, j0, x);
             }
+            // every thread wrote P / Kg rows the tensor core reads (warp 0 does not reach
+            // the solve's fence); on regular chunks only warps 1-15 write P and fence there
+            fence_async_smem();
         }
         __syncthreads();
 
