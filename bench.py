@@ -330,6 +330,40 @@ def bench_short_conv(args, world, peaks):
     return out
 
 
+def bench_o_proj(args, world, peaks):
+    """The output projection (12288 -> 7168, bf16 in/out, fp32 accumulation) for the decode
+    batch (weight-bandwidth bound) and the 8192-token prompt (tensor bound)."""
+    import torch
+    import kimi_delta_attention_gated_gb300 as kda
+    out = {}
+    K, N = 96 * 128, 7168
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    w = (torch.randn((N, K), generator=g, device="cuda") * K ** -0.5).to(torch.bfloat16)
+    for name, rows in (("decode", 256), ("prefill", 8192)):
+        y = torch.randn((rows, K), generator=g, device="cuda").to(torch.bfloat16)
+        o = torch.empty((rows, N), device="cuda", dtype=torch.bfloat16)
+        fn = lambda: kda.o_proj(y, w, out=o)
+        steps = max(args.steps, 20)
+        r = time_steps(fn, steps, args.warmup, world)
+        kernel_ms = r["call_ms"] / max(1, r["launches"] // steps)
+        flop = 2.0 * rows * N * K
+        byts = (N * K + rows * K + rows * N) * 2
+        if name == "decode":
+            ach = byts / (kernel_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": byts}
+        else:
+            ach = flop / (kernel_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": ach / peaks["bf16_tflops"], "traffic": None, "algorithmic_flop_per_launch": flop}
+        roof.update(kernel_ms=kernel_ms, peak_source=peaks["source"])
+        out[name] = {"metric": "o_proj tokens/s", "value": world * rows / (r["ms_per_step"] * 1e-3), "unit": "tokens/s",
+                     "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
+                     "config": {"workload": f"o_proj rows={rows} 12288->7168 bf16 (cuBLASLt)"}, "roofline": roof}
+    return out
+
+
 def bench_e2e(args, world, d):
     """Same prefill through the public call with pinned host inputs and host outputs."""
     import torch
@@ -423,6 +457,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-logits", action="store_true")
+    ap.add_argument("--no-oproj", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -446,6 +481,7 @@ def main():
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
     conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
     logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
+    oproj = None if (args.no_oproj or args.only == "prefill") else bench_o_proj(args, world, peaks)
     e2e = None if (args.no_e2e or args.only == "prefill") else bench_e2e(args, world, d)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
@@ -459,7 +495,7 @@ def main():
         "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": pre["config"],
         "roofline": pre["roofline"], "roofline_tensor": pre["roofline_tensor"], "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
-        "short_conv": conv, "prefill_gate_logits": logits,
+        "short_conv": conv, "prefill_gate_logits": logits, "o_proj": oproj,
         "gpu": torch.cuda.get_device_name(),
     }
     print(json.dumps(line), flush=True)

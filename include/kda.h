@@ -262,6 +262,28 @@ kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *wei
                               const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int D, int W,
                               int activation, void *stream);
 
+/*
+ * kda_o_proj -- the layer's output projection applied to the gated-norm output y.
+ *
+ * Page: Kimi-K3 atlas "gate-project (decode, P = 1000)", sections "Parameters"
+ * (output projection: 88,080,384 weights = 12288 inputs x 7168 outputs) and "Code"
+ * (o = o_proj(o) after o_norm and the heads flattened to heads * head_dim).
+ *
+ *   out[r][n] = sum_c y[r][c] * w_o[n][c]            (nn.Linear, no bias)
+ *
+ *   y     [rows, in_features] bf16 (the y of kda_chunk_fwd / kda_recurrent_step with a
+ *         bf16 output dtype)
+ *   w_o   [out_features, in_features] bf16 (the nn.Linear weight layout)
+ *   out   [rows, out_features] out_dtype
+ *   workspace: caller-owned device scratch for the GEMM, workspace_bytes long (NULL
+ *         and 0 allowed; 32 MiB lets the library pick its fastest kernels).
+ * A plain dense GEMM, run by cuBLASLt with bf16 operands and fp32 accumulation.  The
+ * cuBLASLt handle is created on first use and kept for the process.  Feature counts
+ * must be multiples of 8.
+ */
+kda_status kda_o_proj(const void *y, const void *w_o, void *out, kda_dtype out_dtype, int64_t rows,
+                      int in_features, int out_features, void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,7 @@ import threading
 import torch
 
 __all__ = ["chunk_fwd", "chunk_fwd_logits", "recurrent_fwd", "recurrent_step", "recurrent_step_logits",
-           "gated_rmsnorm", "short_conv", "launch_count",
+           "gated_rmsnorm", "short_conv", "o_proj", "launch_count",
            "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -70,8 +70,9 @@ def _load():
                                              I, F, I, P, I, P, F, P, I, P]
         lib.kda_recurrent_step_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, I, I, I, I, F, I,
                                                   P, I, P, F, P, P]
+        lib.kda_o_proj.argtypes = [P, P, P, I, ctypes.c_int64, I, I, P, ctypes.c_size_t, P]
         for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
-                   "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits"):
+                   "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits", "kda_o_proj"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_launch_count.restype = ctypes.c_uint64
@@ -368,3 +369,36 @@ def short_conv(x, weight, bias=None, conv_state=None, *, cu_seqlens=None, activa
         _ptr(x), _dt(x), _ptr(weight), _ptr(bias), _ptr(conv_state), _ptr(final_state), _ptr(y), _dt(y),
         _ptr(cu_d), _ptr(cu_h), n_seqs, B, T, D, W, act, _stream()))
     return _to_host((y, final_state), host, dests)
+
+
+_WORKSPACE = {}
+O_PROJ_WORKSPACE_BYTES = 32 << 20
+
+
+def o_proj(y, w_o, *, out_dtype=torch.bfloat16, out=None, workspace=None):
+    """out [rows, out_features] = y [rows, in_features] @ w_o[out_features, in_features]^T
+    (bf16 operands, fp32 accumulation).  y may carry extra leading dimensions.  The
+    GEMM workspace is a per-device tensor this binding keeps (32 MiB) unless one is given."""
+    lib = _load()
+    host = y.device.type != "cuda"
+    dev = _device_of(y, w_o)
+    y2 = _prep(y, dev, torch.bfloat16).reshape(-1, y.shape[-1])
+    w = _prep(w_o, dev, torch.bfloat16)
+    rows, K = y2.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("w_o must be [out_features, in_features]")
+    dest = out if host else None
+    if out is None or host:
+        out = torch.empty((rows, N), device=dev, dtype=out_dtype)
+    if workspace is None:
+        key = dev.index if dev.index is not None else torch.cuda.current_device()
+        workspace = _WORKSPACE.get(key)
+        if workspace is None:
+            workspace = _WORKSPACE[key] = torch.empty(O_PROJ_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+    _check(lib.kda_o_proj(_ptr(y2), _ptr(w), _ptr(out), _dt(out), rows, K, N, _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream()))
+    res = out.reshape(*y.shape[:-1], N)
+    if host:
+        return _to_host((res,), True, (dest,))[0]
+    return res

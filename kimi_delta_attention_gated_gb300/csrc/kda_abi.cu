@@ -398,4 +398,24 @@ kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *wei
                                   (cudaStream_t)stream);
 }
 
+kda_status kda_o_proj(const void *y, const void *w_o, void *out, kda_dtype out_dtype, int64_t rows,
+                      int in_features, int out_features, void *workspace, size_t workspace_bytes, void *stream) {
+    kda::g_err[0] = 0;
+    const char *fn = "kda_o_proj";
+    KDA_REQUIRE(rows >= 0 && in_features > 0 && out_features > 0, KDA_ERR_INVALID_ARG,
+                "%s: need rows >= 0 and positive feature counts", fn);
+    KDA_REQUIRE(rows == 0 || (y && w_o && out), KDA_ERR_INVALID_ARG, "%s: y, w_o and out must not be NULL", fn);
+    KDA_REQUIRE(dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED, "%s: unsupported out dtype", fn);
+    KDA_REQUIRE(in_features % 8 == 0 && out_features % 8 == 0, KDA_ERR_UNSUPPORTED,
+                "%s: feature counts must be multiples of 8", fn);
+    KDA_REQUIRE(rows <= INT32_MAX, KDA_ERR_INVALID_ARG, "%s: too many rows", fn);
+    KDA_REQUIRE(workspace_bytes == 0 || workspace, KDA_ERR_INVALID_ARG, "%s: workspace_bytes > 0 needs a workspace", fn);
+    const void *ptrs[] = {y, w_o, out, workspace};
+    for (const void *ptr : ptrs)
+        KDA_REQUIRE(!ptr || aligned16(ptr), KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);
+    if (rows == 0) return KDA_OK;
+    return kda::launch_o_proj(y, w_o, out, out_dtype == KDA_BF16, rows, in_features, out_features, workspace,
+                              workspace_bytes, (cudaStream_t)stream);
+}
+
 }  // extern "C"

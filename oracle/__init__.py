@@ -209,5 +209,12 @@ def short_conv(x, weight, bias=None, conv_state=None, *, cu_seqlens=None, activa
     return y, sf
 
 
+def o_proj(y, w_o):
+    """The layer's output projection, out = y @ w_o^T in fp64 (nn.Linear without bias;
+    Kimi-K3 atlas "gate-project (decode, P = 1000)", sections "Parameters" and "Code").
+    A library matmul serves as the one step."""
+    return np.asarray(y, np.float64) @ np.asarray(w_o, np.float64).T
+
+
 def version() -> int:
     return int(_load().kda_oracle_version())

@@ -189,3 +189,14 @@ def test_short_conv_rejects(lib, over, code):
 def test_short_conv_rejects_bad_cu_seqlens(lib):
     arr, ptr = cu_host([0, 9, 4, 64])
     assert conv_call(lib, cu=FAKE, cu_host=ptr, n_seqs=3) == INVALID
+
+
+def test_o_proj_rejects(lib):
+    f = lib.kda_o_proj
+    ws = ctypes.c_size_t
+    assert f(None, FAKE, FAKE, BF16, ctypes.c_int64(4), 64, 64, None, ws(0), None) == INVALID
+    assert f(FAKE, FAKE, FAKE, BF16, ctypes.c_int64(4), 60, 64, None, ws(0), None) == UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 9, ctypes.c_int64(4), 64, 64, None, ws(0), None) == UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, BF16, ctypes.c_int64(4), 64, 64, None, ws(1024), None) == INVALID
+    assert f(FAKE + 4, FAKE, FAKE, BF16, ctypes.c_int64(4), 64, 64, None, ws(0), None) == INVALID
+    assert f(None, None, None, BF16, ctypes.c_int64(0), 64, 64, None, ws(0), None) == OK  # nothing to do

@@ -1,0 +1,48 @@
+"""GPU parity of the output projection (kda_o_proj, cuBLASLt bf16 GEMM, fp32 accumulation)
+against the oracle's fp64 matmul of the same bf16 inputs: a ragged small case in fp32 and
+bf16 output, and the decode / prefill shapes of the layer (12288 -> 7168) on sampled
+output columns.  Tolerance: fp32 accumulation over K terms of unit-scale products
+(max|diff| / rms 1e-4); bf16 outputs add one rounding per element (2^-8 relative)."""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_gated_gb300 as kda
+import oracle
+from tests.gpu_helpers import rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _data(rows, K, N, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    y = torch.randn((rows, K), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((N, K), generator=g, device="cuda") * K ** -0.5).to(torch.bfloat16)
+    return y, w
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_small_ragged(out_dtype):
+    y, w = _data(37, 1024, 776, 0)
+    out = kda.o_proj(y, w, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ref = oracle.o_proj(y.float().cpu().numpy(), w.float().cpu().numpy())
+    if out_dtype == torch.float32:
+        assert rel_err(out, ref) <= 1e-4
+    else:  # one bf16 rounding of each output (half an ulp: 2^-9 relative) on top of fp32 accumulation
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        assert np.all(np.abs(out.double().cpu().numpy() - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * rms)
+
+
+@pytest.mark.parametrize("rows", [256, 8192])
+def test_layer_shape_sampled(rows):
+    y, w = _data(rows, 12288, 7168, 1 + rows)
+    out = kda.o_proj(y, w, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    cols = np.sort(np.random.default_rng(rows).choice(7168, 64, replace=False))
+    rsel = np.sort(np.random.default_rng(rows + 1).choice(rows, min(rows, 256), replace=False))
+    ref = oracle.o_proj(y[torch.from_numpy(rsel).cuda()].float().cpu().numpy(),
+                        w[torch.from_numpy(cols).cuda()].float().cpu().numpy())
+    got = out[torch.from_numpy(rsel).cuda()][:, torch.from_numpy(cols).cuda()]
+    assert rel_err(got, ref) <= 1e-4
