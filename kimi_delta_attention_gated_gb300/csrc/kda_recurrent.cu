@@ -67,7 +67,9 @@ __device__ __forceinline__ void st_row(float *p, const float (&r)[VPL]) {
     }
 }
 
-template <int K, int V>
+// GL: g and beta come from their logits (a compile-time choice, so the plain path keeps
+// its schedule).
+template <int K, int V, bool GL>
 __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) {
     constexpr int RPW = K / kWarps;  // rows per warp
     constexpr int VPL = V / 32;      // columns per lane
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
             const float kv = ld_in(p.k, hk + tid, p.qkv_bf16);
             sq[tid] = qv;
             sk[tid] = kv;
-            se[tid] = __expf(load_g(p, hk + tid, h, tid));
+            se[tid] = __expf(GL ? load_g(p, hk + tid, h, tid) : p.g[hk + tid]);
             pq = qv * qv;
             pk = kv * kv;
             pqk = qv * kv;
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
                 u += red_u[w][tid];
                 pv += red_q[w][tid];
             }
-            const float b = load_beta(p, row * H + h);
+            const float b = GL ? load_beta(p, row * H + h) : p.beta[row * H + h];
             const float d = b * (sv[tid] - u);
             sd[tid] = d;
             ov = p.scale * fmaf(kq, d, pv);
@@ -217,7 +219,10 @@ template <int K, int V>
 kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return KDA_OK;
-    recurrent_kernel<K, V><<<units, kThreads, 0, st>>>(p);
+    if (p.g_logits)
+        recurrent_kernel<K, V, true><<<units, kThreads, 0, st>>>(p);
+    else
+        recurrent_kernel<K, V, false><<<units, kThreads, 0, st>>>(p);
     note_launch();
     return check_launch("recurrent_kernel");
 }
