@@ -211,6 +211,7 @@ struct ChunkRegs {
     float beta;   // token warp * 4 + lane, lanes 0-3 (or its logit until prepared)
 };
 
+template <bool GL>
 __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, int bos, int t0, int cn, int h,
                                            int warp, int l4) {
 #pragma unroll
@@ -221,7 +222,7 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
         cr.k[r] = make_uint2(0u, 0u);
         if (i < cn) {
             const size_t hk = ((size_t)(bos + t0 + i) * p.H + h) * DK + l4;
-            if (!p.g_logits) {
+            if (!GL) {
                 cr.g[r] = __ldg(reinterpret_cast<const float4 *>(p.g + hk));
             } else if (p.g_logits_bf16) {
                 const uint2 u = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.g_logits) + hk));
@@ -237,9 +238,12 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
     const int ib = warp * 4 + ((l4 >> 2) & 3);
     const bool okb = l4 < 16 && ib < cn;
     const size_t bi = (size_t)(bos + t0 + (okb ? ib : 0)) * p.H + h;
-    cr.beta = !okb ? 0.f : (p.beta_logits ? ld_in(p.beta_logits, bi, p.beta_logits_bf16) : __ldg(p.beta + bi));
+    cr.beta = !okb ? 0.f : (GL ? ld_in(p.beta_logits, bi, p.beta_logits_bf16) : __ldg(p.beta + bi));
 }
 
+// GL: g and beta come from their logits (a compile-time choice; the plain path carries no
+// trace of it).
+template <bool GL>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ TcParams tp) {
     const SeqParams &p = tp.p;
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // first chunk's inputs are in flight while the CTA sets up
     ChunkRegs cr;
-    load_chunk(p, cr, bos, 0, min(C, len), h, warp, l4);
+    load_chunk<GL>(p, cr, bos, 0, min(C, len), h, warp, l4);
 
     if (tid == 0) {
         for (int b = 0; b < 6; ++b) mbar_init(bar_g + b, 1);
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The 8 sums of squares of a warp's 4 tokens are reduced with a reduce-scatter
     // (9 shuffles); lanes 4v..4v+3 end with sum v (q of tokens 0-3, then k).
     auto prep_norms = [&](ChunkRegs &c, int cnn) {
-        if (p.g_logits) {  // g from its logits; tokens past the chunk's end keep g = 0
+        if (GL) {  // g from its logits; tokens past the chunk's end keep g = 0
             const float a_h = __expf(__ldg(p.A_log + h));
             const float4 db = p.dt_bias ? __ldg(reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * DK + l4))
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -364,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      live ? gate_of_logit(z[3] + db.w, a_h, p.g_lower) : 0.f);
             }
         }
-        if (p.beta_logits && lane < 4) c.beta = warp * 4 + lane < cnn ? beta_of_logit(c.beta) : 0.f;
+        if (GL && lane < 4) c.beta = warp * 4 + lane < cnn ? beta_of_logit(c.beta) : 0.f;
         float a[8];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // start loading the next chunk while waiting for the gram
-        if (ch + 1 < nchunks) load_chunk(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
+        if (ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
         if (!wait_group(bar_g, par)) failed = 1;
         if (!fallback) {
             uint32_t r1[16], r2[16];
@@ -917,14 +921,19 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
     }
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) {
-            set_error("chunk_tc: cannot reserve %u bytes of shared memory: %s", SMEM_BYTES, cudaGetErrorString(e));
-            return KDA_ERR_CUDA;
+        for (void *fn : {(void *)chunk_tc_kernel<false>, (void *)chunk_tc_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            if (e != cudaSuccess) {
+                set_error("chunk_tc: cannot reserve %u bytes of shared memory: %s", SMEM_BYTES, cudaGetErrorString(e));
+                return KDA_ERR_CUDA;
+            }
         }
         configured = true;
     }
-    chunk_tc_kernel<<<units, kThreads, SMEM_BYTES, st>>>(tmap, tp);
+    if (p_in.g_logits)
+        chunk_tc_kernel<true><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tp);
+    else
+        chunk_tc_kernel<false><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tp);
     note_launch();
     return check_launch("chunk_tc_kernel");
 }
