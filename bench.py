@@ -40,16 +40,25 @@ PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits b
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture: (330.24 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # B=1 T=2048 H=96 capture: (252.69 + 77.26 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                "sha256": "ccbfb420e83fed6b91d32833e3c9549ad036d7e6470f521a6a048e86be61d4e3",
-                "bytes_per_unit": (330.24e6 - 6.29e6) / (2048 * 96),
+                "sha256": "011760b2d18caf98b96a7e50acb40557ce98542073a45879c3769f37d668d063",
+                "bytes_per_unit": (252.687616e6 + 77.263872e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
-    # B=64 capture: 757.3 MB / (64 * 96) (sequence, head) units
+    # B=64 capture: mean of two launches, 755.2 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
-               "sha256": "0691f03b03e90ea0ee70519ef2406d711739f838c832ffdc89a8050a1db954f4",
-               "bytes_per_unit": 757.3e6 / (64 * 96),
+               "sha256": "3d1913e5bd8d5b799678049317268377001a3f8774c6e27d2d4a1afa97da2178",
+               "bytes_per_unit": 755.20192e6 / (64 * 96),
                "capture": "profiles/recurrent_kernel_decode_B64.md"},
+    # full-size captures: mean of two launches per (token, channel) element
+    "conv_prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
+                     "sha256": "bcea7fe67f85f7bded7c12252f074e37a94f9db2855316708dd42e3358c4d85e",
+                     "bytes_per_unit": 1172.00192e6 / (8192 * 36864),
+                     "capture": "profiles/short_conv_kernels.md"},
+    "conv_decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
+                    "sha256": "bcea7fe67f85f7bded7c12252f074e37a94f9db2855316708dd42e3358c4d85e",
+                    "bytes_per_unit": 204.386944e6 / (256 * 36864),
+                    "capture": "profiles/short_conv_kernels.md"},
 }
 
 
@@ -449,7 +458,7 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
@@ -472,8 +481,11 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "conv"):
-        res = bench_decode(args, world, peaks) if args.only == "decode" else bench_short_conv(args, world, peaks)
+    if args.only in ("decode", "conv", "kernels"):
+        if args.only == "kernels":  # decode step + short convolution (profiling runs)
+            res = {"decode": bench_decode(args, world, peaks), "short_conv": bench_short_conv(args, world, peaks)}
+        else:
+            res = bench_decode(args, world, peaks) if args.only == "decode" else bench_short_conv(args, world, peaks)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
