@@ -204,6 +204,33 @@ __device__ __forceinline__ void conv_tokens(const ConvParams &p, const uint8_t *
     const uint8_t *xs = tile + ((size_t)(ta - (t0 - NH)) * kCh + ch) * ES;
     uint8_t *yp = reinterpret_cast<uint8_t *>(p.y) + ((size_t)ta * D + c0) * YS;
     const size_t ystride = D * YS;
+    if (tb - ta == kTokPer && eos >= tb) {
+        // fast path: all kTokPer tokens in one sequence; unrolled, the window slides by renaming
+        float xw[kTokPer + NH][kVec];
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) xw[j][e] = win[j][e];
+#pragma unroll
+        for (int k = 0; k < kTokPer; ++k) lds_vec<XB>(xs + (size_t)k * kCh * ES, 0, xw[NH + k]);
+#pragma unroll
+        for (int k = 0; k < kTokPer; ++k) {
+            float z[kVec];
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) {
+                float a = fmaf(wv[W - 1][e], xw[NH + k][e], bv[e]);
+#pragma unroll
+                for (int j = 0; j < NH; ++j) a = fmaf(wv[j][e], xw[k + j][e], a);
+                z[e] = ACT ? __fdividef(a, 1.f + __expf(-a)) : a;
+            }
+            st_vec<YB>(yp + (size_t)k * ystride, 0, z);
+        }
+        if (eos == tb && p.sT) {
+#pragma unroll
+            for (int j = 0; j < NH; ++j) st_state(p.sT, ((size_t)n * NH + j) * D + c0, xw[kTokPer + j]);
+        }
+        return;
+    }
     int left = (int)(eos - ta < kTile + 1 ? eos - ta : kTile + 1);  // tokens until the sequence ends
     const int cnt = (int)(tb - ta);
 #pragma unroll 4
