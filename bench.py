@@ -396,7 +396,9 @@ def bench_e2e(args, world, d):
     torch.cuda.synchronize()
     dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
     return {"value": world * B * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": dt * 1e3, "steps": steps}
+            "ms_per_step": dt * 1e3, "steps": steps,
+            "path": f"chunk_fwd on pinned host tensors: {kda.HOST_SEGMENT}-token segments, copy-in / compute / "
+                    "copy-out on three streams"}
 
 
 def cpu_baseline(d, heads: int):
