@@ -52,12 +52,12 @@ MEASURED_TRAFFIC = {
                "capture": "profiles/recurrent_kernel_decode_B64.md"},
     # full-size captures: mean of two launches per (token, channel) element
     "conv_prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
-                     "sha256": "bcea7fe67f85f7bded7c12252f074e37a94f9db2855316708dd42e3358c4d85e",
-                     "bytes_per_unit": 1172.00192e6 / (8192 * 36864),
+                     "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
+                     "bytes_per_unit": 1179.379712e6 / (8192 * 36864),
                      "capture": "profiles/short_conv_kernels.md"},
     "conv_decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
-                    "sha256": "bcea7fe67f85f7bded7c12252f074e37a94f9db2855316708dd42e3358c4d85e",
-                    "bytes_per_unit": 204.386944e6 / (256 * 36864),
+                    "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
+                    "bytes_per_unit": 204.395008e6 / (256 * 36864),
                     "capture": "profiles/short_conv_kernels.md"},
 }
 

@@ -254,7 +254,7 @@ kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,
  * Varlen mode: as kda_chunk_fwd (B = 1, T packed, cu_seqlens device int32
  *   [n_seqs + 1], optional host copy cu_seqlens_host, which is then checked).
  * A decode step is T = 1 with both states given.  Supported: W in {2, 3, 4},
- * D a multiple of 8, B * T < 65535 * 64.  Returns a kda_status.
+ * D a multiple of 8, B * T <= INT32_MAX.  Returns a kda_status.
  */
 kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *weight, const float *bias,
                               const float *conv_state_in, float *conv_state_out, void *y,

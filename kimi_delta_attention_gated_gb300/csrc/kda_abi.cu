@@ -363,7 +363,7 @@ kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *wei
     KDA_REQUIRE(W >= 2 && W <= 4, KDA_ERR_UNSUPPORTED, "%s: W=%d (supported: 2, 3, 4)", fn, W);
     KDA_REQUIRE(D % 8 == 0, KDA_ERR_UNSUPPORTED, "%s: D=%d must be a multiple of 8", fn, D);
     KDA_REQUIRE(activation == 0 || activation == 1, KDA_ERR_INVALID_ARG, "%s: activation must be 0 or 1", fn);
-    KDA_REQUIRE(rows <= (int64_t)65535 * 64, KDA_ERR_UNSUPPORTED, "%s: B*T=%lld too large", fn, (long long)rows);
+    KDA_REQUIRE(rows <= (int64_t)INT32_MAX, KDA_ERR_INVALID_ARG, "%s: B*T=%lld too large", fn, (long long)rows);
     const void *ptrs[] = {x, weight, bias, conv_state_in, conv_state_out, y, cu_seqlens};
     for (const void *ptr : ptrs)
         KDA_REQUIRE(!ptr || aligned16(ptr), KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);

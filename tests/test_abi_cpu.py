@@ -179,7 +179,7 @@ def conv_call(lib, **over):
     (dict(cu=FAKE, n_seqs=0), INVALID),
     (dict(cu=FAKE, n_seqs=2, B=2), INVALID),
     (dict(cu_host=FAKE), INVALID),
-    (dict(B=70000, T=64), UNSUPPORTED),             # grid limit
+    (dict(B=70000, T=40000), INVALID),              # B*T beyond int32
 ])
 def test_short_conv_rejects(lib, over, code):
     assert conv_call(lib, **over) == code
