@@ -91,8 +91,10 @@ constexpr uint32_t F_RQ = 64;     // q scale per token (norm * scale) [64]
 constexpr uint32_t F_RK = 128;    // k norm per token [64]
 constexpr uint32_t F_GEXP = 192;  // exp(gamma) [128]
 constexpr uint32_t F_RED = 320;   // norm partials [4 wg][4 quarters][16]
-constexpr uint32_t F_END = 576;
-constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 6 mbarriers + tmem slot
+constexpr uint32_t F_BETA0 = 576; // beta of tokens 0-3 (warp 0 prepares them while the solve reads F_BETA)
+constexpr uint32_t F_SCAN0 = 580; // decay totals of tokens 0-3 [128]
+constexpr uint32_t F_END = 708;
+constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 7 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = S_BARS + 64 + 1024;  // + alignment slack
 // scan scratch aliases T (free during prep): [16 warps][128] floats
 constexpr uint32_t S_SCAN = S_T;
@@ -130,14 +132,26 @@ __device__ __forceinline__ void st_tile8(uint32_t hi_base, uint32_t lo_base, uin
 }
 
 // Kg^T rows c..c+3 (one per key channel) at columns j0..j0+3 (4 tokens) of the
-// [P ; Kg^T] tiles, hi and lo: x[t][e] is token j0 + t, channel c + e.
+// [P ; Kg^T] tiles, hi and lo: x[t][e] is token j0 + t, channel c + e, c = 4 * lane.
+// Store e of a lane writes channel c + ((e + rot) & 3) with rot = (lane >> 1) & 3, so the
+// 32 rows of one store cover all 8 swizzle phases (4 wavefronts instead of 16).
 __device__ __forceinline__ void st_kgt(uint32_t sb, int c, int j0, const float (&x)[4][4]) {
+    const int rot = (c >> 3) & 3;
+    float y[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        float a[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = (rot & 1) ? x[t][(e + 1) & 3] : x[t][e];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[t][e] = (rot & 2) ? a[(e + 2) & 3] : a[e];
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         uint32_t h0, l0, h1, l1;
-        split2(x[0][e], x[1][e], h0, l0);
-        split2(x[2][e], x[3][e], h1, l1);
-        const uint32_t off = sw128_off(64 + c + e, j0, 192);
+        split2(y[0][e], y[1][e], h0, l0);
+        split2(y[2][e], y[3][e], h1, l1);
+        const uint32_t off = sw128_off(64 + c + ((e + rot) & 3), j0, 192);
         st_shared_v2(sb + S_PKGH + off, h0, h1);
         st_shared_v2(sb + S_PKGL + off, l0, l1);
     }
@@ -204,7 +218,8 @@ __device__ __forceinline__ void tri_offdiag(float *Asm, float *Tsm, int ctid) {
     tbar();
 }
 
-// Loads of one chunk's q, k, g for this thread's 4 tokens x 4 key channels.
+// One chunk's q and k for this thread's 4 tokens x 4 key channels (loaded into
+// registers ahead of use), and g, read from its TMA-staged tile when the chunk is prepared.
 struct ChunkRegs {
     float4 g[4];  // g, or its raw logits (fp32, or bf16 bits in .x/.y) until the chunk is prepared
     uint2 q[4], k[4];
@@ -217,19 +232,10 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = warp * 4 + r;
-        cr.g[r] = make_float4(0.f, 0.f, 0.f, 0.f);
         cr.q[r] = make_uint2(0u, 0u);
         cr.k[r] = make_uint2(0u, 0u);
         if (i < cn) {
             const size_t hk = ((size_t)(bos + t0 + i) * p.H + h) * DK + l4;
-            if (!GL) {
-                cr.g[r] = __ldg(reinterpret_cast<const float4 *>(p.g + hk));
-            } else if (p.g_logits_bf16) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.g_logits) + hk));
-                cr.g[r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), 0.f, 0.f);
-            } else {
-                cr.g[r] = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.g_logits) + hk));
-            }
             cr.q[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + hk));
             cr.k[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
         }
@@ -245,7 +251,8 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
 // trace of it).
 template <bool GL>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ TcParams tp) {
+    chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_g,
+                    const __grid_constant__ TcParams tp) {
     const SeqParams &p = tp.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -260,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar_s = bar_g + 3;                                    // O and S updates
     uint64_t *tma_bar = bar_g + 4;                                  // V tile
     uint64_t *drain_bar = bar_g + 5;                                // drain after a failure
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 48);
+    uint64_t *gt_bar = bar_g + 6;                                   // g tile
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 56);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wg = warp >> 2, wq = warp & 3;
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_chunk<GL>(p, cr, bos, 0, min(C, len), h, warp, l4);
 
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) mbar_init(bar_g + b, 1);
+        for (int b = 0; b < 7; ++b) mbar_init(bar_g + b, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -307,9 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sb + S_V + 8192, &tmap_v, tma_bar, 64, h, bos + chunk * C);
     };
     int v_pending = -1;  // chunk whose V tile is in flight (thread 0 only)
+    // g (or its logits) of one chunk, 64 tokens x 128 channels, into the Km tile, which is
+    // free from the end of a gram pass until the next operand tiles are written
+    const uint32_t g_bytes = (GL && p.g_logits_bf16) ? C * DK * 2 : C * DK * 4;
+    auto issue_g = [&](int chunk) {
+        mbar_arrive_expect_tx(gt_bar, g_bytes);
+        tma_load_3d(sb + S_KM, &tmap_g, gt_bar, 0, h, bos + chunk * C);
+    };
+    int g_pending = -1;  // chunk whose g tile is in flight (thread 0 only)
+    int failed = 0;      // a bounded wait gave up
     if (tid == 0 && nchunks > 0) {
         issue_v(0);
         v_pending = 0;
+        issue_g(0);
+        g_pending = 0;
     }
 
     {  // initial state -> S^T accumulator and its hi/lo copy; O^T = 0
@@ -347,7 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // small buffers, each warp's decay totals per key channel into the scan buffer.
     // The 8 sums of squares of a warp's 4 tokens are reduced with a reduce-scatter
     // (9 shuffles); lanes 4v..4v+3 end with sum v (q of tokens 0-3, then k).
-    auto prep_norms = [&](ChunkRegs &c, int cnn) {
+    auto prep_norms = [&](ChunkRegs &c, int cnn, int chunk) {
+        if (!mbar_wait(gt_bar, (uint32_t)(chunk & 1), kPolls))
+            failed = 1;
+        else if (tid == 0)
+            g_pending = -1;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {  // tokens past the chunk's end read as g = 0
+            const int i = warp * 4 + r;
+            if (GL && p.g_logits_bf16) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(sm + S_KM + (i * DK + l4) * 2);
+                c.g[r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), 0.f, 0.f);
+            } else {
+                c.g[r] = *reinterpret_cast<const float4 *>(sm + S_KM + (i * DK + l4) * 4);
+            }
+            if (!GL && i >= cnn) c.g[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         if (GL) {  // g from its logits; tokens past the chunk's end keep g = 0
             const float a_h = __expf(__ldg(p.A_log + h));
             const float4 db = p.dt_bias ? __ldg(reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * DK + l4))
@@ -396,13 +430,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 fs[F_RK + warp * 4 + v - 4] = sc;
         }
-        if (lane < 4) fs[F_BETA + warp * 4 + lane] = c.beta;
+        if (lane < 4) fs[(!GL && warp == 0 ? F_BETA0 : F_BETA + warp * 4) + lane] = c.beta;
         float4 t = c.g[0];
 #pragma unroll
         for (int r = 1; r < 4; ++r) {
             t.x += c.g[r].x; t.y += c.g[r].y; t.z += c.g[r].z; t.w += c.g[r].w;
         }
-        *reinterpret_cast<float4 *>(scan + warp * 128 + l4) = t;
+        *reinterpret_cast<float4 *>(!GL && warp == 0 ? fs + F_SCAN0 + l4 : scan + warp * 128 + l4) = t;
+    };
+    // With g and beta given (!GL), warp 0 (which issues the tensor-core work) prepares its
+    // tokens' norms while the solve runs, into side buffers; beta joins the others once
+    // the current chunk's solve has read F_BETA.  With logits, the transforms take longer
+    // than the solve leaves, and warp 0 prepares its tokens with the others.
+    auto beta0_publish = [&]() {
+        if (!GL && warp == 0 && lane < 4) fs[F_BETA + lane] = fs[F_BETA0 + lane];
     };
 
     // ---- preparation, second half (after a barrier): cumulative decay, exp(gamma),
@@ -412,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o4[4] = {0.f, 0.f, 0.f, 0.f}, gam[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < 16; ++w) {  // offset of this warp's tokens and the chunk total, per channel
-            const float4 t = *reinterpret_cast<const float4 *>(scan + w * 128 + l4);
+            const float4 t = *reinterpret_cast<const float4 *>(!GL && w == 0 ? fs + F_SCAN0 + l4 : scan + w * 128 + l4);
             const float tt[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -473,14 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's tensor-core waits)
     int oor_next = 0;
     if (nchunks > 0) {
-        prep_norms(cr, min(C, len));
+        prep_norms(cr, min(C, len), 0);
+        beta0_publish();
         __syncthreads();
         float kgv[4][4];
         oor_next = prep_tiles(cr, kgv);
         st_kg(kgv);
     }
 
-    int failed = 0;
     for (int ch = 0; ch < nchunks; ++ch) {
         const int par = ch & 1;
         const int t0 = ch * C;
@@ -511,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar_g);  // an empty commit on fallback chunks
         }
         __syncwarp();
-        // start loading the next chunk while waiting for the gram
-        if (ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
+        // warps 1-15 (every warp with logits) start loading the next chunk while waiting for the gram
+        if ((GL || warp > 0) && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
         if (!wait_group(bar_g, par)) failed = 1;
         if (!fallback) {
             uint32_t r1[16], r2[16];
@@ -614,6 +655,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
 
+        if (warp == 0) {
+            if (lane == 0 && ch + 1 < nchunks && !failed) {  // the gram has read Km (and the exact path its G scratch)
+                issue_g(ch + 1);
+                g_pending = ch + 1;
+            }
+            if (!GL && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
+        }
         if (tid == 0) {
             // ================= R^T = V^T I + S^T (-Kd)^T, O^T = S^T Qd^T (while warps 1-15 solve T)
             if (mbar_wait(tma_bar, (uint32_t)par, kPolls))
@@ -664,6 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_async_smem();
         }
         __syncwarp();
+        // warp 0, idle while the solve runs (g and beta given): the next chunk's norms for its own tokens
+        if (!GL && warp == 0 && ch + 1 < nchunks) prep_norms(cr, min(C, len - t0 - C), ch + 1);
         __syncthreads();
 
         // ================= R pass: R^T (lane v, column j) -> hi/lo operand in TMEM
@@ -701,7 +751,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // while D runs: the next chunk's norms, beta and decay totals
-        if (ch + 1 < nchunks) prep_norms(cr, min(C, len - t0 - C));
+        if (ch + 1 < nchunks) {
+            if (GL || warp > 0) {
+                prep_norms(cr, min(C, len - t0 - C), ch + 1);
+            } else {
+                beta0_publish();
+            }
+        }
         // ================= D pass (hi/lo into TMEM) and S decay by exp(gamma)
         if (!wait_group(bar_d, par)) failed = 1;
         {
@@ -758,19 +814,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             uint32_t r[16];
             const int c0 = wg * 32;
-            {
-                uint32_t s1[16], s2[16], hi[16], lo[16];
+            {  // S^T columns c0.. as packed hi/lo pairs, 16 columns at a time
+                uint32_t s1[16], hi[8], lo[8];
                 tmem_ld16(tb + lane_off + T_O + wg * 16, r);
-                tmem_ld16(tb + lane_off + T_S + c0, s1);
-                tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
-                tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    split2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]), hi[c], lo[c]);
-                    split2(__uint_as_float(s2[2 * c]), __uint_as_float(s2[2 * c + 1]), hi[8 + c], lo[8 + c]);
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld16(tb + lane_off + T_S + c0 + half * 16, s1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        split2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]), hi[c], lo[c]);
+                    tmem_st8(tb + lane_off + T_SH + wg * 16 + half * 8, hi);
+                    tmem_st8(tb + lane_off + T_SL + wg * 16 + half * 8, lo);
                 }
-                tmem_st16(tb + lane_off + T_SH + wg * 16, hi);
-                tmem_st16(tb + lane_off + T_SL + wg * 16, lo);
                 const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
                 tmem_st16(tb + lane_off + T_O + wg * 16, zero);  // O^T starts from zero next chunk
             }
@@ -824,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicAdd(&g_chunk_tc_timeouts, 1);
             mma_commit(drain_bar);  // arrives once the tensor-core work already issued has drained
             if (v_pending >= 0) mbar_wait(tma_bar, (uint32_t)(v_pending & 1), kPolls);  // V copy in flight
+            if (g_pending >= 0) mbar_wait(gt_bar, (uint32_t)(g_pending & 1), kPolls);   // g copy in flight
         }
         __syncthreads();
         mbar_wait(drain_bar, 0, kPolls);
@@ -901,6 +958,22 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
         set_error("chunk_tc: cuTensorMapEncodeTiled failed (%d)", (int)cres);
         return KDA_ERR_CUDA;
     }
+    CUtensorMap tmap_g;
+    {
+        const bool gb = p_in.g_logits && p_in.g_logits_bf16;
+        const cuuint64_t es = gb ? 2 : 4;
+        const void *gsrc = p_in.g_logits ? p_in.g_logits : (const void *)p_in.g;
+        const cuuint64_t gdims[3] = {(cuuint64_t)DK, (cuuint64_t)p_in.H, (cuuint64_t)rows};
+        const cuuint64_t gstrides[2] = {(cuuint64_t)DK * es, (cuuint64_t)p_in.H * DK * es};
+        const cuuint32_t gbox[3] = {(cuuint32_t)DK, 1, (cuuint32_t)C};
+        cres = enc(&tmap_g, gb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<void *>(gsrc), gdims, gstrides, gbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cres != CUDA_SUCCESS) {
+            set_error("chunk_tc: cuTensorMapEncodeTiled failed for g (%d)", (int)cres);
+            return KDA_ERR_CUDA;
+        }
+    }
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     tp.p = p_in;
@@ -931,9 +1004,9 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
         configured = true;
     }
     if (p_in.g_logits)
-        chunk_tc_kernel<true><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tp);
+        chunk_tc_kernel<true><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tp);
     else
-        chunk_tc_kernel<false><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tp);
+        chunk_tc_kernel<false><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tp);
     note_launch();
     return check_launch("chunk_tc_kernel");
 }
