@@ -96,7 +96,8 @@ constexpr uint32_t F_SCAN0 = 580; // decay totals of tokens 0-3 [128]
 constexpr uint32_t F_END = 708;
 constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 7 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = S_BARS + 64 + 1024;  // + alignment slack
-// scan scratch aliases T (free during prep): [16 warps][128] floats
+// scan scratch aliases T (free during prep): [16 warps][128] floats of decay totals, then
+// their exclusive prefixes [16][128] and the chunk total [128]
 constexpr uint32_t S_SCAN = S_T;
 // fallback scratch: G fp32 [64][128] in the Km tile (Km is not used then)
 constexpr uint32_t S_FB_G = S_KM;
@@ -449,16 +450,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- preparation, second half (after a barrier): cumulative decay, exp(gamma),
     // the [-Kd ; Qd] and Km operand tiles; Kg is returned in registers because its
     // tile may still be in use.  Returns 1 if the chunk's decay range is too wide.
-    auto prep_tiles = [&](const ChunkRegs &c, float (&kgv)[4][4]) -> int {
+    // ---- exclusive prefix of the warps' decay totals per key channel, and the chunk
+    // total (row 16), by warps 1-4; then a barrier of warps 1-15 (warp 0 is issuing)
+    float *pre = scan + 16 * 128;
+    auto scan_prefix = [&]() {
+        if (warp >= 1 && warp <= 4) {
+            const int c = tid - 32;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+                const float t = (!GL && w == 0) ? fs[F_SCAN0 + c] : scan[w * 128 + c];
+                pre[w * 128 + c] = acc;
+                acc += t;
+            }
+            pre[16 * 128 + c] = acc;
+        }
+        tbar();
+    };
+
+    auto prep_tiles = [&](const ChunkRegs &c, float (&kgv)[4][4], bool use_pre) -> int {
         float o4[4] = {0.f, 0.f, 0.f, 0.f}, gam[4] = {0.f, 0.f, 0.f, 0.f};
+        if (use_pre) {  // offset of this warp's tokens and the chunk total, per channel
+            const float4 t = *reinterpret_cast<const float4 *>(pre + warp * 128 + l4);
+            const float4 u = *reinterpret_cast<const float4 *>(pre + 16 * 128 + l4);
+            o4[0] = t.x; o4[1] = t.y; o4[2] = t.z; o4[3] = t.w;
+            gam[0] = u.x; gam[1] = u.y; gam[2] = u.z; gam[3] = u.w;
+        } else {
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {  // offset of this warp's tokens and the chunk total, per channel
-            const float4 t = *reinterpret_cast<const float4 *>(!GL && w == 0 ? fs + F_SCAN0 + l4 : scan + w * 128 + l4);
-            const float tt[4] = {t.x, t.y, t.z, t.w};
+            for (int w = 0; w < 16; ++w) {
+                const float4 t = *reinterpret_cast<const float4 *>(!GL && w == 0 ? fs + F_SCAN0 + l4 : scan + w * 128 + l4);
+                const float tt[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (w < warp) o4[e] += tt[e];
-                gam[e] += tt[e];
+                for (int e = 0; e < 4; ++e) {
+                    if (w < warp) o4[e] += tt[e];
+                    gam[e] += tt[e];
+                }
             }
         }
         float egam[4];
@@ -518,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         beta0_publish();
         __syncthreads();
         float kgv[4][4];
-        oor_next = prep_tiles(cr, kgv);
+        oor_next = prep_tiles(cr, kgv, false);
         st_kg(kgv);
     }
 
@@ -807,7 +833,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // while O and S update: the next chunk's operand tiles (its Kg waits for this MMA)
         float kgv[4][4];
-        if (ch + 1 < nchunks) oor_next = prep_tiles(cr, kgv);
+        if (ch + 1 < nchunks) {
+            if (warp > 0) scan_prefix();
+            oor_next = prep_tiles(cr, kgv, warp > 0);
+        }
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
         if (ch + 1 < nchunks) st_kg(kgv);  // the Kg tile has been read
