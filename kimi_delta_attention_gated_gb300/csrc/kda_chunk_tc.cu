@@ -173,21 +173,19 @@ __device__ __forceinline__ void blk16(float *dst, const float *X, const float *Y
         const float4 v = *reinterpret_cast<const float4 *>(X + r * AP + k);
         x[k] = v.x; x[k + 1] = v.y; x[k + 2] = v.z; x[k + 3] = v.w;
     }
-    float4 o = acc ? *reinterpret_cast<const float4 *>(dst + r * AP + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 o = acc ? *reinterpret_cast<const float4 *>(dst + r * AP + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);  // packed f32x2 accumulators
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const float4 y = *reinterpret_cast<const float4 *>(Y + k * AP + c4);
-        s.x = fmaf(x[k], y.x, s.x);
-        s.y = fmaf(x[k], y.y, s.y);
-        s.z = fmaf(x[k], y.z, s.z);
-        s.w = fmaf(x[k], y.w, s.w);
+        const float2 xk = make_float2(x[k], x[k]);
+        s01 = __ffma2_rn(xk, make_float2(y.x, y.y), s01);
+        s23 = __ffma2_rn(xk, make_float2(y.z, y.w), s23);
     }
-    o.x = fmaf(sign, s.x, o.x);
-    o.y = fmaf(sign, s.y, o.y);
-    o.z = fmaf(sign, s.z, o.z);
-    o.w = fmaf(sign, s.w, o.w);
-    *reinterpret_cast<float4 *>(dst + r * AP + c4) = o;
+    const float2 sg = make_float2(sign, sign);
+    const float2 o01 = __ffma2_rn(sg, s01, make_float2(o.x, o.y));
+    const float2 o23 = __ffma2_rn(sg, s23, make_float2(o.z, o.w));
+    *reinterpret_cast<float4 *>(dst + r * AP + c4) = make_float4(o01.x, o01.y, o23.x, o23.y);
 }
 
 // Off-diagonal 16 x 16 blocks of T = (I + A)^-1 from the diagonal inverses T_II:
@@ -498,36 +496,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 rq4 = *reinterpret_cast<const float4 *>(fs + F_RQ + warp * 4);
         const float4 rk4 = *reinterpret_cast<const float4 *>(fs + F_RK + warp * 4);
         const float rq[4] = {rq4.x, rq4.y, rq4.z, rq4.w}, rk[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
+        // channel pairs (0,1) and (2,3) in packed f32x2 arithmetic, each product in the
+        // same order as its scalar form
+        float2 o2[2] = {make_float2(o4[0], o4[1]), make_float2(o4[2], o4[3])};
+        const float2 eg2[2] = {make_float2(egam[0], egam[1]), make_float2(egam[2], egam[3])};
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = warp * 4 + r;
-            const float gr[4] = {c.g[r].x, c.g[r].y, c.g[r].z, c.g[r].w};
-            const float qv[4] = {bf16lo(c.q[r].x), bf16hi(c.q[r].x), bf16lo(c.q[r].y), bf16hi(c.q[r].y)};
-            const float kv[4] = {bf16lo(c.k[r].x), bf16hi(c.k[r].x), bf16lo(c.k[r].y), bf16hi(c.k[r].y)};
-            float kd[4], qd[4], km[4];
+            const float2 gr2[2] = {make_float2(c.g[r].x, c.g[r].y), make_float2(c.g[r].z, c.g[r].w)};
+            const float2 qv2[2] = {make_float2(bf16lo(c.q[r].x), bf16hi(c.q[r].x)),
+                                   make_float2(bf16lo(c.q[r].y), bf16hi(c.q[r].y))};
+            const float2 kv2[2] = {make_float2(bf16lo(c.k[r].x), bf16hi(c.k[r].x)),
+                                   make_float2(bf16lo(c.k[r].y), bf16hi(c.k[r].y))};
+            const float2 rk2 = make_float2(rk[r], rk[r]), nrk2 = make_float2(-rk[r], -rk[r]);
+            const float2 rq2 = make_float2(rq[r], rq[r]);
+            float2 kd[2], qd[2], km[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o4[e] += gr[e];  // inclusive cumulative decay G of token i
-                const float eG = __expf(o4[e]);
-                const float kh = kv[e] * rk[r];
-                kd[e] = -kh * eG;
-                qd[e] = qv[e] * rq[r] * eG;
-                km[e] = kh * __expf(-o4[e]);
-                kgv[r][e] = km[e] * egam[e];
+            for (int e = 0; e < 2; ++e) {
+                o2[e] = __fadd2_rn(o2[e], gr2[e]);  // inclusive cumulative decay G of token i
+                const float2 eG = make_float2(__expf(o2[e].x), __expf(o2[e].y));
+                const float2 em = make_float2(__expf(-o2[e].x), __expf(-o2[e].y));
+                kd[e] = __fmul2_rn(__fmul2_rn(kv2[e], nrk2), eG);  // -k^ exp(G)
+                qd[e] = __fmul2_rn(__fmul2_rn(qv2[e], rq2), eG);
+                km[e] = __fmul2_rn(__fmul2_rn(kv2[e], rk2), em);
+                const float2 kg = __fmul2_rn(km[e], eg2[e]);
+                kgv[r][2 * e] = kg.x;
+                kgv[r][2 * e + 1] = kg.y;
             }
             // rows i and 64 + i of the 128-row tiles share the swizzle phase, 8 KB apart
             const uint32_t off = sw128_off(i, l4, 128);
             uint32_t h0, l0, h1, l1;
-            split2(kd[0], kd[1], h0, l0);
-            split2(kd[2], kd[3], h1, l1);
+            split2(kd[0].x, kd[0].y, h0, l0);
+            split2(kd[1].x, kd[1].y, h1, l1);
             st_shared_v2(sb + S_KQH + off, h0, h1);
             st_shared_v2(sb + S_KQL + off, l0, l1);
-            split2(qd[0], qd[1], h0, l0);
-            split2(qd[2], qd[3], h1, l1);
+            split2(qd[0].x, qd[0].y, h0, l0);
+            split2(qd[1].x, qd[1].y, h1, l1);
             st_shared_v2(sb + S_KQH + off + 8192, h0, h1);
             st_shared_v2(sb + S_KQL + off + 8192, l0, l1);
-            split2(km[0], km[1], h0, l0);
-            split2(km[2], km[3], h1, l1);
+            split2(km[0].x, km[0].y, h0, l0);
+            split2(km[1].x, km[1].y, h1, l1);
             st_shared_v2(sb + S_KM + off, h0, h1);
             st_shared_v2(sb + S_KM + off + 8192, l0, l1);
         }
@@ -591,19 +599,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = m;
                 const float b = -fs[F_BETA + i];  // gram rows hold -Kd Km^T
                 float4 *dst = reinterpret_cast<float4 *>(Asm + i * AP + j0);
+                const float2 b2 = make_float2(b, b);
 #pragma unroll
                 for (int c = 0; c < 16; c += 4) {
                     float x[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        x[e] = (j0 + c + e < i) ? b * (__uint_as_float(r1[c + e]) + __uint_as_float(r2[c + e])) : 0.f;
+                    for (int e = 0; e < 4; e += 2) {
+                        const float2 v = __fmul2_rn(
+                            b2, __fadd2_rn(make_float2(__uint_as_float(r1[c + e]), __uint_as_float(r1[c + e + 1])),
+                                           make_float2(__uint_as_float(r2[c + e]), __uint_as_float(r2[c + e + 1]))));
+                        x[e] = (j0 + c + e < i) ? v.x : 0.f;
+                        x[e + 1] = (j0 + c + e + 1 < i) ? v.y : 0.f;
+                    }
                     dst[c / 4] = make_float4(x[0], x[1], x[2], x[3]);
                 }
             } else {
                 const int i = m - 64;
                 float x[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) x[c] = (j0 + c <= i) ? __uint_as_float(r1[c]) + __uint_as_float(r2[c]) : 0.f;
+                for (int c = 0; c < 16; c += 2) {
+                    const float2 v = __fadd2_rn(make_float2(__uint_as_float(r1[c]), __uint_as_float(r1[c + 1])),
+                                                make_float2(__uint_as_float(r2[c]), __uint_as_float(r2[c + 1])));
+                    x[c] = (j0 + c <= i) ? v.x : 0.f;
+                    x[c + 1] = (j0 + c + 1 <= i) ? v.y : 0.f;
+                }
                 st_tile8(sb + S_PKGH, sb + S_PKGL, 192, i, j0, x);
                 st_tile8(sb + S_PKGH, sb + S_PKGL, 192, i, j0 + 8, x + 8);
             }
@@ -801,14 +820,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 const float4 a = ge[c4], b = ge[4 + c4];
-                s1[4 * c4 + 0] = __float_as_uint(__uint_as_float(s1[4 * c4 + 0]) * a.x);
-                s1[4 * c4 + 1] = __float_as_uint(__uint_as_float(s1[4 * c4 + 1]) * a.y);
-                s1[4 * c4 + 2] = __float_as_uint(__uint_as_float(s1[4 * c4 + 2]) * a.z);
-                s1[4 * c4 + 3] = __float_as_uint(__uint_as_float(s1[4 * c4 + 3]) * a.w);
-                s2[4 * c4 + 0] = __float_as_uint(__uint_as_float(s2[4 * c4 + 0]) * b.x);
-                s2[4 * c4 + 1] = __float_as_uint(__uint_as_float(s2[4 * c4 + 1]) * b.y);
-                s2[4 * c4 + 2] = __float_as_uint(__uint_as_float(s2[4 * c4 + 2]) * b.z);
-                s2[4 * c4 + 3] = __float_as_uint(__uint_as_float(s2[4 * c4 + 3]) * b.w);
+                const float2 x0 = __fmul2_rn(make_float2(__uint_as_float(s1[4 * c4]), __uint_as_float(s1[4 * c4 + 1])),
+                                             make_float2(a.x, a.y));
+                const float2 x1 = __fmul2_rn(make_float2(__uint_as_float(s1[4 * c4 + 2]), __uint_as_float(s1[4 * c4 + 3])),
+                                             make_float2(a.z, a.w));
+                const float2 y0 = __fmul2_rn(make_float2(__uint_as_float(s2[4 * c4]), __uint_as_float(s2[4 * c4 + 1])),
+                                             make_float2(b.x, b.y));
+                const float2 y1 = __fmul2_rn(make_float2(__uint_as_float(s2[4 * c4 + 2]), __uint_as_float(s2[4 * c4 + 3])),
+                                             make_float2(b.z, b.w));
+                s1[4 * c4 + 0] = __float_as_uint(x0.x); s1[4 * c4 + 1] = __float_as_uint(x0.y);
+                s1[4 * c4 + 2] = __float_as_uint(x1.x); s1[4 * c4 + 3] = __float_as_uint(x1.y);
+                s2[4 * c4 + 0] = __float_as_uint(y0.x); s2[4 * c4 + 1] = __float_as_uint(y0.y);
+                s2[4 * c4 + 2] = __float_as_uint(y1.x); s2[4 * c4 + 3] = __float_as_uint(y1.y);
             }
             tmem_st16(tb + lane_off + T_S + c0, s1);
             tmem_st16(tb + lane_off + T_S + c0 + 16, s2);
