@@ -404,11 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GL && lane < 4) c.beta = warp * 4 + lane < cnn ? beta_of_logit(c.beta) : 0.f;
         float a[8];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float q0 = bf16lo(c.q[r].x), q1 = bf16hi(c.q[r].x), q2 = bf16lo(c.q[r].y), q3 = bf16hi(c.q[r].y);
-            const float k0 = bf16lo(c.k[r].x), k1 = bf16hi(c.k[r].x), k2 = bf16lo(c.k[r].y), k3 = bf16hi(c.k[r].y);
-            a[r] = fmaf(q0, q0, fmaf(q1, q1, fmaf(q2, q2, q3 * q3)));
-            a[4 + r] = fmaf(k0, k0, fmaf(k1, k1, fmaf(k2, k2, k3 * k3)));
+        for (int r = 0; r < 4; ++r) {  // (q, k) sums of squares as packed pairs
+            const float2 v0 = make_float2(bf16lo(c.q[r].x), bf16lo(c.k[r].x));
+            const float2 v1 = make_float2(bf16hi(c.q[r].x), bf16hi(c.k[r].x));
+            const float2 v2 = make_float2(bf16lo(c.q[r].y), bf16lo(c.k[r].y));
+            const float2 v3 = make_float2(bf16hi(c.q[r].y), bf16hi(c.k[r].y));
+            const float2 ss = __ffma2_rn(v0, v0, __ffma2_rn(v1, v1, __ffma2_rn(v2, v2, __fmul2_rn(v3, v3))));
+            a[r] = ss.x;
+            a[4 + r] = ss.y;
         }
         const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
         float b[4], d2[2];
@@ -430,11 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fs[F_RK + warp * 4 + v - 4] = sc;
         }
         if (lane < 4) fs[(!GL && warp == 0 ? F_BETA0 : F_BETA + warp * 4) + lane] = c.beta;
-        float4 t = c.g[0];
+        float2 t01 = make_float2(c.g[0].x, c.g[0].y), t23 = make_float2(c.g[0].z, c.g[0].w);
 #pragma unroll
         for (int r = 1; r < 4; ++r) {
-            t.x += c.g[r].x; t.y += c.g[r].y; t.z += c.g[r].z; t.w += c.g[r].w;
+            t01 = __fadd2_rn(t01, make_float2(c.g[r].x, c.g[r].y));
+            t23 = __fadd2_rn(t23, make_float2(c.g[r].z, c.g[r].w));
         }
+        const float4 t = make_float4(t01.x, t01.y, t23.x, t23.y);
         *reinterpret_cast<float4 *>(!GL && warp == 0 ? fs + F_SCAN0 + l4 : scan + warp * 128 + l4) = t;
     };
     // With g and beta given (!GL), warp 0 (which issues the tensor-core work) prepares its
@@ -751,7 +756,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = it >> 3, j0 = (it & 7) * 8;
                 float x[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) x[c] = (j0 + c <= i) ? Tsm[i * AP + j0 + c] * fs[F_BETA + j0 + c] : 0.f;
+                for (int c = 0; c < 8; c += 2) {
+                    const float2 v = __fmul2_rn(make_float2(Tsm[i * AP + j0 + c], Tsm[i * AP + j0 + c + 1]),
+                                                make_float2(fs[F_BETA + j0 + c], fs[F_BETA + j0 + c + 1]));
+                    x[c] = (j0 + c <= i) ? v.x : 0.f;
+                    x[c + 1] = (j0 + c + 1 <= i) ? v.y : 0.f;
+                }
                 st_tile8(sb + S_TBH, sb + S_TBL, 64, i, j0, x);
             }
             fence_async_smem();
