@@ -188,32 +188,30 @@ __device__ __forceinline__ void blk16(float *dst, const float *X, const float *Y
     *reinterpret_cast<float4 *>(dst + r * AP + c4) = make_float4(o01.x, o01.y, o23.x, o23.y);
 }
 
-// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 from the diagonal inverses T_II:
-//   T_IJ = -T_II X_IJ,  X_IJ = sum_{K=J}^{I-1} A_IK T_KJ        (I > J)
-// The partial sums that need only diagonal blocks are formed first, so every phase
-// is a batch of independent K = 16 products.  X_IJ lives in A's unused upper block (J, I).
+// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 from the diagonal inverses T_II.  Block
+// row I of (I + A) T = I gives, for I > J,
+//   T_IJ = -sum_{K=J}^{I-1} Y_IK T_KJ,   Y_IK = T_II A_IK,
+// so after one phase that forms every Y (kept in A's unused upper block (K, I)) the
+// blocks follow in three more phases of independent K = 16 products; the partial sums
+// of T_20, T_31 and T_30 accumulate in place.
 __device__ __forceinline__ void tri_offdiag(float *Asm, float *Tsm, int ctid) {
     auto A = [&](int i, int j) { return Asm + 16 * i * AP + 16 * j; };
     auto T = [&](int i, int j) { return Tsm + 16 * i * AP + 16 * j; };
-    auto X = [&](int i, int j) { return Asm + 16 * j * AP + 16 * i; };  // upper block (j, i) of A
+    auto Y = [&](int i, int j) { return Asm + 16 * j * AP + 16 * i; };  // upper block (j, i) of A
     const int p = ctid >> 6, t = ctid & 63;
-    if (p < 6) {  // X10, X21, X32 and the first terms of X20, X31, X30: (I, J) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-        const int I = p < 3 ? p + 1 : (p == 3 ? 2 : 3), J = p < 3 ? p : (p == 4 ? 1 : 0);
-        blk16(X(I, J), A(I, J), T(J, J), 1.f, false, t);
-    }
+    // (I, J) of the six blocks below the diagonal: (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+    const int I6 = p < 3 ? p + 1 : (p == 3 ? 2 : 3), J6 = p < 3 ? p : (p == 4 ? 1 : 0);
+    if (p < 6) blk16(Y(I6, J6), T(I6, I6), A(I6, J6), 1.f, false, t);  // every Y_IJ
     tbar();
-    if (p < 3) blk16(T(p + 1, p), T(p + 1, p + 1), X(p + 1, p), -1.f, false, t);  // T10, T21, T32
+    // T10, T21, T32 = -Y T_JJ; the first terms -Y20 T00, -Y31 T11, -Y30 T00 of T20, T31, T30
+    if (p < 6) blk16(T(I6, J6), Y(I6, J6), T(J6, J6), -1.f, false, t);
     tbar();
-    if (p < 3) {  // X20 += A21 T10, X31 += A32 T21, X30 += A31 T10: (I, J, K) = (2,0,1) (3,1,2) (3,0,1)
+    if (p < 3) {  // T20 -= Y21 T10, T31 -= Y32 T21, T30 -= Y31 T10: (I, J, K) = (2,0,1) (3,1,2) (3,0,1)
         const int I = p == 0 ? 2 : 3, J = p == 1 ? 1 : 0, K = p == 1 ? 2 : 1;
-        blk16(X(I, J), A(I, K), T(K, J), 1.f, true, t);
+        blk16(T(I, J), Y(I, K), T(K, J), -1.f, true, t);
     }
     tbar();
-    if (p < 2) blk16(T(p + 2, p), T(p + 2, p + 2), X(p + 2, p), -1.f, false, t);  // T20, T31
-    tbar();
-    if (p == 0) blk16(X(3, 0), A(3, 2), T(2, 0), 1.f, true, t);  // X30 += A32 T20
-    tbar();
-    if (p == 0) blk16(T(3, 0), T(3, 3), X(3, 0), -1.f, false, t);  // T30
+    if (p == 0) blk16(T(3, 0), Y(3, 2), T(2, 0), -1.f, true, t);  // T30 -= Y32 T20
     tbar();
 }
 
@@ -742,9 +740,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float x[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
+                    float a[16];
+#pragma unroll
+                    for (int j4 = 0; j4 < i; j4 += 4) {  // row i of the block, 16 B at a time
+                        const float4 v = *reinterpret_cast<const float4 *>(Asm + (o + i) * AP + o + j4);
+                        a[j4] = v.x; a[j4 + 1] = v.y; a[j4 + 2] = v.z; a[j4 + 3] = v.w;
+                    }
                     float acc = 0.f;
 #pragma unroll
-                    for (int j = 0; j < i; ++j) acc = fmaf(Asm[(o + i) * AP + o + j], x[j], acc);
+                    for (int j = 0; j < i; ++j) acc = fmaf(a[j], x[j], acc);
                     x[i] = (i < c) ? 0.f : (i == c ? 1.f : -acc);
                 }
 #pragma unroll
