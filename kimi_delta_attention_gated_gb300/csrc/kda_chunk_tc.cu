@@ -63,7 +63,6 @@ constexpr int C = 64;            // tokens per chunk
 constexpr int DK = 128;          // key dim
 constexpr int DV = 128;          // value dim
 constexpr int kThreads = 512;    // 16 warps = 4 warpgroups
-constexpr int kSolve = 480;      // warps 1-15 run the triangular solve
 constexpr float kRangeMax = 80.f;
 constexpr uint32_t kPolls = 1u << 26;  // bound on every mbarrier wait
 
@@ -298,6 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (i >= j0 && i < j0 + 8) w[(i - j0) >> 1] = (i & 1) ? 0x3F800000u : 0x00003F80u;
         st_shared_v4(sb + S_ID + sw128_off(i, j0, 64), w[0], w[1], w[2], w[3]);
+        // T diag(beta) tiles (hi and lo, 8 KB each): zero; each chunk rewrites only the
+        // blocks on or below the diagonal
+        st_shared_v4(sb + S_TBH + tid * 32, 0u, 0u, 0u, 0u);
+        st_shared_v4(sb + S_TBH + tid * 32 + 16, 0u, 0u, 0u, 0u);
     }
     fence_async_smem();
     fence_before_sync();
@@ -756,8 +759,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tbar();
             tri_offdiag(Asm, Tsm, ctid);
-            for (int it = ctid; it < 64 * 8; it += kSolve) {  // T diag(beta) -> hi/lo tile (rows i, K = j)
-                const int i = it >> 3, j0 = (it & 7) * 8;
+            {  // T diag(beta) -> hi/lo tile (rows i, K = j): only the 288 blocks of 8 columns on or
+               // below the diagonal (the rest stays zero from the setup), one per thread: the
+               // threads whose block lies above it take rows 60-63
+                int i = ctid >> 3, jb = ctid & 7;
+                if (jb == 7 && i < 32) {
+                    jb = i & 7;
+                    i = 60 + (i >> 3);
+                }
+                const int j0 = jb * 8;
+                if (j0 <= i) {
                 float x[8];
 #pragma unroll
                 for (int c = 0; c < 8; c += 2) {
@@ -767,6 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x[c + 1] = (j0 + c + 1 <= i) ? v.y : 0.f;
                 }
                 st_tile8(sb + S_TBH, sb + S_TBL, 64, i, j0, x);
+                }
             }
             fence_async_smem();
         }
