@@ -553,13 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- first chunk's preparation (later chunks are prepared inside the previous
     // chunk's tensor-core waits)
     int oor_next = 0;
+    float kgv[4][4];  // the next chunk's Kg (g and beta given: stored while that chunk's gram runs)
     if (nchunks > 0) {
         prep_norms(cr, min(C, len), 0);
         beta0_publish();
         __syncthreads();
-        float kgv[4][4];
         oor_next = prep_tiles(cr, kgv, false);
-        st_kg(kgv);
+        if (GL) st_kg(kgv);
     }
 
     for (int ch = 0; ch < nchunks; ++ch) {
@@ -592,6 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar_g);  // an empty commit on fallback chunks
         }
         __syncwarp();
+        // g and beta given: this chunk's Kg^T tile (the previous O/S product has read the old
+        // one; the gram does not read it).  With logits every warp loads here and warp 0
+        // would arrive late, so the tile is stored after the previous O/S product instead.
+        if (!GL) {
+            st_kg(kgv);
+            fence_async_smem();
+        }
         // warps 1-15 (every warp with logits) start loading the next chunk while waiting for the gram
         if ((GL || warp > 0) && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
         if (!wait_group(bar_g, par)) failed = 1;
@@ -881,14 +888,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // while O and S update: the next chunk's operand tiles (its Kg waits for this MMA)
-        float kgv[4][4];
         if (ch + 1 < nchunks) {
             if (warp > 0) scan_prefix();
             oor_next = prep_tiles(cr, kgv, warp > 0);
         }
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
-        if (ch + 1 < nchunks) st_kg(kgv);  // the Kg tile has been read
+        if (GL && ch + 1 < nchunks) st_kg(kgv);  // the Kg tile has been read
         {
             uint32_t r[16];
             const int c0 = wg * 32;
