@@ -157,6 +157,16 @@ __device__ __forceinline__ void st_kgt(uint32_t sb, int c, int j0, const float (
     }
 }
 
+// SWIZZLE_128B shared-memory descriptor (the same fields as sdesc) of the operand at byte
+// offset off from the 1024-aligned shared base whose address / 16 is sb16: the address
+// field is sb16 + off / 16 (below 2^14, shared addresses being below 2^18 bytes), so with
+// compile-time off, lbo and sbo the whole descriptor is one add and a constant high word.
+__device__ __forceinline__ uint64_t sdesc_at(uint32_t sb16, uint32_t off, uint32_t lbo, uint32_t sbo) {
+    const uint32_t lo = (sb16 + (off >> 4)) | ((lbo >> 4) << 16);
+    const uint32_t hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+    return ((uint64_t)hi << 32) | lo;
+}
+
 // hi*hi, hi*lo, lo*hi: (A part, B part) of the three products of a split operand pair
 __device__ __forceinline__ int combo_a(int cb) { return cb == 2 ? 1 : 0; }
 __device__ __forceinline__ int combo_b(int cb) { return cb == 1 ? 1 : 0; }
@@ -253,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
+    const uint32_t sb16 = sb >> 4;
     float *fs = reinterpret_cast<float *>(sm + S_SMALL);
     float *Asm = reinterpret_cast<float *>(sm + S_A);
     float *Tsm = reinterpret_cast<float *>(sm + S_T);
@@ -308,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after_sync();
     const uint32_t tb = *tmem_slot;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+
 
     auto issue_v = [&](int chunk) {
         mbar_arrive_expect_tx(tma_bar, 16384);
@@ -580,13 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s) {  // [-Kd;Qd]_hi x [Km_hi;Km_lo]^T
                     const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_ss(tb + T_G, sdesc(sb + S_KQH + koff, 16, 1024), sdesc(sb + S_KM + koff, 16, 1024), id128,
+                    mma_ss(tb + T_G, sdesc_at(sb16, S_KQH + koff, 16, 1024), sdesc_at(sb16, S_KM + koff, 16, 1024), id128,
                            s ? 1u : 0u);
                 }
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s) {  // [-Kd;Qd]_lo x Km_hi^T into the first half
                     const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_ss(tb + T_G, sdesc(sb + S_KQL + koff, 16, 1024), sdesc(sb + S_KM + koff, 16, 1024), id64, 1u);
+                    mma_ss(tb + T_G, sdesc_at(sb16, S_KQL + koff, 16, 1024), sdesc_at(sb16, S_KM + koff, 16, 1024), id64, 1u);
                 }
             }
             mma_commit(bar_g);  // an empty commit on fallback chunks
@@ -730,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_mn = idesc_bf16(128, 64, true, false);
 #pragma unroll 1
             for (int s = 0; s < 4; ++s)
-                mma_ss(tb + T_R, sdesc(sb + S_V + s * 2048, 8192, 1024), sdesc(sb + S_ID + s * 32, 16, 1024), id_mn,
+                mma_ss(tb + T_R, sdesc_at(sb16, S_V + s * 2048, 8192, 1024), sdesc_at(sb16, S_ID + s * 32, 16, 1024), id_mn,
                        s ? 1u : 0u);
             const uint32_t id128 = idesc_bf16(128, 128, false, false);
 #pragma unroll
@@ -738,8 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t a = tb + (combo_a(cb) ? T_SL : T_SH) + s * 8;
-                    const uint32_t bk = (combo_b(cb) ? sb + S_KQL : sb + S_KQH) + (s >> 2) * 16384 + (s & 3) * 32;
-                    mma_ts(tb + T_R, a, sdesc(bk, 16, 1024), id128, 1u);
+                    const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_ts(tb + T_R, a, sdesc_at(sb16, (combo_b(cb) ? S_KQL : S_KQH) + koff, 16, 1024), id128, 1u);
                 }
             mma_commit(bar_r);
         } else if (warp > 0) {
@@ -818,13 +830,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             fence_after_sync();
             const uint32_t id64 = idesc_bf16(128, 64, false, false);
-#pragma unroll 1
+#pragma unroll
             for (int cb = 0; cb < 3; ++cb)
 #pragma unroll 1
                 for (int s = 0; s < 4; ++s)
                     mma_ts(tb + T_D, tb + (combo_a(cb) ? T_RL : T_RH) + s * 8,
-                           sdesc((combo_b(cb) ? sb + S_TBL : sb + S_TBH) + s * 32, 16, 1024), id64,
-                           (cb | s) ? 1u : 0u);
+                           sdesc_at(sb16, (combo_b(cb) ? S_TBL : S_TBH) + s * 32, 16, 1024), id64, (cb | s) ? 1u : 0u);
             mma_commit(bar_d);
         }
         __syncwarp();
@@ -878,12 +889,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             fence_after_sync();
             const uint32_t id192 = idesc_bf16(128, 192, false, false);
-#pragma unroll 1
+#pragma unroll
             for (int cb = 0; cb < 3; ++cb)
 #pragma unroll 1
                 for (int s = 0; s < 4; ++s)
                     mma_ts(tb + T_O, tb + (combo_a(cb) ? T_DL : T_DH) + s * 8,
-                           sdesc((combo_b(cb) ? sb + S_PKGL : sb + S_PKGH) + s * 32, 16, 1024), id192, 1u);
+                           sdesc_at(sb16, (combo_b(cb) ? S_PKGL : S_PKGH) + s * 32, 16, 1024), id192, 1u);
             mma_commit(bar_s);
         }
         __syncwarp();
