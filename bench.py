@@ -40,10 +40,10 @@ PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits b
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture: (252.93 + 77.44 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # B=1 T=2048 H=96 capture: (252.79 + 77.79 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                "sha256": "0228db496d7380027aa7af68b8465210f73345f902d06d8ce48ab381cf044f56",
-                "bytes_per_unit": (252.925184e6 + 77.439232e6 - 6.291456e6) / (2048 * 96),
+                "sha256": "0fccd070f8eb85530e65c30c9bd47fb8aa82ab3f500d1cd652d49f45a4d28431",
+                "bytes_per_unit": (252.794368e6 + 77.790976e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # B=64 capture: mean of two launches, 755.2 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
