@@ -21,6 +21,7 @@
 #include <math.h>
 
 #include "kda_internal.cuh"
+#include "kda_tc_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -215,10 +216,237 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Decode step (one token per sequence, dense batch, K = V = 128).  The same arithmetic
+// and thread mapping as recurrent_kernel, but persistent: two CTAs per SM walk the
+// (sequence, head) units with the grid as stride.  While one unit is computed from
+// registers, the next unit's 64 KiB state and its q, k, v, g and gate rows are already
+// on their way into shared memory (bulk copies on an mbarrier), so each SM keeps about
+// 128 KiB of reads in flight instead of stalling at every CTA's start.
+
+constexpr int kDK = 128;                                  // K = V
+constexpr uint32_t D_STATE = 0;                           // [128][128] fp32
+constexpr uint32_t D_Q = 65536, D_K = D_Q + 512, D_V = D_K + 512, D_G = D_V + 512, D_GATE = D_G + 512;
+constexpr uint32_t D_ARR = D_GATE + 512;                  // sq, sk, se, sv, sd: [128] floats each
+constexpr uint32_t D_RED = D_ARR + 5 * 512;               // red_u, red_q: [8][128] floats each
+constexpr uint32_t D_MISC = D_RED + 2 * 8 * 512;          // [8][4] floats
+constexpr uint32_t D_BAR = D_MISC + 128;
+constexpr uint32_t D_SMEM = D_BAR + 16;
+constexpr uint32_t kDecodePolls = 1u << 26;
+
+// Set by a CTA whose bounded wait on its copies gave up; that unit's state becomes NaN.
+__device__ int g_decode_timeouts = 0;
+
+__device__ __forceinline__ float in_elem(const uint8_t *base, int i, int is_bf16) {
+    return is_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i])
+                   : reinterpret_cast<const float *>(base)[i];
+}
+
+template <bool GL>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    constexpr int RPW = kDK / kWarps, VPL = kDK / 32;
+    const uint32_t sb = tc::smem_u32(dsm);
+    float *sq = reinterpret_cast<float *>(dsm + D_ARR), *sk = sq + kDK, *se = sk + kDK, *sv = se + kDK,
+          *sd = sv + kDK;
+    float(*red_u)[kDK] = reinterpret_cast<float(*)[kDK]>(dsm + D_RED);
+    float(*red_q)[kDK] = reinterpret_cast<float(*)[kDK]>(dsm + D_RED + 8 * 512);
+    float(*misc)[4] = reinterpret_cast<float(*)[4]>(dsm + D_MISC);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(dsm + D_BAR);
+
+    const int H = p.H, units = p.N * p.H, stride = gridDim.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t eq = p.qkv_bf16 ? 2 : 4;
+    const void *gsrc = GL ? p.g_logits : static_cast<const void *>(p.g);
+    const uint32_t eg = GL && p.g_logits_bf16 ? 2 : 4, eo = p.gate_bf16 ? 2 : 4;
+    const uint32_t tx = (p.s0 ? 65536u : 0u) + 3u * kDK * eq + kDK * eg + (p.gate ? kDK * eo : 0u);
+    auto issue = [&](int u) {  // thread 0: every copy of unit u
+        tc::mbar_arrive_expect_tx(bar, tx);
+        if (p.s0) tc::bulk_load(sb + D_STATE, p.s0 + (size_t)u * kDK * kDK, 65536u, bar);
+        tc::bulk_load(sb + D_Q, static_cast<const uint8_t *>(p.q) + (size_t)u * kDK * eq, kDK * eq, bar);
+        tc::bulk_load(sb + D_K, static_cast<const uint8_t *>(p.k) + (size_t)u * kDK * eq, kDK * eq, bar);
+        tc::bulk_load(sb + D_V, static_cast<const uint8_t *>(p.v) + (size_t)u * kDK * eq, kDK * eq, bar);
+        tc::bulk_load(sb + D_G, static_cast<const uint8_t *>(gsrc) + (size_t)u * kDK * eg, kDK * eg, bar);
+        if (p.gate)
+            tc::bulk_load(sb + D_GATE, static_cast<const uint8_t *>(p.gate) + (size_t)u * kDK * eo, kDK * eo, bar);
+    };
+    // beta (or its logit) and, with logits, the head's exp(A_log) and dt_bias of this
+    // thread's channel: loaded one unit ahead, into registers
+    auto pre_beta = [&](int u) {
+        if (u >= units) return 0.f;
+        return GL ? ld_in(p.beta_logits, (size_t)u, p.beta_logits_bf16) : __ldg(p.beta + u);
+    };
+    auto pre_alog = [&](int u) { return GL && u < units ? __ldg(p.A_log + u % H) : 0.f; };
+    auto pre_db = [&](int u) {
+        return GL && u < units && p.dt_bias && tid < kDK ? __ldg(p.dt_bias + (size_t)(u % H) * kDK + tid) : 0.f;
+    };
+
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    int u = blockIdx.x;
+    if (tid == 0 && u < units) issue(u);
+    const float nw = p.gate && tid < kDK ? p.norm_w[tid] : 0.f;
+    float b_cur = pre_beta(u), al_cur = pre_alog(u), db_cur = pre_db(u);
+    int pend_it = u < units ? 0 : -1;  // loop iteration whose copies are in flight
+
+    for (int it = 0; u < units; u += stride, ++it) {
+        const int failed = __syncthreads_or(!tc::mbar_wait(bar, (uint32_t)(it & 1), kDecodePolls));
+        if (failed) {  // the copies never arrived: poison this unit's state and stop
+            if (tid == 0) atomicAdd(&g_decode_timeouts, 1);
+            for (int e = tid; e < kDK * kDK; e += kThreads) p.sT[(size_t)u * kDK * kDK + e] = __int_as_float(0x7fc00000);
+            break;
+        }
+        pend_it = -1;
+        float s[RPW][VPL];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            if (p.s0) {
+                const float4 t = *reinterpret_cast<const float4 *>(dsm + D_STATE + ((warp * RPW + r) * kDK + lane * VPL) * 4);
+                s[r][0] = t.x; s[r][1] = t.y; s[r][2] = t.z; s[r][3] = t.w;
+            } else {
+#pragma unroll
+                for (int c = 0; c < VPL; ++c) s[r][c] = 0.f;
+            }
+        }
+        // -- prologue from the staged rows: q, k, exp(g), v, the gate; partial norms
+        float pq = 0.f, pk = 0.f, pqk = 0.f, gt = 0.f;
+        if (tid < kDK) {
+            const float qv = in_elem(dsm + D_Q, tid, p.qkv_bf16), kv = in_elem(dsm + D_K, tid, p.qkv_bf16);
+            const float z = in_elem(dsm + D_G, tid, GL ? p.g_logits_bf16 : 0);
+            sq[tid] = qv;
+            sk[tid] = kv;
+            se[tid] = __expf(GL ? gate_of_logit(z + db_cur, __expf(al_cur), p.g_lower) : z);
+            pq = qv * qv;
+            pk = kv * kv;
+            pqk = qv * kv;
+            if (p.gate) gt = in_elem(dsm + D_GATE, tid, p.gate_bf16);
+        }
+        if (tid >= kThreads - kDK) sv[tid - (kThreads - kDK)] = in_elem(dsm + D_V, tid - (kThreads - kDK), p.qkv_bf16);
+        pq = warp_sum(pq);
+        pk = warp_sum(pk);
+        pqk = warp_sum(pqk);
+        if (lane == 0) {
+            misc[warp][0] = pq;
+            misc[warp][1] = pk;
+            misc[warp][2] = pqk;
+        }
+        tc::fence_async_smem();  // these reads of the buffers come before the next copies into them
+        __syncthreads();         // the staged rows are consumed: the next unit's copies may start
+        const int un = u + stride;
+        if (un < units) {
+            if (tid == 0) issue(un);
+            pend_it = it + 1;
+        }
+        const float b_next = pre_beta(un), al_next = pre_alog(un), db_next = pre_db(un);
+        float ssq = 0.f, ssk = 0.f, sqk = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDK / 32; ++w) {
+            ssq += misc[w][0];
+            ssk += misc[w][1];
+            sqk += misc[w][2];
+        }
+        const float rq = p.l2norm ? rsqrtf(ssq + 1e-6f) : 1.f;
+        const float rk = p.l2norm ? rsqrtf(ssk + 1e-6f) : 1.f;
+        const float kq = sqk * rq * rk;  // k^ . q^
+
+        // -- decay rows, partial u = S'^T k^ and p = S'^T q^
+        float pu[VPL], pp[VPL];
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) pu[c] = pp[c] = 0.f;
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const int i = warp * RPW + r;
+            const float e = se[i], ki = sk[i] * rk, qi = sq[i] * rq;
+#pragma unroll
+            for (int c = 0; c < VPL; ++c) {
+                s[r][c] *= e;
+                pu[c] = fmaf(ki, s[r][c], pu[c]);
+                pp[c] = fmaf(qi, s[r][c], pp[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) {
+            red_u[warp][lane * VPL + c] = pu[c];
+            red_q[warp][lane * VPL + c] = pp[c];
+        }
+        __syncthreads();
+
+        // -- delta and output, one thread per value column
+        const size_t hv = (size_t)u * kDK;
+        float ov = 0.f;
+        if (tid < kDK) {
+            float uu = 0.f, pv = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                uu += red_u[w][tid];
+                pv += red_q[w][tid];
+            }
+            const float b = GL ? beta_of_logit(b_cur) : b_cur;
+            const float d = b * (sv[tid] - uu);
+            sd[tid] = d;
+            ov = p.scale * fmaf(kq, d, pv);
+            if (p.o) st_out(p.o, hv + tid, ov, p.o_bf16);
+        }
+        if (p.gate) {
+            const float sq2 = warp_sum(tid < kDK ? ov * ov : 0.f);
+            if (lane == 0) misc[warp][3] = sq2;
+        }
+        __syncthreads();
+        if (p.gate && tid < kDK) {
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDK / 32; ++w) ss += misc[w][3];
+            const float inv = rsqrtf(ss / (float)kDK + p.eps);
+            st_out(p.y, hv + tid, ov * inv * nw * sigmoidf_(gt), p.o_bf16);
+        }
+
+        // -- rank-one write, straight from registers to the state output
+        float dl[VPL];
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) dl[c] = sd[lane * VPL + c];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float ki = sk[warp * RPW + r] * rk;
+#pragma unroll
+            for (int c = 0; c < VPL; ++c) s[r][c] = fmaf(ki, dl[c], s[r][c]);
+            st_row<VPL>(p.sT + (size_t)u * kDK * kDK + (size_t)(warp * RPW + r) * kDK + lane * VPL, s[r]);
+        }
+        b_cur = b_next;
+        al_cur = al_next;
+        db_cur = db_next;
+        __syncthreads();  // shared arrays are rewritten by the next unit
+    }
+    // after a failure: give the copies still in flight their bounded time before exiting
+    if (tid == 0 && pend_it >= 0) tc::mbar_wait(bar, (uint32_t)(pend_it & 1), kDecodePolls);
+}
+
 template <int K, int V>
 kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return KDA_OK;
+    if (K == kDK && V == kDK && p.T == 1 && !p.cu_seqlens && !p.states && p.sT) {
+        static bool configured = false;
+        if (!configured) {
+            for (void *fn : {(void *)decode_kernel<false>, (void *)decode_kernel<true>}) {
+                const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM);
+                if (e != cudaSuccess) {
+                    set_error("decode: cannot reserve %u bytes of shared memory: %s", D_SMEM, cudaGetErrorString(e));
+                    return KDA_ERR_CUDA;
+                }
+            }
+            configured = true;
+        }
+        const int grid = units < 2 * sm_count() ? units : 2 * sm_count();
+        if (p.g_logits)
+            decode_kernel<true><<<grid, kThreads, D_SMEM, st>>>(p);
+        else
+            decode_kernel<false><<<grid, kThreads, D_SMEM, st>>>(p);
+        note_launch();
+        return check_launch("decode_kernel");
+    }
     if (p.g_logits)
         recurrent_kernel<K, V, true><<<units, kThreads, 0, st>>>(p);
     else

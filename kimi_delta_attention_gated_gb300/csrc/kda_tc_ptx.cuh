@@ -226,6 +226,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (a multiple of 16; both addresses 16-byte
+// aligned) from global into shared memory, completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // TMA: 2-D tiled load into shared memory, completion counted on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint64_t *bar, int x, int y) {
     asm volatile(
