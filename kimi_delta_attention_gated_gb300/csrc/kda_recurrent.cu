@@ -224,15 +224,20 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
 // on their way into shared memory (bulk copies on an mbarrier), so each SM keeps about
 // 128 KiB of reads in flight instead of stalling at every CTA's start.
 
-constexpr int kDK = 128;                                  // K = V
-constexpr uint32_t D_STATE = 0;                           // [128][128] fp32
-constexpr uint32_t D_Q = 65536, D_K = D_Q + 512, D_V = D_K + 512, D_G = D_V + 512, D_GATE = D_G + 512;
-constexpr uint32_t D_ARR = D_GATE + 512;                  // sq, sk, se, sv, sd: [128] floats each
-constexpr uint32_t D_RED = D_ARR + 5 * 512;               // red_u, red_q: [8][128] floats each
-constexpr uint32_t D_MISC = D_RED + 2 * 8 * 512;          // [8][4] floats
-constexpr uint32_t D_BAR = D_MISC + 128;
-constexpr uint32_t D_SMEM = D_BAR + 16;
+constexpr int kDK = 128;                 // K = V
+constexpr uint32_t kStage = 65536 + 5 * 512;  // one unit: state [128][128] fp32, then q, k, v, g, gate rows
+constexpr uint32_t S_Q = 65536, S_K = S_Q + 512, S_V = S_K + 512, S_G = S_V + 512, S_GATE = S_G + 512;
 constexpr uint32_t kDecodePolls = 1u << 26;
+
+// Shared-memory layout of the decode kernel with NW warps and NS staging buffers.
+template <int NW, int NS>
+struct DecodeSmem {
+    static constexpr uint32_t arr = NS * kStage;               // sq, sk, se, sv, sd: [128] floats each
+    static constexpr uint32_t red = arr + 5 * 512;             // red_u, red_q: [NW][128] floats each
+    static constexpr uint32_t misc = red + 2 * NW * 512;       // [NW][4] floats
+    static constexpr uint32_t bar = misc + NW * 16;            // NS mbarriers
+    static constexpr uint32_t bytes = bar + NS * 8;
+};
 
 // Set by a CTA whose bounded wait on its copies gave up; that unit's state becomes NaN.
 __device__ int g_decode_timeouts = 0;
@@ -242,17 +247,21 @@ __device__ __forceinline__ float in_elem(const uint8_t *base, int i, int is_bf16
                    : reinterpret_cast<const float *>(base)[i];
 }
 
-template <bool GL>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) {
+// NW warps (warp w owns rows [w * 128 / NW, (w + 1) * 128 / NW) of the state, lane l the
+// columns 4l .. 4l+3) and NS staging buffers: the copies of the NS units after the one
+// being computed are in flight.
+template <bool GL, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const SeqParams p) {
+    using L = DecodeSmem<NW, NS>;
+    constexpr int NT = NW * 32, RPW = kDK / NW, VPL = kDK / 32;
     extern __shared__ __align__(1024) uint8_t dsm[];
-    constexpr int RPW = kDK / kWarps, VPL = kDK / 32;
     const uint32_t sb = tc::smem_u32(dsm);
-    float *sq = reinterpret_cast<float *>(dsm + D_ARR), *sk = sq + kDK, *se = sk + kDK, *sv = se + kDK,
+    float *sq = reinterpret_cast<float *>(dsm + L::arr), *sk = sq + kDK, *se = sk + kDK, *sv = se + kDK,
           *sd = sv + kDK;
-    float(*red_u)[kDK] = reinterpret_cast<float(*)[kDK]>(dsm + D_RED);
-    float(*red_q)[kDK] = reinterpret_cast<float(*)[kDK]>(dsm + D_RED + 8 * 512);
-    float(*misc)[4] = reinterpret_cast<float(*)[4]>(dsm + D_MISC);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(dsm + D_BAR);
+    float(*red_u)[kDK] = reinterpret_cast<float(*)[kDK]>(dsm + L::red);
+    float(*red_q)[kDK] = reinterpret_cast<float(*)[kDK]>(dsm + L::red + NW * 512);
+    float(*misc)[4] = reinterpret_cast<float(*)[4]>(dsm + L::misc);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(dsm + L::bar);
 
     const int H = p.H, units = p.N * p.H, stride = gridDim.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -260,18 +269,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) 
     const void *gsrc = GL ? p.g_logits : static_cast<const void *>(p.g);
     const uint32_t eg = GL && p.g_logits_bf16 ? 2 : 4, eo = p.gate_bf16 ? 2 : 4;
     const uint32_t tx = (p.s0 ? 65536u : 0u) + 3u * kDK * eq + kDK * eg + (p.gate ? kDK * eo : 0u);
-    auto issue = [&](int u) {  // thread 0: every copy of unit u
+    auto issue = [&](int u, int st) {  // thread 0: every copy of unit u into buffer st
+        uint64_t *bar = bars + st;
+        const uint32_t d = sb + (uint32_t)st * kStage;
         tc::mbar_arrive_expect_tx(bar, tx);
-        if (p.s0) tc::bulk_load(sb + D_STATE, p.s0 + (size_t)u * kDK * kDK, 65536u, bar);
-        tc::bulk_load(sb + D_Q, static_cast<const uint8_t *>(p.q) + (size_t)u * kDK * eq, kDK * eq, bar);
-        tc::bulk_load(sb + D_K, static_cast<const uint8_t *>(p.k) + (size_t)u * kDK * eq, kDK * eq, bar);
-        tc::bulk_load(sb + D_V, static_cast<const uint8_t *>(p.v) + (size_t)u * kDK * eq, kDK * eq, bar);
-        tc::bulk_load(sb + D_G, static_cast<const uint8_t *>(gsrc) + (size_t)u * kDK * eg, kDK * eg, bar);
+        if (p.s0) tc::bulk_load(d, p.s0 + (size_t)u * kDK * kDK, 65536u, bar);
+        tc::bulk_load(d + S_Q, static_cast<const uint8_t *>(p.q) + (size_t)u * kDK * eq, kDK * eq, bar);
+        tc::bulk_load(d + S_K, static_cast<const uint8_t *>(p.k) + (size_t)u * kDK * eq, kDK * eq, bar);
+        tc::bulk_load(d + S_V, static_cast<const uint8_t *>(p.v) + (size_t)u * kDK * eq, kDK * eq, bar);
+        tc::bulk_load(d + S_G, static_cast<const uint8_t *>(gsrc) + (size_t)u * kDK * eg, kDK * eg, bar);
         if (p.gate)
-            tc::bulk_load(sb + D_GATE, static_cast<const uint8_t *>(p.gate) + (size_t)u * kDK * eo, kDK * eo, bar);
+            tc::bulk_load(d + S_GATE, static_cast<const uint8_t *>(p.gate) + (size_t)u * kDK * eo, kDK * eo, bar);
     };
-    // beta (or its logit) and, with logits, the head's exp(A_log) and dt_bias of this
-    // thread's channel: loaded one unit ahead, into registers
+    // beta (or its logit) and, with logits, the head's A_log and this thread's dt_bias:
+    // loaded one unit ahead, into registers
     auto pre_beta = [&](int u) {
         if (u >= units) return 0.f;
         return GL ? ld_in(p.beta_logits, (size_t)u, p.beta_logits_bf16) : __ldg(p.beta + u);
@@ -282,29 +293,32 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) 
     };
 
     if (tid == 0) {
-        tc::mbar_init(bar, 1);
+        for (int st = 0; st < NS; ++st) tc::mbar_init(bars + st, 1);
         tc::fence_mbar_init();
     }
     __syncthreads();
     int u = blockIdx.x;
-    if (tid == 0 && u < units) issue(u);
+    if (tid == 0)
+        for (int st = 0; st < NS; ++st)
+            if (u + st * stride < units) issue(u + st * stride, st);
     const float nw = p.gate && tid < kDK ? p.norm_w[tid] : 0.f;
     float b_cur = pre_beta(u), al_cur = pre_alog(u), db_cur = pre_db(u);
-    int pend_it = u < units ? 0 : -1;  // loop iteration whose copies are in flight
-
-    for (int it = 0; u < units; u += stride, ++it) {
-        const int failed = __syncthreads_or(!tc::mbar_wait(bar, (uint32_t)(it & 1), kDecodePolls));
+    int it = 0;
+    bool failed = false;
+    for (; u < units; u += stride, ++it) {
+        const int st = it % NS;
+        const uint8_t *buf = dsm + (uint32_t)st * kStage;
+        failed = __syncthreads_or(!tc::mbar_wait(bars + st, (uint32_t)((it / NS) & 1), kDecodePolls));
         if (failed) {  // the copies never arrived: poison this unit's state and stop
             if (tid == 0) atomicAdd(&g_decode_timeouts, 1);
-            for (int e = tid; e < kDK * kDK; e += kThreads) p.sT[(size_t)u * kDK * kDK + e] = __int_as_float(0x7fc00000);
+            for (int e = tid; e < kDK * kDK; e += NT) p.sT[(size_t)u * kDK * kDK + e] = __int_as_float(0x7fc00000);
             break;
         }
-        pend_it = -1;
         float s[RPW][VPL];
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             if (p.s0) {
-                const float4 t = *reinterpret_cast<const float4 *>(dsm + D_STATE + ((warp * RPW + r) * kDK + lane * VPL) * 4);
+                const float4 t = *reinterpret_cast<const float4 *>(buf + ((warp * RPW + r) * kDK + lane * VPL) * 4);
                 s[r][0] = t.x; s[r][1] = t.y; s[r][2] = t.z; s[r][3] = t.w;
             } else {
 #pragma unroll
@@ -314,17 +328,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) 
         // -- prologue from the staged rows: q, k, exp(g), v, the gate; partial norms
         float pq = 0.f, pk = 0.f, pqk = 0.f, gt = 0.f;
         if (tid < kDK) {
-            const float qv = in_elem(dsm + D_Q, tid, p.qkv_bf16), kv = in_elem(dsm + D_K, tid, p.qkv_bf16);
-            const float z = in_elem(dsm + D_G, tid, GL ? p.g_logits_bf16 : 0);
+            const float qv = in_elem(buf + S_Q, tid, p.qkv_bf16), kv = in_elem(buf + S_K, tid, p.qkv_bf16);
+            const float z = in_elem(buf + S_G, tid, GL ? p.g_logits_bf16 : 0);
             sq[tid] = qv;
             sk[tid] = kv;
             se[tid] = __expf(GL ? gate_of_logit(z + db_cur, __expf(al_cur), p.g_lower) : z);
             pq = qv * qv;
             pk = kv * kv;
             pqk = qv * kv;
-            if (p.gate) gt = in_elem(dsm + D_GATE, tid, p.gate_bf16);
+            if (p.gate) gt = in_elem(buf + S_GATE, tid, p.gate_bf16);
         }
-        if (tid >= kThreads - kDK) sv[tid - (kThreads - kDK)] = in_elem(dsm + D_V, tid - (kThreads - kDK), p.qkv_bf16);
+        if (tid >= NT - kDK) sv[tid - (NT - kDK)] = in_elem(buf + S_V, tid - (NT - kDK), p.qkv_bf16);
         pq = warp_sum(pq);
         pk = warp_sum(pk);
         pqk = warp_sum(pqk);
@@ -333,13 +347,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) 
             misc[warp][1] = pk;
             misc[warp][2] = pqk;
         }
-        tc::fence_async_smem();  // these reads of the buffers come before the next copies into them
-        __syncthreads();         // the staged rows are consumed: the next unit's copies may start
+        tc::fence_async_smem();  // these reads of the buffer come before the next copies into it
+        __syncthreads();         // the staged rows are consumed: the buffer takes unit u + NS * stride
+        if (tid == 0 && u + NS * stride < units) issue(u + NS * stride, st);
         const int un = u + stride;
-        if (un < units) {
-            if (tid == 0) issue(un);
-            pend_it = it + 1;
-        }
         const float b_next = pre_beta(un), al_next = pre_alog(un), db_next = pre_db(un);
         float ssq = 0.f, ssk = 0.f, sqk = 0.f;
 #pragma unroll
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) 
         if (tid < kDK) {
             float uu = 0.f, pv = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 uu += red_u[w][tid];
                 pv += red_q[w][tid];
             }
@@ -419,31 +430,44 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const SeqParams p) 
         db_cur = db_next;
         __syncthreads();  // shared arrays are rewritten by the next unit
     }
-    // after a failure: give the copies still in flight their bounded time before exiting
-    if (tid == 0 && pend_it >= 0) tc::mbar_wait(bar, (uint32_t)(pend_it & 1), kDecodePolls);
+    // after a failure: give the copies still in flight (iterations it .. it + NS - 1) their
+    // bounded time before exiting
+    if (failed && tid == 0)
+        for (int k = 0; k < NS; ++k) {
+            const int j = it + k, uj = blockIdx.x + j * stride;
+            if (uj < units) tc::mbar_wait(bars + j % NS, (uint32_t)((j / NS) & 1), kDecodePolls);
+        }
 }
+
+// Decode configuration: NW warps per CTA, NS staging buffers (CTAs per SM follow from
+// the registers and shared memory: 2 for 8 warps and one buffer, 1 for 16 warps and 2
+// or 3).  Measured at B = 256: 8 warps / 1 buffer 0.515 ms, 16 / 2 0.527 ms, 16 / 3
+// 0.530 ms.
+constexpr int kDecNW = 8, kDecNS = 1;
 
 template <int K, int V>
 kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return KDA_OK;
     if (K == kDK && V == kDK && p.T == 1 && !p.cu_seqlens && !p.states && p.sT) {
+        using L = DecodeSmem<kDecNW, kDecNS>;
         static bool configured = false;
         if (!configured) {
-            for (void *fn : {(void *)decode_kernel<false>, (void *)decode_kernel<true>}) {
-                const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM);
+            for (void *fn : {(void *)decode_kernel<false, kDecNW, kDecNS>, (void *)decode_kernel<true, kDecNW, kDecNS>}) {
+                const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::bytes);
                 if (e != cudaSuccess) {
-                    set_error("decode: cannot reserve %u bytes of shared memory: %s", D_SMEM, cudaGetErrorString(e));
+                    set_error("decode: cannot reserve %u bytes of shared memory: %s", L::bytes, cudaGetErrorString(e));
                     return KDA_ERR_CUDA;
                 }
             }
             configured = true;
         }
-        const int grid = units < 2 * sm_count() ? units : 2 * sm_count();
+        const int per_sm = kDecNW == 8 ? 2 : 1;
+        const int grid = units < per_sm * sm_count() ? units : per_sm * sm_count();
         if (p.g_logits)
-            decode_kernel<true><<<grid, kThreads, D_SMEM, st>>>(p);
+            decode_kernel<true, kDecNW, kDecNS><<<grid, kDecNW * 32, L::bytes, st>>>(p);
         else
-            decode_kernel<false><<<grid, kThreads, D_SMEM, st>>>(p);
+            decode_kernel<false, kDecNW, kDecNS><<<grid, kDecNW * 32, L::bytes, st>>>(p);
         note_launch();
         return check_launch("decode_kernel");
     }
