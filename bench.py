@@ -45,11 +45,11 @@ MEASURED_TRAFFIC = {
                 "sha256": "0fccd070f8eb85530e65c30c9bd47fb8aa82ab3f500d1cd652d49f45a4d28431",
                 "bytes_per_unit": (252.794368e6 + 77.790976e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
-    # B=64 capture: mean of two launches, 755.2 MB / (64 * 96) (sequence, head) units
+    # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
-               "sha256": "3d1913e5bd8d5b799678049317268377001a3f8774c6e27d2d4a1afa97da2178",
-               "bytes_per_unit": 755.20192e6 / (64 * 96),
-               "capture": "profiles/recurrent_kernel_decode_B64.md"},
+               "sha256": "ede5158c131edfc4a652ea4d3a646abd27d6ef5093fa3bf7fdd0920d87253ef4",
+               "bytes_per_unit": 754.843776e6 / (64 * 96),
+               "capture": "profiles/decode_kernel_B64.md"},
     # full-size captures: mean of two launches per (token, channel) element
     "conv_prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
                      "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
