@@ -96,6 +96,26 @@ def test_decode_zero_state_and_no_norm():
     assert rel_err(s, so) <= FP32_TOL
 
 
+def test_decode_fp32_inputs_bf16_outputs_and_many_units_per_cta():
+    """fp32 q, k, v and gate (staged rows of 512 bytes instead of 256) and bf16 outputs;
+    5 x 97 units, more than one per CTA of the persistent decode kernel on most GPUs
+    with few SMs and exactly its stride pattern on the others."""
+    d = decode_inputs(B=5, H=97)
+    f32 = {n: d[n].float() for n in ("q", "k", "v", "gate")}
+    o, s, y = kda.recurrent_step(f32["q"], f32["k"], f32["v"], d["g"], d["beta"], d["initial_state"],
+                                 gate=f32["gate"], norm_w=d["norm_w"], eps=d["eps"], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert o.dtype == torch.bfloat16 and y.dtype == torch.bfloat16
+    oo, so, yo = decode_oracle(d)
+    assert rel_err(s, so) <= FP32_TOL
+    # bf16 outputs: the oracle's values, rounded to bf16 once (half an ulp, 2^-9 relative)
+    for got, ref in ((o.float(), oo), (y.float().view(5, 97, 128), yo.reshape(5, 97, 128))):
+        got = got.cpu().double().numpy()
+        ref = np.asarray(ref, np.float64)
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * rms)
+
+
 @pytest.mark.parametrize("K,V", [(32, 32), (64, 64), (128, 64), (64, 128)])
 def test_decode_other_head_sizes(K, V):
     torch.manual_seed(0)
