@@ -45,6 +45,12 @@ MEASURED_TRAFFIC = {
                 "sha256": "0fccd070f8eb85530e65c30c9bd47fb8aa82ab3f500d1cd652d49f45a4d28431",
                 "bytes_per_unit": (252.794368e6 + 77.790976e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
+    # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture (one launch):
+    # (202.09 + 73.61 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
+                       "sha256": "0fccd070f8eb85530e65c30c9bd47fb8aa82ab3f500d1cd652d49f45a4d28431",
+                       "bytes_per_unit": (202.094848e6 + 73.614080e6 - 6.291456e6) / (2048 * 96),
+                       "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
                "sha256": "ede5158c131edfc4a652ea4d3a646abd27d6ef5093fa3bf7fdd0920d87253ef4",
@@ -300,7 +306,8 @@ def bench_prefill_logits(args, world, peaks):
             "config": {"workload": f"prefill B={B} T={T} H={H} d={K}, bf16 g/beta logits + A_log + dt_bias, "
                                    "lower bound -5", "l2_flush": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": measured_traffic("prefill_logits", th, B * H * STATE_BYTES),
                          "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
                          "peak_source": peaks["source"]}}
 
@@ -460,7 +467,7 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
@@ -483,9 +490,11 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "conv", "kernels"):
+    if args.only in ("decode", "conv", "kernels", "logits"):
         if args.only == "kernels":  # decode step + short convolution (profiling runs)
             res = {"decode": bench_decode(args, world, peaks), "short_conv": bench_short_conv(args, world, peaks)}
+        elif args.only == "logits":  # the prefill with gates from logits alone (profiling runs)
+            res = bench_prefill_logits(args, world, peaks)
         else:
             res = bench_decode(args, world, peaks) if args.only == "decode" else bench_short_conv(args, world, peaks)
         if rank == 0:
