@@ -425,6 +425,30 @@ def cpu_baseline(d, heads: int):
                       f"tokens/s scaled by {heads}/{d['H']}; {dt:.2f} s wall"}
 
 
+def cpu_baseline_decode_one_core(units: int = 2048):
+    """The fp64 oracle on one host core for the decode step (B=256, H=96): a sample of
+    `units` (sequence, head) units, tokens/s scaled to the whole batch."""
+    import numpy as np
+    import torch
+    import oracle
+    from kimi_delta_attention_gated_gb300.inputs import make_inputs
+    d = make_inputs("decode", device="cpu")
+    B, H = d["B"], d["H"]
+    f = lambda t: np.ascontiguousarray(t.float().numpy())
+    n = min(units, B * H)
+    flat = lambda t: t.reshape((B * H, 1, 1) + tuple(t.shape[3:]))[:n]  # each unit its own sequence
+    q, k, v, g = (f(flat(d[x])) for x in ("q", "k", "v", "g"))
+    beta = f(d["beta"].reshape(B * H, 1, 1)[:n])
+    s0 = f(d["initial_state"].reshape((B * H, 1) + tuple(d["initial_state"].shape[2:]))[:n])
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.recurrent(q, k, v, g, beta, s0, scale=d["scale"], n_threads=1)
+    dt = time.perf_counter() - t0
+    return {"value": B * (n / (B * H)) / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {B * H} (sequence, head) units of the decode step B={B} H={H}; tokens/s scaled "
+                      f"by {n}/{B * H}; {dt:.2f} s wall (the gated norm epilogue not included)"}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the fp64 oracle on the host cores, a bounded sample per step."""
     if rank != 0:
@@ -509,6 +533,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
         cpu = cpu_baseline(d, args.cpu_heads)
+        if dec is not None:
+            dec["cpu_baseline_one_core"] = cpu_baseline_decode_one_core()
     if rank != 0:
         return
     dtype = "f32" if args.mode == "fp32" else "bf16 hi/lo split operands, f32 accumulate and state"
