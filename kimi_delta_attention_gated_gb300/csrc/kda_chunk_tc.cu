@@ -44,9 +44,11 @@
 //       ... meanwhile on CUDA cores: gram pass, T = (I + A)^-1, T diag(beta) tile
 //     D^T  = R^T (T diag beta)^T                           N=64  K=64  (R^T in TMEM)
 //     [O|S]^T += D^T [P^T | Kg]  (S^T pre-scaled by exp(gamma))  N=192 K=64
-// The next chunk's q, k and g are loaded into registers while the current one runs,
-// and its CUDA-core preparation (norms, cumulative decay, operand tiles) is done while
-// this chunk's D and [O|S] products run on the tensor cores.
+// The next chunk's q and k are loaded into registers and its g (or logits) arrives by
+// TMA while the current one runs; its CUDA-core preparation (norms, cumulative decay,
+// operand tiles) is done while this chunk's D and [O|S] products run on the tensor
+// cores.  Warp 0, which issues every product and stalls behind the tensor core's queue
+// meanwhile, prepares its own tokens' norms during the solve instead (g and beta given).
 #include <cuda.h>
 #include <math.h>
 #include <string.h>
