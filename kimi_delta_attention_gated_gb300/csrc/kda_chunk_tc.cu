@@ -31,18 +31,20 @@
 // R/O product is issued while warps 1-15 run the triangular solve (thread 0's warp
 // stalls on the MMA queue meanwhile).  Everything is transposed so that the value
 // dimension (128) is the MMA M dimension and the TMEM lane:
-//   TMEM columns   [0,64)   R^T accumulator, then D^T hi [0,32) / lo [32,64)
+//   TMEM columns   [0,64)   R^T accumulator, then R^T hi/lo in place: for tokens
+//                           16b..16b+15, hi in [16b, 16b+8) and lo in [16b+8, 16b+16)
 //                 [64,128)  O^T accumulator
 //                [128,256)  S^T fp32 accumulator (lane v, column c)
 //                [256,320)  S^T hi, packed bf16 pairs (A operand of the state MMAs)
 //                [320,384)  S^T lo
-//                [384,512)  gram accumulator: [hi*hi + lo*hi | hi*lo], then R^T hi
-//                           [384,416) / lo [416,448) and the D^T accumulator [448,512)
+//                [384,512)  gram accumulator: [hi*hi + lo*hi | hi*lo]; then the D^T
+//                           accumulator [hi*(hi;lo) + lo*hi | ...], summed into D^T hi/lo
+//                           in place in [384,448) with the layout of R^T
 //   per chunk (B operands in shared memory are K-major unless noted):
 //     gram   [-Kd;Qd] [Km_hi;Km_lo]^T  M=128 N=128 K=128, + [-Kd;Qd]_lo Km_hi^T N=64
 //     R^T  = V^T I (N=64), then [R|O]^T += S^T [-Kd;Qd]^T   N=128 K=128 (S^T in TMEM)
 //       ... meanwhile on CUDA cores: gram pass, T = (I + A)^-1, T diag(beta) tile
-//     D^T  = R^T (T diag beta)^T                           N=64  K=64  (R^T in TMEM)
+//     D^T  = R^T (T diag beta)^T   N=128 (hi against both halves) + N=64, K=64 (R^T in TMEM)
 //     [O|S]^T += D^T [P^T | Kg]  (S^T pre-scaled by exp(gamma))  N=192 K=64
 // The next chunk's q and k are loaded into registers and its g (or logits) arrives by
 // TMA while the current one runs; its CUDA-core preparation (norms, cumulative decay,
@@ -69,8 +71,7 @@ constexpr float kRangeMax = 80.f;
 constexpr uint32_t kPolls = 1u << 26;  // bound on every mbarrier wait
 
 // TMEM columns
-constexpr uint32_t T_R = 0, T_DH = 0, T_DL = 32, T_O = 64, T_S = 128, T_SH = 256, T_SL = 320, T_G = 384,
-                   T_RH = 384, T_RL = 416, T_D = 448;
+constexpr uint32_t T_R = 0, T_O = 64, T_S = 128, T_SH = 256, T_SL = 320, T_G = 384;
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t S_V = 0;             // V tile, two TMA boxes of 64 tokens x 64 values (16 KB)
@@ -820,8 +821,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
-            tmem_st8(tb + lane_off + T_RH + wg * 8, hi);
-            tmem_st8(tb + lane_off + T_RL + wg * 8, lo);
+            tmem_st8(tb + lane_off + T_R + wg * 16, hi);  // in place: tokens 16 wg.. as hi, then lo
+            tmem_st8(tb + lane_off + T_R + wg * 16 + 8, lo);
             tmem_wait_st();
         }
         fence_before_sync();
@@ -831,13 +832,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= D^T = R^T (T diag beta)^T
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t id64 = idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int cb = 0; cb < 3; ++cb)
+            // R^T_hi [T diag(beta)_hi ; _lo]^T (N = 128: the two tiles are contiguous) into
+            // [D_a | D_b], then R^T_lo (T diag beta)_hi^T onto D_a
+            const uint32_t id128 = idesc_bf16(128, 128, false, false), id64 = idesc_bf16(128, 64, false, false);
 #pragma unroll 1
-                for (int s = 0; s < 4; ++s)
-                    mma_ts(tb + T_D, tb + (combo_a(cb) ? T_RL : T_RH) + s * 8,
-                           sdesc_at(sb16, (combo_b(cb) ? S_TBL : S_TBH) + s * 32, 16, 1024), id64, (cb | s) ? 1u : 0u);
+            for (int s = 0; s < 4; ++s)
+                mma_ts(tb + T_G, tb + T_R + s * 16, sdesc_at(sb16, S_TBH + s * 32, 16, 1024), id128, s ? 1u : 0u);
+#pragma unroll 1
+            for (int s = 0; s < 4; ++s)
+                mma_ts(tb + T_G, tb + T_R + s * 16 + 8, sdesc_at(sb16, S_TBH + s * 32, 16, 1024), id64, 1u);
             mma_commit(bar_d);
         }
         __syncwarp();
@@ -854,14 +857,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             uint32_t r[16], s1[16], s2[16], hi[8], lo[8];
             const int c0 = wg * 32;
-            tmem_ld16(tb + lane_off + T_D + wg * 16, r);
+            {
+                uint32_t rb[16];
+                tmem_ld16(tb + lane_off + T_G + wg * 16, r);
+                tmem_ld16(tb + lane_off + T_G + 64 + wg * 16, rb);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {  // D = D_a + D_b
+                    const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])),
+                                                make_float2(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])));
+                    r[c] = __float_as_uint(v.x);
+                    r[c + 1] = __float_as_uint(v.y);
+                }
+            }
             tmem_ld16(tb + lane_off + T_S + c0, s1);
             tmem_ld16(tb + lane_off + T_S + c0 + 16, s2);
-            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
-            tmem_st8(tb + lane_off + T_DH + wg * 8, hi);
-            tmem_st8(tb + lane_off + T_DL + wg * 8, lo);
+            tmem_st8(tb + lane_off + T_G + wg * 16, hi);  // in place: tokens 16 wg.. as hi, then lo
+            tmem_st8(tb + lane_off + T_G + wg * 16 + 8, lo);
+            tmem_wait_ld();
             const float4 *ge = reinterpret_cast<const float4 *>(fs + F_GEXP + c0);
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
@@ -895,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cb = 0; cb < 3; ++cb)
 #pragma unroll 1
                 for (int s = 0; s < 4; ++s)
-                    mma_ts(tb + T_O, tb + (combo_a(cb) ? T_DL : T_DH) + s * 8,
+                    mma_ts(tb + T_O, tb + T_G + s * 16 + (combo_a(cb) ? 8 : 0),
                            sdesc_at(sb16, (combo_b(cb) ? S_PKGL : S_PKGH) + s * 32, 16, 1024), id192, 1u);
             mma_commit(bar_s);
         }
