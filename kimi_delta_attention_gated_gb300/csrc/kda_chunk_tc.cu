@@ -96,8 +96,8 @@ constexpr uint32_t F_RED = 320;   // norm partials [4 wg][4 quarters][16]
 constexpr uint32_t F_BETA0 = 576; // beta of tokens 0-3 (warp 0 prepares them while the solve reads F_BETA)
 constexpr uint32_t F_SCAN0 = 580; // decay totals of tokens 0-3 [128]
 constexpr uint32_t F_END = 708;
-constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 7 mbarriers + tmem slot
-constexpr uint32_t SMEM_BYTES = S_BARS + 64 + 1024;  // + alignment slack
+constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 8 mbarriers + tmem slot
+constexpr uint32_t SMEM_BYTES = S_BARS + 80 + 1024;  // + alignment slack
 // scan scratch aliases T (free during prep): [16 warps][128] floats of decay totals, then
 // their exclusive prefixes [16][128] and the chunk total [128]
 constexpr uint32_t S_SCAN = S_T;
@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tma_bar = bar_g + 4;                                  // V tile
     uint64_t *drain_bar = bar_g + 5;                                // drain after a failure
     uint64_t *gt_bar = bar_g + 6;                                   // g tile
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 56);
+    uint64_t *pre_bar = bar_g + 7;                                  // decay prefix written (128 arrivals)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 64);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wg = warp >> 2, wq = warp & 3;
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int b = 0; b < 7; ++b) mbar_init(bar_g + b, 1);
+        mbar_init(pre_bar, 128);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -483,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc += t;
             }
             pre[16 * 128 + c] = acc;
+            mbar_arrive(pre_bar);  // for warp 0, which is not in the barrier below
         }
         tbar();
     };
@@ -917,8 +920,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // while O and S update: the next chunk's operand tiles (its Kg waits for this MMA)
         if (ch + 1 < nchunks) {
-            if (warp > 0) scan_prefix();
-            oor_next = prep_tiles(cr, kgv, warp > 0);
+            if (warp > 0)
+                scan_prefix();
+            else if (!mbar_wait(pre_bar, (uint32_t)(ch & 1), kPolls))  // warp 0, after its O/S issue
+                failed = 1;
+            oor_next = prep_tiles(cr, kgv, true);
         }
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
