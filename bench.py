@@ -40,17 +40,17 @@ PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits b
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture, mean of two launches: (328.183424 MB - 6.29 MB of final state)
+    # B=1 T=2048 H=96 capture, mean of two launches: (328.194816 MB - 6.29 MB of final state)
     # / (2048 * 96) token-heads
     "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                "sha256": "e52a976b52922b60846f9ff4d2766cf246557ab48ca44db67786335daed77ec9",
-                "bytes_per_unit": (328.183424e6 - 6.291456e6) / (2048 * 96),
+                "sha256": "091ea7eaab910be4e2814f3820a8cae147fc5b9ac8ce0aa9988912da0e9ccfe9",
+                "bytes_per_unit": (328.194816e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture, mean of two
-    # launches: (274.384 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # launches: (274.532096 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                       "sha256": "e52a976b52922b60846f9ff4d2766cf246557ab48ca44db67786335daed77ec9",
-                       "bytes_per_unit": (274.384e6 - 6.291456e6) / (2048 * 96),
+                       "sha256": "091ea7eaab910be4e2814f3820a8cae147fc5b9ac8ce0aa9988912da0e9ccfe9",
+                       "bytes_per_unit": (274.532096e6 - 6.291456e6) / (2048 * 96),
                        "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",

@@ -95,7 +95,9 @@ constexpr uint32_t F_GEXP = 192;  // exp(gamma) [128]
 constexpr uint32_t F_RED = 320;   // norm partials [4 wg][4 quarters][16]
 constexpr uint32_t F_BETA0 = 576; // beta of tokens 0-3 (warp 0 prepares them while the solve reads F_BETA)
 constexpr uint32_t F_SCAN0 = 580; // decay totals of tokens 0-3 [128]
-constexpr uint32_t F_END = 708;
+constexpr uint32_t F_AH = 708;    // gates from logits: exp(A_log) of the head [1 of 4]
+constexpr uint32_t F_DB = 712;    // gates from logits: dt_bias of the head's channels [128]
+constexpr uint32_t F_END = 840;
 constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 8 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = S_BARS + 80 + 1024;  // + alignment slack
 // scan scratch aliases T (free during prep): [16 warps][128] floats of decay totals, then
@@ -235,25 +237,32 @@ struct ChunkRegs {
     float beta;   // token warp * 4 + lane, lanes 0-3 (or its logit until prepared)
 };
 
+// The next chunk's q, k (and beta, or the raw bits of its logit) into registers.  Nothing
+// here waits for the data: rows past the chunk's end read its last row instead and are
+// zeroed when the chunk is prepared, and a logit is converted there too.
 template <bool GL>
 __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, int bos, int t0, int cn, int h,
                                            int warp, int l4) {
+    if (cn <= 0) return;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const int i = warp * 4 + r;
-        cr.q[r] = make_uint2(0u, 0u);
-        cr.k[r] = make_uint2(0u, 0u);
-        if (i < cn) {
-            const size_t hk = ((size_t)(bos + t0 + i) * p.H + h) * DK + l4;
-            cr.q[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + hk));
-            cr.k[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
-        }
+        const int i = min(warp * 4 + r, cn - 1);
+        const size_t hk = ((size_t)(bos + t0 + i) * p.H + h) * DK + l4;
+        cr.q[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + hk));
+        cr.k[r] = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + hk));
     }
-    // beta of token warp * 4 + lane (lanes 0-3); the address stays inside the chunk for every lane
-    const int ib = warp * 4 + ((l4 >> 2) & 3);
-    const bool okb = l4 < 16 && ib < cn;
-    const size_t bi = (size_t)(bos + t0 + (okb ? ib : 0)) * p.H + h;
-    cr.beta = !okb ? 0.f : (GL ? ld_in(p.beta_logits, bi, p.beta_logits_bf16) : __ldg(p.beta + bi));
+    // beta of token warp * 4 + lane (lanes 0-3; the others hold a copy)
+    const size_t bi = (size_t)(bos + t0 + min(warp * 4 + ((l4 >> 2) & 3), cn - 1)) * p.H + h;
+    if (!GL) {
+        cr.beta = __ldg(p.beta + bi);
+    } else {
+        uint32_t raw;
+        if (p.beta_logits_bf16)
+            asm("ld.global.nc.u16 %0, [%1];" : "=r"(raw) : "l"(reinterpret_cast<const uint16_t *>(p.beta_logits) + bi));
+        else
+            asm("ld.global.nc.u32 %0, [%1];" : "=r"(raw) : "l"(reinterpret_cast<const uint32_t *>(p.beta_logits) + bi));
+        cr.beta = __uint_as_float(raw);
+    }
 }
 
 // GL: g and beta come from their logits (a compile-time choice; the plain path carries no
@@ -317,6 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // blocks on or below the diagonal
         st_shared_v4(sb + S_TBH + tid * 32, 0u, 0u, 0u, 0u);
         st_shared_v4(sb + S_TBH + tid * 32 + 16, 0u, 0u, 0u, 0u);
+    }
+    if (GL) {  // the head's gate constants, read by every chunk's conversion
+        if (tid < DK) fs[F_DB + tid] = p.dt_bias ? __ldg(p.dt_bias + (size_t)h * DK + tid) : 0.f;
+        if (tid == DK) fs[F_AH] = __expf(__ldg(p.A_log + h));
     }
     fence_async_smem();
     fence_before_sync();
@@ -389,6 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (tid == 0)
             g_pending = -1;
 #pragma unroll
+        for (int r = 0; r < 4; ++r)  // tokens past the chunk's end: q = k = 0 (loaded as a copy)
+            if (warp * 4 + r >= cnn) {
+                c.q[r] = make_uint2(0u, 0u);
+                c.k[r] = make_uint2(0u, 0u);
+            }
+#pragma unroll
         for (int r = 0; r < 4; ++r) {  // tokens past the chunk's end read as g = 0
             const int i = warp * 4 + r;
             if (GL && p.g_logits_bf16) {
@@ -400,9 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!GL && i >= cnn) c.g[r] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (GL) {  // g from its logits; tokens past the chunk's end keep g = 0
-            const float a_h = __expf(__ldg(p.A_log + h));
-            const float4 db = p.dt_bias ? __ldg(reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * DK + l4))
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float a_h = fs[F_AH];
+            const float4 db = *reinterpret_cast<const float4 *>(fs + F_DB + l4);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 float z[4];
@@ -419,7 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      live ? gate_of_logit(z[3] + db.w, a_h, p.g_lower) : 0.f);
             }
         }
-        if (GL && lane < 4) c.beta = warp * 4 + lane < cnn ? beta_of_logit(c.beta) : 0.f;
+        if (GL && lane < 4) {
+            const uint32_t raw = __float_as_uint(c.beta);
+            c.beta = warp * 4 + lane < cnn ? beta_of_logit(__uint_as_float(p.beta_logits_bf16 ? raw << 16 : raw)) : 0.f;
+        }
+        if (!GL && warp * 4 + lane >= cnn) c.beta = 0.f;
         float a[8];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {  // (q, k) sums of squares as packed pairs
@@ -490,6 +512,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tbar();
     };
 
+    // [-Kd ; Qd] rows of token i (hi and lo tiles) from its cumulative decay G on this
+    // lane's four key channels; rows i and 64 + i share the swizzle phase, 8 KB apart
+    auto put_kq = [&](int i, const float2 (&G)[2], uint2 q, uint2 k, float rq, float rk) {
+        const float2 qv2[2] = {make_float2(bf16lo(q.x), bf16hi(q.x)), make_float2(bf16lo(q.y), bf16hi(q.y))};
+        const float2 kv2[2] = {make_float2(bf16lo(k.x), bf16hi(k.x)), make_float2(bf16lo(k.y), bf16hi(k.y))};
+        const float2 nrk2 = make_float2(-rk, -rk), rq2 = make_float2(rq, rq);
+        float2 kd[2], qd[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float2 eG = make_float2(__expf(G[e].x), __expf(G[e].y));
+            kd[e] = __fmul2_rn(__fmul2_rn(kv2[e], nrk2), eG);  // -k^ exp(G)
+            qd[e] = __fmul2_rn(__fmul2_rn(qv2[e], rq2), eG);
+        }
+        const uint32_t off = sw128_off(i, l4, 128);
+        uint32_t h0, l0, h1, l1;
+        split2(kd[0].x, kd[0].y, h0, l0);
+        split2(kd[1].x, kd[1].y, h1, l1);
+        st_shared_v2(sb + S_KQH + off, h0, h1);
+        st_shared_v2(sb + S_KQL + off, l0, l1);
+        split2(qd[0].x, qd[0].y, h0, l0);
+        split2(qd[1].x, qd[1].y, h1, l1);
+        st_shared_v2(sb + S_KQH + off + 8192, h0, h1);
+        st_shared_v2(sb + S_KQL + off + 8192, l0, l1);
+    };
     auto prep_tiles = [&](const ChunkRegs &c, float (&kgv)[4][4], bool use_pre) -> int {
         float o4[4] = {0.f, 0.f, 0.f, 0.f}, gam[4] = {0.f, 0.f, 0.f, 0.f};
         if (use_pre) {  // offset of this warp's tokens and the chunk total, per channel
@@ -516,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             egam[e] = __expf(gam[e]);
             oor |= (-gam[e] > kRangeMax);
         }
-        if (warp == 0) *reinterpret_cast<float4 *>(fs + F_GEXP + l4) = make_float4(egam[0], egam[1], egam[2], egam[3]);
+        if (warp == 1) *reinterpret_cast<float4 *>(fs + F_GEXP + l4) = make_float4(egam[0], egam[1], egam[2], egam[3]);
         const float4 rq4 = *reinterpret_cast<const float4 *>(fs + F_RQ + warp * 4);
         const float4 rk4 = *reinterpret_cast<const float4 *>(fs + F_RK + warp * 4);
         const float rq[4] = {rq4.x, rq4.y, rq4.z, rq4.w}, rk[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
@@ -528,36 +574,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 4; ++r) {
             const int i = warp * 4 + r;
             const float2 gr2[2] = {make_float2(c.g[r].x, c.g[r].y), make_float2(c.g[r].z, c.g[r].w)};
-            const float2 qv2[2] = {make_float2(bf16lo(c.q[r].x), bf16hi(c.q[r].x)),
-                                   make_float2(bf16lo(c.q[r].y), bf16hi(c.q[r].y))};
             const float2 kv2[2] = {make_float2(bf16lo(c.k[r].x), bf16hi(c.k[r].x)),
                                    make_float2(bf16lo(c.k[r].y), bf16hi(c.k[r].y))};
-            const float2 rk2 = make_float2(rk[r], rk[r]), nrk2 = make_float2(-rk[r], -rk[r]);
-            const float2 rq2 = make_float2(rq[r], rq[r]);
-            float2 kd[2], qd[2], km[2];
+            const float2 rk2 = make_float2(rk[r], rk[r]);
+            float2 km[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 o2[e] = __fadd2_rn(o2[e], gr2[e]);  // inclusive cumulative decay G of token i
-                const float2 eG = make_float2(__expf(o2[e].x), __expf(o2[e].y));
                 const float2 em = make_float2(__expf(-o2[e].x), __expf(-o2[e].y));
-                kd[e] = __fmul2_rn(__fmul2_rn(kv2[e], nrk2), eG);  // -k^ exp(G)
-                qd[e] = __fmul2_rn(__fmul2_rn(qv2[e], rq2), eG);
                 km[e] = __fmul2_rn(__fmul2_rn(kv2[e], rk2), em);
                 const float2 kg = __fmul2_rn(km[e], eg2[e]);
                 kgv[r][2 * e] = kg.x;
                 kgv[r][2 * e + 1] = kg.y;
             }
-            // rows i and 64 + i of the 128-row tiles share the swizzle phase, 8 KB apart
+            put_kq(i, o2, c.q[r], c.k[r], rq[r], rk[r]);
             const uint32_t off = sw128_off(i, l4, 128);
             uint32_t h0, l0, h1, l1;
-            split2(kd[0].x, kd[0].y, h0, l0);
-            split2(kd[1].x, kd[1].y, h1, l1);
-            st_shared_v2(sb + S_KQH + off, h0, h1);
-            st_shared_v2(sb + S_KQL + off, l0, l1);
-            split2(qd[0].x, qd[0].y, h0, l0);
-            split2(qd[1].x, qd[1].y, h1, l1);
-            st_shared_v2(sb + S_KQH + off + 8192, h0, h1);
-            st_shared_v2(sb + S_KQL + off + 8192, l0, l1);
             split2(km[0].x, km[0].y, h0, l0);
             split2(km[1].x, km[1].y, h1, l1);
             st_shared_v2(sb + S_KM + off, h0, h1);
@@ -571,13 +603,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- first chunk's preparation (later chunks are prepared inside the previous
     // chunk's tensor-core waits)
     int oor_next = 0;
-    float kgv[4][4];  // the next chunk's Kg (g and beta given: stored while that chunk's gram runs)
+    float kgv[4][4];  // the next chunk's Kg, stored while that chunk's gram runs
     if (nchunks > 0) {
         prep_norms(cr, min(C, len), 0);
         beta0_publish();
         __syncthreads();
         oor_next = prep_tiles(cr, kgv, false);
-        if (GL) st_kg(kgv);
     }
 
     for (int ch = 0; ch < nchunks; ++ch) {
@@ -610,15 +641,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar_g);  // an empty commit on fallback chunks
         }
         __syncwarp();
-        // g and beta given: this chunk's Kg^T tile (the previous O/S product has read the old
-        // one; the gram does not read it).  With logits every warp loads here and warp 0
-        // would arrive late, so the tile is stored after the previous O/S product instead.
-        if (!GL) {
-            st_kg(kgv);
-            fence_async_smem();
-        }
-        // warps 1-15 (every warp with logits) start loading the next chunk while waiting for the gram
-        if ((GL || warp > 0) && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
+        // this chunk's Kg^T tile (the previous O/S product has read the old one; the gram
+        // does not read it)
+        st_kg(kgv);
+        fence_async_smem();
+        // warps 1-15 start loading the next chunk while waiting for the gram (warp 0 loads
+        // its tokens after the gram pass)
+        if (warp > 0 && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
         if (!wait_group(bar_g, par)) failed = 1;
         if (!fallback) {
             uint32_t r1[16], r2[16];
@@ -736,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_g(ch + 1);
                 g_pending = ch + 1;
             }
-            if (!GL && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
+            if (ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
         }
         if (tid == 0) {
             // ================= R^T = V^T I + S^T (-Kd)^T, O^T = S^T Qd^T (while warps 1-15 solve T)
@@ -928,7 +957,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
-        if (GL && ch + 1 < nchunks) st_kg(kgv);  // the Kg tile has been read
         {
             uint32_t r[16];
             const int c0 = wg * 32;
