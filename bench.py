@@ -35,23 +35,30 @@ PREFILL_FLOP_PER_TH = 10 * 64 * 128 + 6 * 128 * 128 + (2 * 64 * 64) // 3  # 182,
 STATE_BYTES = 128 * 128 * 4
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256 + 512  # + gate bf16, y fp32
 PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits bf16 + beta logit bf16 + o fp32
+PREFILL_NORM_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 256  # q,k,v bf16 + g fp32 + beta + gate bf16 + y bf16
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work from one
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture, mean of two launches: (328.194816 MB - 6.29 MB of final state)
+    # B=1 T=2048 H=96 capture, mean of two launches: (328.167424 MB - 6.29 MB of final state)
     # / (2048 * 96) token-heads
     "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                "sha256": "091ea7eaab910be4e2814f3820a8cae147fc5b9ac8ce0aa9988912da0e9ccfe9",
-                "bytes_per_unit": (328.194816e6 - 6.291456e6) / (2048 * 96),
+                "sha256": "a4a4aca3c624cabbb0a5312fe6d47fda7e086fcc10e587a1dc5981c57982ec91",
+                "bytes_per_unit": (328.167424e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture, mean of two
-    # launches: (274.532096 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # launches: (274.316928 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                       "sha256": "091ea7eaab910be4e2814f3820a8cae147fc5b9ac8ce0aa9988912da0e9ccfe9",
-                       "bytes_per_unit": (274.532096e6 - 6.291456e6) / (2048 * 96),
+                       "sha256": "a4a4aca3c624cabbb0a5312fe6d47fda7e086fcc10e587a1dc5981c57982ec91",
+                       "bytes_per_unit": (274.316928e6 - 6.291456e6) / (2048 * 96),
                        "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
+    # the same kernel with the fused gated norm (bf16 gate in, bf16 y out), B=1 T=2048 H=96
+    # capture, mean of two launches: (343.17248 MB - 6.29 MB of final state) / (2048 * 96)
+    "prefill_norm": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
+                     "sha256": "a4a4aca3c624cabbb0a5312fe6d47fda7e086fcc10e587a1dc5981c57982ec91",
+                     "bytes_per_unit": (343.17248e6 - 6.291456e6) / (2048 * 96),
+                     "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
                "sha256": "ede5158c131edfc4a652ea4d3a646abd27d6ef5093fa3bf7fdd0920d87253ef4",
@@ -313,6 +320,40 @@ def bench_prefill_logits(args, world, peaks):
                          "peak_source": peaks["source"]}}
 
 
+def bench_prefill_norm(args, world, peaks):
+    """The same prefill with the fused sigmoid-gated RMSNorm: bf16 gate in, y = the layer's
+    normed output in bf16 out (o itself is not written), sharing the prefill's q, k, v, g,
+    beta; gate ~ N(0, 1), norm weight 1 + N(0, 0.1^2), eps 1e-5."""
+    import torch
+    import kimi_delta_attention_gated_gb300 as kda
+    from kimi_delta_attention_gated_gb300.inputs import make_inputs
+    d = make_inputs("prefill", device="cuda", T=args.prefill_T)
+    B, T, H, K, V = d["B"], d["T"], d["H"], d["K"], d["V"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20_000)
+    gate = torch.randn((B, T, H, V), generator=gen, device="cuda").to(torch.bfloat16)
+    norm_w = 1 + 0.1 * torch.randn(V, generator=gen, device="cuda")
+    y = torch.empty((B, T, H * V), device="cuda", dtype=torch.bfloat16)
+    fs = torch.empty((B, H, K, V), device="cuda", dtype=torch.float32)
+    fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, scale=d["scale"], mode=args.mode,
+                               gate=gate, norm_w=norm_w, eps=1e-5, out_dtype=torch.bfloat16, return_o=False, y=y,
+                               final_state=fs)
+    r = time_steps(fn, args.steps, args.warmup, world)
+    kernel_ms = r["call_ms"] / max(1, r["launches"] // args.steps)
+    th = B * T * H
+    algo_bytes = th * PREFILL_NORM_BYTES_PER_TH + B * H * STATE_BYTES
+    achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+    return {"metric": "KDA prefill tokens/s, fused gated RMSNorm output", "value": world * B * T / (r["ms_per_step"] * 1e-3),
+            "unit": "tokens/s", "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
+            "config": {"workload": f"prefill B={B} T={T} H={H} d={K}, bf16 gate in, bf16 y out (sigmoid-gated "
+                                   "RMSNorm), o not written", "l2_flush": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": measured_traffic("prefill_norm", th, B * H * STATE_BYTES),
+                         "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
+                         "peak_source": peaks["source"]}}
+
+
 def bench_short_conv(args, world, peaks):
     """The q/k/v short convolution (causal depthwise, 4 taps, SiLU): one 8192-token prompt
     (state out) and one decode step of 256 sequences (state updated in place), each over
@@ -492,7 +533,7 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits", "norm"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
@@ -500,6 +541,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-logits", action="store_true")
+    ap.add_argument("--no-norm", action="store_true")
     ap.add_argument("--no-oproj", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -515,11 +557,13 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "conv", "kernels", "logits"):
+    if args.only in ("decode", "conv", "kernels", "logits", "norm"):
         if args.only == "kernels":  # decode step + short convolution (profiling runs)
             res = {"decode": bench_decode(args, world, peaks), "short_conv": bench_short_conv(args, world, peaks)}
         elif args.only == "logits":  # the prefill with gates from logits alone (profiling runs)
             res = bench_prefill_logits(args, world, peaks)
+        elif args.only == "norm":  # the prefill with the fused gated norm alone (profiling runs)
+            res = bench_prefill_norm(args, world, peaks)
         else:
             res = bench_decode(args, world, peaks) if args.only == "decode" else bench_short_conv(args, world, peaks)
         if rank == 0:
@@ -529,6 +573,7 @@ def main():
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
     conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
     logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
+    norm = None if (args.no_norm or args.only == "prefill") else bench_prefill_norm(args, world, peaks)
     oproj = None if (args.no_oproj or args.only == "prefill") else bench_o_proj(args, world, peaks)
     e2e = None if (args.no_e2e or args.only == "prefill") else bench_e2e(args, world, d)
     cpu = None
@@ -545,7 +590,7 @@ def main():
         "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": pre["config"],
         "roofline": pre["roofline"], "roofline_tensor": pre["roofline_tensor"], "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
-        "short_conv": conv, "prefill_gate_logits": logits, "o_proj": oproj,
+        "short_conv": conv, "prefill_gate_logits": logits, "prefill_gated_norm": norm, "o_proj": oproj,
         "gpu": torch.cuda.get_device_name(),
     }
     print(json.dumps(line), flush=True)

@@ -265,9 +265,10 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
     }
 }
 
-// GL: g and beta come from their logits (a compile-time choice; the plain path carries no
-// trace of it).
-template <bool GL>
+// GL: g and beta come from their logits.  NORM: the output goes through the fused
+// sigmoid-gated RMSNorm.  Both are compile-time choices, so the plain path carries no
+// trace of either.
+template <bool GL, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_g,
                     const __grid_constant__ TcParams tp) {
@@ -955,6 +956,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 failed = 1;
             oor_next = prep_tiles(cr, kgv, true);
         }
+        // the O pass's gate values, as raw bits from in-bounds rows, requested while the O/S
+        // product runs (read-only loads: none waits behind this thread's output stores)
+        uint32_t graw[16];
+        if (NORM) {
+            const size_t gstride = (size_t)H * DV, gbase = ((size_t)(bos + t0) * H + h) * DV + m;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const size_t gi = gbase + (size_t)min(wg * 16 + c, cn - 1) * gstride;
+                graw[c] = p.gate_bf16 ? ld_nc_u16(reinterpret_cast<const uint16_t *>(p.gate) + gi)
+                                      : ld_nc_u32(reinterpret_cast<const uint32_t *>(p.gate) + gi);
+            }
+        }
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
         {
@@ -978,27 +991,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int v = m;
             const int i0 = wg * 16;
-            if (p.gate) {
+            if (NORM) {
+                // sum of squares of each of the 16 rows over this warp's 32 value channels,
+                // by a reduce-scatter (16 shuffles): lane pair (2c, 2c + 1) ends with row c
                 float *red = fs + F_RED;
+                float x2[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float x = __uint_as_float(r[c]);
-                    const float s2v = warp_sum(x * x);
-                    if (lane == 0) red[(wg * 4 + wq) * 16 + c] = s2v;
+                    x2[c] = x * x;
                 }
+                const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+                float a8[8], a4[4], a2[2];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    a8[j] = (u16 ? x2[j + 8] : x2[j]) + __shfl_xor_sync(0xffffffffu, u16 ? x2[j] : x2[j + 8], 16);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    a4[j] = (u8 ? a8[j + 4] : a8[j]) + __shfl_xor_sync(0xffffffffu, u8 ? a8[j] : a8[j + 4], 8);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    a2[j] = (u4 ? a4[j + 2] : a4[j]) + __shfl_xor_sync(0xffffffffu, u4 ? a4[j] : a4[j + 2], 4);
+                float e = (u2 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, u2 ? a2[0] : a2[1], 2);
+                e += __shfl_xor_sync(0xffffffffu, e, 1);
+                if (!(lane & 1)) red[(wg * 4 + wq) * 16 + ((lane >> 1) & 15)] = e;
+                const float w = __ldg(p.norm_w + v);
                 __syncthreads();
-                const float w = p.norm_w[v];
+                // lane l forms 1 / rms of row l % 16 once; the others take it by shuffle
+                const int cl = lane & 15;
+                const float ssl = red[(wg * 4 + 0) * 16 + cl] + red[(wg * 4 + 1) * 16 + cl] +
+                                  red[(wg * 4 + 2) * 16 + cl] + red[(wg * 4 + 3) * 16 + cl];
+                const float invl = rsqrtf(ssl * (1.f / DV) + p.eps);
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int i = i0 + c;
+                    const float inv = __shfl_sync(0xffffffffu, invl, c);
                     if (i < cn) {
-                        const float ss = red[(wg * 4 + 0) * 16 + c] + red[(wg * 4 + 1) * 16 + c] +
-                                         red[(wg * 4 + 2) * 16 + c] + red[(wg * 4 + 3) * 16 + c];
-                        const float inv = rsqrtf(ss * (1.f / DV) + p.eps);
                         const size_t idx = ((size_t)(bos + t0 + i) * H + h) * DV + v;
                         const float x = __uint_as_float(r[c]);
-                        const float gt = ld_in(p.gate, idx, p.gate_bf16);
-                        st_out(p.y, idx, x * inv * w * sigmoidf_(gt), p.o_bf16);
+                        const float gt = __uint_as_float(p.gate_bf16 ? graw[c] << 16 : graw[c]);
+                        // sigmoid with the correctly rounded reciprocal (the value 1 / x has)
+                        st_out(p.y, idx, x * inv * w * __frcp_rn(1.0f + __expf(-gt)), p.o_bf16);
                         if (p.o) st_out(p.o, idx, x, p.o_bf16);
                     }
                 }
@@ -1140,7 +1173,8 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
     }
     static bool configured = false;
     if (!configured) {
-        for (void *fn : {(void *)chunk_tc_kernel<false>, (void *)chunk_tc_kernel<true>}) {
+        for (void *fn : {(void *)chunk_tc_kernel<false, false>, (void *)chunk_tc_kernel<true, false>,
+                         (void *)chunk_tc_kernel<false, true>, (void *)chunk_tc_kernel<true, true>}) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
             if (e != cudaSuccess) {
                 set_error("chunk_tc: cannot reserve %u bytes of shared memory: %s", SMEM_BYTES, cudaGetErrorString(e));
@@ -1149,10 +1183,9 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
         }
         configured = true;
     }
-    if (p_in.g_logits)
-        chunk_tc_kernel<true><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tp);
-    else
-        chunk_tc_kernel<false><<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tp);
+    auto kern = p_in.g_logits ? (p_in.gate ? chunk_tc_kernel<true, true> : chunk_tc_kernel<true, false>)
+                              : (p_in.gate ? chunk_tc_kernel<false, true> : chunk_tc_kernel<false, false>);
+    kern<<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tp);
     note_launch();
     return check_launch("chunk_tc_kernel");
 }

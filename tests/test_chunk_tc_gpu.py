@@ -145,6 +145,24 @@ def test_tc_fused_norm_and_o_together():
     assert rel_err(s, so) <= PARITY
 
 
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+def test_tc_fused_norm_gate_dtypes_bf16_out(gdt):
+    """The fused-norm instance with an fp32 or bf16 gate, o and y in bf16 (ragged tail)."""
+    d = make_inputs("long", device="cuda", B=1, T=333, H=3)
+    gate = d["gate"].to(gdt)
+    o, s, y = run_tc(d, gate=gate, norm_w=d["norm_w"], eps=d["eps"], out_dtype=torch.bfloat16)
+    oo, so = oracle_run(d)
+    yo = oracle.gated_rmsnorm(oo, np32(gate), np32(d["norm_w"]), eps=d["eps"])
+    assert o.dtype == torch.bfloat16 and y.dtype == torch.bfloat16
+    # bf16 outputs: within the rounding to bf16 (half an ulp, 2^-9 relative) plus the
+    # fp32 path's own error, element by element
+    for a, ref in ((o, oo), (y, yo)):
+        a = a.double().cpu().numpy().reshape(ref.shape)
+        rms = np.sqrt((ref ** 2).mean())
+        assert np.all(np.abs(a - ref) <= 2.0 ** -8 * np.abs(ref) + 5e-4 * rms)
+    assert rel_err(s, so) <= PARITY
+
+
 def test_tc_bf16_output():
     d = make_inputs("prefill", device="cuda", T=256, H=2)
     o, s = run_tc(d, out_dtype=torch.bfloat16)

@@ -65,6 +65,29 @@ def test_varlen_partial_chunks(mode):
     assert rel_err(sf, rs) <= PARITY
 
 
+@pytest.mark.parametrize("gdt", [torch.bfloat16, torch.float32])
+def test_prefill_logits_with_gated_norm(gdt):
+    """The gates-from-logits tensor kernel with the fused sigmoid-gated RMSNorm (its own
+    compiled instance), varlen with partial chunks, bf16 or fp32 gate: o, y and the final
+    states against the oracle (y = the oracle's gated norm of the oracle's o)."""
+    d = make_logit_inputs("varlen", H=3, lengths=[70, 1, 129, 64, 33])
+    B, T, H, V = d["v"].shape
+    gen = torch.Generator().manual_seed(2024)
+    gate = torch.randn((B, T, H, V), generator=gen).to(gdt)
+    norm_w = 1 + 0.1 * torch.randn(V, generator=gen)
+    x = dev(d)
+    o, sf, y = kda.chunk_fwd_logits(x["q"], x["k"], x["v"], x["g_logits"], x["beta_logits"], x["A_log"],
+                                    x["initial_state"], dt_bias=x["dt_bias"], g_lower_bound=x["g_lower_bound"],
+                                    scale=x["scale"], cu_seqlens=d["cu_seqlens"], mode="tensor",
+                                    gate=gate.cuda(), norm_w=norm_w.cuda(), eps=1e-5)
+    torch.cuda.synchronize()
+    ro, rs = oracle_from_logits(d)
+    ry = oracle.gated_rmsnorm(ro, np32(gate), np32(norm_w), 1e-5)
+    assert rel_err(o, ro) <= PARITY
+    assert rel_err(y, ry) <= PARITY
+    assert rel_err(sf, rs) <= PARITY
+
+
 def test_wide_decay_takes_exact_fallback():
     """Large logits with A = 16 drive g to the -5 floor on every channel: a chunk's decay
     range is 320 > 80, so the tensor kernel computes its grams exactly (reading g from
