@@ -1016,6 +1016,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 e += __shfl_xor_sync(0xffffffffu, e, 1);
                 if (!(lane & 1)) red[(wg * 4 + wq) * 16 + ((lane >> 1) & 15)] = e;
                 const float w = __ldg(p.norm_w + v);
+                // sigmoid of the gates before the barrier, where the warps wait for the last
+                // one, with the correctly rounded reciprocal (the value 1 / x has)
+                float sg[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float gt = __uint_as_float(p.gate_bf16 ? graw[c] << 16 : graw[c]);
+                    sg[c] = __frcp_rn(1.0f + __expf(-gt));
+                }
                 __syncthreads();
                 // lane l forms 1 / rms of row l % 16 once; the others take it by shuffle
                 const int cl = lane & 15;
@@ -1029,9 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i < cn) {
                         const size_t idx = ((size_t)(bos + t0 + i) * H + h) * DV + v;
                         const float x = __uint_as_float(r[c]);
-                        const float gt = __uint_as_float(p.gate_bf16 ? graw[c] << 16 : graw[c]);
-                        // sigmoid with the correctly rounded reciprocal (the value 1 / x has)
-                        st_out(p.y, idx, x * inv * w * __frcp_rn(1.0f + __expf(-gt)), p.o_bf16);
+                        st_out(p.y, idx, x * inv * w * sg[c], p.o_bf16);
                         if (p.o) st_out(p.o, idx, x, p.o_bf16);
                     }
                 }
