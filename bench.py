@@ -41,23 +41,23 @@ PREFILL_NORM_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 256  # q,k,v bf16 + g fp32
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture, mean of two launches: (328.272128 MB - 6.29 MB of final state)
+    # B=1 T=2048 H=96 capture, mean of two launches: (328.259712 MB - 6.29 MB of final state)
     # / (2048 * 96) token-heads
     "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                "sha256": "e6c64802b5fda0addfc2dbd3b7df8fa51c00076885409221dd912e7677eb0ea8",
-                "bytes_per_unit": (328.272128e6 - 6.291456e6) / (2048 * 96),
+                "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
+                "bytes_per_unit": (328.259712e6 - 6.291456e6) / (2048 * 96),
                 "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture, mean of two
-    # launches: (274.509696 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # launches: (274.432128 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                       "sha256": "e6c64802b5fda0addfc2dbd3b7df8fa51c00076885409221dd912e7677eb0ea8",
-                       "bytes_per_unit": (274.509696e6 - 6.291456e6) / (2048 * 96),
+                       "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
+                       "bytes_per_unit": (274.432128e6 - 6.291456e6) / (2048 * 96),
                        "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # the same kernel with the fused gated norm (bf16 gate in, bf16 y out), B=1 T=2048 H=96
-    # capture, mean of two launches: (342.192384 MB - 6.29 MB of final state) / (2048 * 96)
+    # capture, mean of two launches: (343.342848 MB - 6.29 MB of final state) / (2048 * 96)
     "prefill_norm": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                     "sha256": "e6c64802b5fda0addfc2dbd3b7df8fa51c00076885409221dd912e7677eb0ea8",
-                     "bytes_per_unit": (342.192384e6 - 6.291456e6) / (2048 * 96),
+                     "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
+                     "bytes_per_unit": (343.342848e6 - 6.291456e6) / (2048 * 96),
                      "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
     # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",

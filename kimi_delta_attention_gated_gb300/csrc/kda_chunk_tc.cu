@@ -271,7 +271,7 @@ __device__ __forceinline__ void load_chunk(const SeqParams &p, ChunkRegs &cr, in
 template <bool GL, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_g,
-                    const __grid_constant__ TcParams tp) {
+                    const __grid_constant__ CUtensorMap tmap_gate, const __grid_constant__ TcParams tp) {
     const SeqParams &p = tp.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain_bar = bar_g + 5;                                // drain after a failure
     uint64_t *gt_bar = bar_g + 6;                                   // g tile
     uint64_t *pre_bar = bar_g + 7;                                  // decay prefix written (128 arrivals)
+    uint64_t *gate_bar = reinterpret_cast<uint64_t *>(sm + S_BARS + 72);  // fused norm: gate tile
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 64);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int b = 0; b < 7; ++b) mbar_init(bar_g + b, 1);
         mbar_init(pre_bar, 128);
+        if (NORM) mbar_init(gate_bar, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -346,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sb + S_V + 8192, &tmap_v, tma_bar, 64, h, bos + chunk * C);
     };
     int v_pending = -1;  // chunk whose V tile is in flight (thread 0 only)
+    int q_pending = -1;  // chunk whose gate tile is in flight (thread 0 only)
     // g (or its logits) of one chunk, 64 tokens x 128 channels, into the Km tile, which is
     // free from the end of a gram pass until the next operand tiles are written
     const uint32_t g_bytes = (GL && p.g_logits_bf16) ? C * DK * 2 : C * DK * 4;
@@ -858,9 +861,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st8(tb + lane_off + T_R + wg * 16 + 8, lo);
             tmem_wait_st();
         }
+        if (NORM) fence_async_smem();  // the A buffer (written in the gram pass) takes the gate tile next
         fence_before_sync();
         // ---- T diag(beta) tile and R^T hi/lo are ready
         if (__syncthreads_or(failed)) break;
+        // fused norm, bf16 gate: this chunk's gate tile (64 tokens x 128 values) into the A
+        // buffer, free from the end of the solve to the next gram pass, read by the O pass
+        if (NORM && tid == 0 && p.gate_bf16) {
+            mbar_arrive_expect_tx(gate_bar, C * DV * 2);
+            tma_load_3d(sb + S_A, &tmap_gate, gate_bar, 0, h, bos + t0);
+            q_pending = ch;
+        }
 
         // ================= D^T = R^T (T diag beta)^T
         if (tid == 0) {
@@ -956,18 +967,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 failed = 1;
             oor_next = prep_tiles(cr, kgv, true);
         }
-        // the O pass's gate values, as raw bits from in-bounds rows, requested while the O/S
-        // product runs (read-only loads: none waits behind this thread's output stores)
-        uint32_t graw[16];
-        if (NORM) {
-            const size_t gstride = (size_t)H * DV, gbase = ((size_t)(bos + t0) * H + h) * DV + m;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const size_t gi = gbase + (size_t)min(wg * 16 + c, cn - 1) * gstride;
-                graw[c] = p.gate_bf16 ? ld_nc_u16(reinterpret_cast<const uint16_t *>(p.gate) + gi)
-                                      : ld_nc_u32(reinterpret_cast<const uint32_t *>(p.gate) + gi);
-            }
-        }
         // ================= O pass (+ gated norm) and state pass
         if (!wait_group(bar_s, par)) failed = 1;
         {
@@ -1017,12 +1016,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(lane & 1)) red[(wg * 4 + wq) * 16 + ((lane >> 1) & 15)] = e;
                 const float w = __ldg(p.norm_w + v);
                 // sigmoid of the gates before the barrier, where the warps wait for the last
-                // one, with the correctly rounded reciprocal (the value 1 / x has)
+                // one, with the correctly rounded reciprocal (the value 1 / x has).  A bf16
+                // gate comes from the tile in shared memory; an fp32 one from global memory
                 float sg[16];
+                if (p.gate_bf16) {
+                    if (!mbar_wait(gate_bar, (uint32_t)(ch & 1), kPolls))
+                        failed = 1;
+                    else if (tid == 0)
+                        q_pending = -1;
+                    const uint16_t *gs = reinterpret_cast<const uint16_t *>(sm + S_A) + i0 * DV + v;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float gt = __uint_as_float(p.gate_bf16 ? graw[c] << 16 : graw[c]);
-                    sg[c] = __frcp_rn(1.0f + __expf(-gt));
+                    for (int c = 0; c < 16; ++c)
+                        sg[c] = __frcp_rn(1.0f + __expf(-__uint_as_float((uint32_t)gs[c * DV] << 16)));
+                } else {
+                    const float *gp = reinterpret_cast<const float *>(p.gate) + ((size_t)(bos + t0) * H + h) * DV + v;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        sg[c] = __frcp_rn(1.0f + __expf(-__ldg(gp + (size_t)min(i0 + c, cn - 1) * H * DV)));
                 }
                 __syncthreads();
                 // lane l forms 1 / rms of row l % 16 once; the others take it by shuffle
@@ -1066,6 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(drain_bar);  // arrives once the tensor-core work already issued has drained
             if (v_pending >= 0) mbar_wait(tma_bar, (uint32_t)(v_pending & 1), kPolls);  // V copy in flight
             if (g_pending >= 0) mbar_wait(gt_bar, (uint32_t)(g_pending & 1), kPolls);   // g copy in flight
+            if (q_pending >= 0) mbar_wait(gate_bar, (uint32_t)(q_pending & 1), kPolls);  // gate copy in flight
         }
         __syncthreads();
         mbar_wait(drain_bar, 0, kPolls);
@@ -1159,6 +1170,21 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
             return KDA_ERR_CUDA;
         }
     }
+    // fused norm with a bf16 gate: the gate tile of a chunk by one TMA copy; otherwise the
+    // map is not read (V's map stands in)
+    CUtensorMap tmap_gate = tmap;
+    if (p_in.gate && p_in.gate_bf16) {
+        const cuuint64_t qdims[3] = {(cuuint64_t)DV, (cuuint64_t)p_in.H, (cuuint64_t)rows};
+        const cuuint64_t qstrides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)p_in.H * DV * 2};
+        const cuuint32_t qbox[3] = {(cuuint32_t)DV, 1, (cuuint32_t)C};
+        cres = enc(&tmap_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p_in.gate), qdims, qstrides,
+                   qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cres != CUDA_SUCCESS) {
+            set_error("chunk_tc: cuTensorMapEncodeTiled failed for the gate (%d)", (int)cres);
+            return KDA_ERR_CUDA;
+        }
+    }
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     tp.p = p_in;
@@ -1191,7 +1217,7 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
     }
     auto kern = p_in.g_logits ? (p_in.gate ? chunk_tc_kernel<true, true> : chunk_tc_kernel<true, false>)
                               : (p_in.gate ? chunk_tc_kernel<false, true> : chunk_tc_kernel<false, false>);
-    kern<<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tp);
+    kern<<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tmap_gate, tp);
     note_launch();
     return check_launch("chunk_tc_kernel");
 }

@@ -215,20 +215,6 @@ __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
-// Read-only global loads of raw bits into a 32-bit register (a 16-bit value zero-
-// extended), ordered before any later memory access of the thread.
-__device__ __forceinline__ uint32_t ld_nc_u16(const uint16_t *ptr) {
-    uint32_t x;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(x) : "l"(ptr) : "memory");
-    return x;
-}
-
-__device__ __forceinline__ uint32_t ld_nc_u32(const uint32_t *ptr) {
-    uint32_t x;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(x) : "l"(ptr) : "memory");
-    return x;
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
