@@ -36,6 +36,7 @@ STATE_BYTES = 128 * 128 * 4
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256 + 512  # + gate bf16, y fp32
 PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits bf16 + beta logit bf16 + o fp32
 PREFILL_NORM_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 256  # q,k,v bf16 + g fp32 + beta + gate bf16 + y bf16
+PREFILL_LONG_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 512  # q,k,v bf16 + g fp32 + beta + gate bf16 + y fp32
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work from one
 # ncu capture summarised under profiles/, valid only for the kernel source it was
@@ -46,33 +47,33 @@ MEASURED_TRAFFIC = {
     "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
                 "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
                 "bytes_per_unit": (328.259712e6 - 6.291456e6) / (2048 * 96),
-                "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
+                "capture": "ncu, B=1 T=2048 H=96, g and beta given"},
     # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture, mean of two
     # launches: (274.432128 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
                        "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
                        "bytes_per_unit": (274.432128e6 - 6.291456e6) / (2048 * 96),
-                       "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
+                       "capture": "ncu, B=1 T=2048 H=96, bf16 logits"},
     # the same kernel with the fused gated norm (bf16 gate in, bf16 y out), B=1 T=2048 H=96
     # capture, mean of two launches: (343.342848 MB - 6.29 MB of final state) / (2048 * 96)
     "prefill_norm": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
                      "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
                      "bytes_per_unit": (343.342848e6 - 6.291456e6) / (2048 * 96),
-                     "capture": "profiles/chunk_tc_kernel_prefill_T2048.md"},
+                     "capture": "ncu, B=1 T=2048 H=96, fused gated norm"},
     # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
                "sha256": "ede5158c131edfc4a652ea4d3a646abd27d6ef5093fa3bf7fdd0920d87253ef4",
                "bytes_per_unit": 754.843776e6 / (64 * 96),
-               "capture": "profiles/decode_kernel_B64.md"},
+               "capture": "ncu, decode B=64 H=96"},
     # full-size captures: mean of two launches per (token, channel) element
     "conv_prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
                      "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
                      "bytes_per_unit": 1179.379712e6 / (8192 * 36864),
-                     "capture": "profiles/short_conv_kernels.md"},
+                     "capture": "ncu, full size"},
     "conv_decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
                     "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
                     "bytes_per_unit": 204.395008e6 / (256 * 36864),
-                    "capture": "profiles/short_conv_kernels.md"},
+                    "capture": "ncu, full size"},
 }
 
 
@@ -263,6 +264,56 @@ def bench_prefill(args, world, rank, peaks):
                    "parallelism": f"replicas x{world}"},
     }
     return out, d
+
+
+def bench_prefill_workload(args, world, peaks, name):
+    """A full-size prefill workload timed in the launch configuration its parity test uses:
+    "varlen" = 8 packed sequences, lengths log-uniform in [512, 16384], each with an fp32
+    initial state N(0, 0.02^2) and its own final state, fp32 o; "long" = B=2, T=65536 with
+    the fused sigmoid-gated RMSNorm (bf16 gate in, fp32 y out, o not written) and the
+    final states."""
+    import torch
+    import kimi_delta_attention_gated_gb300 as kda
+    from kimi_delta_attention_gated_gb300.inputs import make_inputs
+    d = make_inputs(name, device="cuda")
+    B, T, H, K, V, N = d["B"], d["T"], d["H"], d["K"], d["V"], d["N"]
+    fs = torch.empty((N, H, K, V), device="cuda", dtype=torch.float32)
+    th = B * T * H
+    if name == "varlen":
+        o = torch.empty((B, T, H, V), device="cuda", dtype=torch.float32)
+        cu = d["cu_seqlens"]
+        fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], scale=d["scale"],
+                                   chunk=64, cu_seqlens=cu, o=o, final_state=fs, mode=args.mode)
+        per_th, state_bytes = PREFILL_BYTES_PER_TH, 2 * N * H * STATE_BYTES
+        lens = (cu[1:] - cu[:-1]).tolist()
+        workload = f"varlen prefill, {N} packed sequences of {lens} tokens ({T} total), H={H} d={K}, fp32 initial " \
+                   "and final states, fp32 o"
+        traffic = measured_traffic("prefill", th, state_bytes)
+    else:
+        y = torch.empty((B, T, H * V), device="cuda", dtype=torch.float32)
+        fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, scale=d["scale"], chunk=64,
+                                   gate=d["gate"], norm_w=d["norm_w"], eps=d["eps"], return_o=False, y=y,
+                                   final_state=fs, mode=args.mode)
+        per_th, state_bytes = PREFILL_LONG_BYTES_PER_TH, N * H * STATE_BYTES
+        workload = f"long prefill B={B} T={T} H={H} d={K} + fused sigmoid-gated RMSNorm (bf16 gate, fp32 y, o not " \
+                   "written), final states"
+        traffic = None
+    steps = max(3, args.steps // (4 if name == "long" else 1))
+    r = time_steps(fn, steps, args.warmup, world)
+    launches_per_step = max(1, r["launches"] // steps)
+    kernel_ms = r["call_ms"] / launches_per_step
+    algo_bytes = th * per_th + state_bytes
+    achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+    tflops = th * PREFILL_FLOP_PER_TH / (kernel_ms * 1e-3) / 1e12
+    return {"metric": "KDA prefill tokens/s", "value": world * B * T / (r["ms_per_step"] * 1e-3), "unit": "tokens/s",
+            "ms_per_step": r["ms_per_step"], "steps": steps, "gpu_launches": r["launches"],
+            "config": {"workload": workload, "l2_flush": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
+                         "peak_source": peaks["source"]},
+            "roofline_tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": tflops / peaks["bf16_tflops"]}}
 
 
 def bench_decode(args, world, peaks):
@@ -533,7 +584,8 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits", "norm"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits", "norm", "varlen",
+                                       "long"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
@@ -543,6 +595,7 @@ def main():
     ap.add_argument("--no-logits", action="store_true")
     ap.add_argument("--no-norm", action="store_true")
     ap.add_argument("--no-oproj", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the varlen and long prefill workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -557,8 +610,10 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "conv", "kernels", "logits", "norm"):
-        if args.only == "kernels":  # decode step + short convolution (profiling runs)
+    if args.only in ("decode", "conv", "kernels", "logits", "norm", "varlen", "long"):
+        if args.only in ("varlen", "long"):
+            res = bench_prefill_workload(args, world, peaks, args.only)
+        elif args.only == "kernels":  # decode step + short convolution (profiling runs)
             res = {"decode": bench_decode(args, world, peaks), "short_conv": bench_short_conv(args, world, peaks)}
         elif args.only == "logits":  # the prefill with gates from logits alone (profiling runs)
             res = bench_prefill_logits(args, world, peaks)
@@ -575,6 +630,10 @@ def main():
     logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
     norm = None if (args.no_norm or args.only == "prefill") else bench_prefill_norm(args, world, peaks)
     oproj = None if (args.no_oproj or args.only == "prefill") else bench_o_proj(args, world, peaks)
+    varlen = long_ = None
+    if not (args.no_workloads or args.only == "prefill"):
+        varlen = bench_prefill_workload(args, world, peaks, "varlen")
+        long_ = bench_prefill_workload(args, world, peaks, "long")
     e2e = None if (args.no_e2e or args.only == "prefill") else bench_e2e(args, world, d)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
@@ -591,9 +650,32 @@ def main():
         "roofline": pre["roofline"], "roofline_tensor": pre["roofline_tensor"], "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
         "short_conv": conv, "prefill_gate_logits": logits, "prefill_gated_norm": norm, "o_proj": oproj,
-        "gpu": torch.cuda.get_device_name(),
+        "prefill_varlen": varlen, "prefill_long_norm": long_, "gpu": torch.cuda.get_device_name(),
     }
+    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj)
     print(json.dumps(line), flush=True)
+
+
+def summary(pre, dec, varlen, long_, logits, norm, conv, oproj):
+    """Every timed workload in a few numbers, last on the line so that a reader of the
+    line's tail sees all of them: kernel ms per launch, throughput and the fraction of
+    the binding roofline (of the measured peak)."""
+    def row(r, unit_scale, unit):
+        if r is None:
+            return None
+        f = r["roofline"]
+        return {"kernel_ms": round(f["kernel_ms"], 4), unit: round(r["value"] / unit_scale, 3),
+                "frac": round(f["frac"], 4), "bound": f["bound"]}
+    out = {"prefill_T8192": row(pre, 1e6, "Mtok_s"), "prefill_varlen": row(varlen, 1e6, "Mtok_s"),
+           "prefill_long_norm": row(long_, 1e6, "Mtok_s"), "decode_B256": row(dec, 1e3, "Ktok_s"),
+           "prefill_logits": row(logits, 1e6, "Mtok_s"), "prefill_norm_bf16": row(norm, 1e6, "Mtok_s")}
+    if conv:
+        out["conv_prefill"] = row(conv["conv_prefill"], 1e6, "Mtok_s")
+        out["conv_decode"] = row(conv["conv_decode"], 1e6, "Mtok_s")
+    if oproj:
+        out["o_proj_256"] = row(oproj["decode"], 1e6, "Mtok_s")
+        out["o_proj_8192"] = row(oproj["prefill"], 1e6, "Mtok_s")
+    return {k: v for k, v in out.items() if v is not None}
 
 
 if __name__ == "__main__":

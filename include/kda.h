@@ -61,7 +61,7 @@ typedef enum kda_status {
     KDA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad cu_seqlens */
     KDA_ERR_UNSUPPORTED = 2,  /* well-formed but not built (dims, dtype, chunk, mode) */
     KDA_ERR_CUDA = 3,         /* a CUDA runtime / launch error */
-    KDA_ERR_TIMEOUT = 4       /* reserved: a bounded device wait gave up */
+    KDA_ERR_TIMEOUT = 4       /* a bounded device wait gave up (returned by kda_device_status) */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -86,6 +86,39 @@ const char *kda_status_string(int status);
 
 /* Number of kernels this library has launched in this process (all threads). */
 uint64_t kda_launch_count(void);
+
+/*
+ * kda_device_status -- failures detected on the device since the last call.
+ *
+ * Every wait inside the kernels (on a bulk or TMA copy, or on the tensor core) is
+ * bounded.  A CTA whose wait gives up lets the copies it started land, writes NaN
+ * into every output it was responsible for (the state, o and y of its (sequence,
+ * head) units, or the y and state rows of its convolution tiles; a decode CTA also
+ * poisons every later unit it owned), and counts the event in a device-side counter.
+ * The compute calls are asynchronous and cannot see this, so this call synchronises
+ * `stream` (a cudaStream_t; NULL = the legacy default stream), reads the counters of
+ * the current device and clears them.  Returns KDA_ERR_TIMEOUT if any wait gave up
+ * (kda_last_error() names the kernels and counts), KDA_ERR_CUDA if the stream or a
+ * counter read failed, KDA_OK otherwise.  The counters are shared by all streams of
+ * the device: call it when the work to be checked has been enqueued on `stream` or
+ * has finished.  No counterpart on the pages: it is the library's failure detection.
+ */
+kda_status kda_device_status(void *stream);
+
+/*
+ * kda_set_wait_limit -- bound on the first-line waits of the streaming kernels.
+ *
+ * The decode step's copy waits (kda_recurrent_step, kda_recurrent_step_logits with
+ * K = V = 128) and the short convolution's tile waits (kda_short_conv_fwd over a
+ * prompt) poll their mbarrier at most this many times before they give up, for the
+ * calls made after this one (process-wide).  polls < 0 restores the default (2^26);
+ * 0 makes every such wait give up at once, which tests of the failure handling use
+ * (kda_device_status then reports KDA_ERR_TIMEOUT and the outputs hold NaN).  The
+ * waits that let copies in flight land before a CTA exits, and the tensor-core
+ * waits of the chunked prefill, always keep their full bound.  Returns KDA_OK, or
+ * KDA_ERR_INVALID_ARG above 2^32 - 1.  No counterpart on the pages.
+ */
+kda_status kda_set_wait_limit(int64_t polls);
 
 /*
  * kda_chunk_fwd -- chunked prefill over whole prompts.

@@ -23,7 +23,7 @@ import threading
 import torch
 
 __all__ = ["chunk_fwd", "chunk_fwd_logits", "recurrent_fwd", "recurrent_step", "recurrent_step_logits",
-           "gated_rmsnorm", "short_conv", "o_proj", "launch_count",
+           "gated_rmsnorm", "short_conv", "o_proj", "launch_count", "device_status", "set_wait_limit",
            "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +74,10 @@ def _load():
         for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
                    "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits", "kda_o_proj"):
             getattr(lib, fn).restype = ctypes.c_int
+        lib.kda_device_status.argtypes = [P]
+        lib.kda_device_status.restype = ctypes.c_int
+        lib.kda_set_wait_limit.argtypes = [ctypes.c_int64]
+        lib.kda_set_wait_limit.restype = ctypes.c_int
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_launch_count.restype = ctypes.c_uint64
         lib.kda_version.restype = ctypes.c_int
@@ -89,6 +93,20 @@ def _check(status: int):
 def launch_count() -> int:
     """Kernels libkda has launched in this process."""
     return int(_load().kda_launch_count())
+
+
+def device_status(stream=None):
+    """Synchronise the stream (default: the current one) and raise KDAError with
+    KDA_ERR_TIMEOUT if a bounded wait inside a kernel gave up since the last check
+    (those outputs hold NaN).  Clears the device's counters."""
+    st = ctypes.c_void_p((stream or torch.cuda.current_stream()).cuda_stream)
+    _check(_load().kda_device_status(st))
+
+
+def set_wait_limit(polls):
+    """Bound on the streaming kernels' first-line waits (None or a negative value: the
+    default; 0: every such wait gives up at once, for tests of the failure handling)."""
+    _check(_load().kda_set_wait_limit(-1 if polls is None else int(polls)))
 
 
 def _dt(t: torch.Tensor) -> int:

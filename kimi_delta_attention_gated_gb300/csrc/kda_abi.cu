@@ -14,8 +14,20 @@ namespace kda {
 namespace {
 thread_local char g_err[512] = "";
 std::atomic<uint64_t> g_launches{0};
-constexpr int kVersion = 10000;  // 1.0.0
+std::atomic<uint32_t> g_wait_polls{kDefaultWaitPolls};
+constexpr int kVersion = 10100;  // 1.1.0
 }  // namespace
+
+uint32_t wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return dev;
+}
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -54,6 +66,64 @@ bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
             return code;             \
         }                            \
     } while (0)
+
+// A byte range of one argument, for the overlap checks.
+struct Span {
+    const void *p;
+    size_t bytes;
+    const char *name;
+};
+
+bool overlaps(const Span &a, const Span &b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const char *x = static_cast<const char *>(a.p), *y = static_cast<const char *>(b.p);
+    return x < y + b.bytes && y < x + a.bytes;
+}
+
+// The kernels read their inputs chunk by chunk while they write their outputs, so no
+// output may share bytes with an input or with another output.  The one exception is
+// the state: final_state may be initial_state itself (the same pointer), never a
+// partial overlap.  Returns the first offending pair in the error message.
+kda_status check_overlaps(const char *fn, const Span *in, int n_in, const Span *out, int n_out, const Span &s0,
+                          const Span &sT) {
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < n_in; ++j)
+            KDA_REQUIRE(!overlaps(out[i], in[j]), KDA_ERR_INVALID_ARG, "%s: %s must not overlap %s", fn, out[i].name,
+                        in[j].name);
+        for (int j = i + 1; j < n_out; ++j)
+            KDA_REQUIRE(!overlaps(out[i], out[j]), KDA_ERR_INVALID_ARG, "%s: %s must not overlap %s", fn,
+                        out[i].name, out[j].name);
+        KDA_REQUIRE(!overlaps(out[i], s0) && !overlaps(out[i], sT), KDA_ERR_INVALID_ARG,
+                    "%s: %s must not overlap the state", fn, out[i].name);
+    }
+    for (int j = 0; j < n_in; ++j)
+        KDA_REQUIRE(!overlaps(sT, in[j]), KDA_ERR_INVALID_ARG, "%s: the final state must not overlap %s", fn,
+                    in[j].name);
+    KDA_REQUIRE(!overlaps(s0, sT) || s0.p == sT.p, KDA_ERR_INVALID_ARG,
+                "%s: final_state may be initial_state itself but must not partly overlap it", fn);
+    return KDA_OK;
+}
+
+size_t esize(int dtype) { return dtype == KDA_BF16 ? 2 : 4; }
+
+// Overlap check of one prefill / decode call: rows tokens, N sequences.
+kda_status check_call_overlaps(const char *fn, const void *q, const void *k, const void *v, int qkv_dtype,
+                               const void *g, size_t g_esz, const void *beta, size_t b_esz, const float *s0,
+                               const float *sT, const void *o, int o_dtype, const float *states, const void *gate,
+                               int gate_dtype, const float *norm_w, const void *y, int64_t rows, int N, int H, int K,
+                               int V) {
+    const size_t r = (size_t)rows, hk = (size_t)H * K, hv = (size_t)H * V, st = (size_t)N * H * K * V * 4;
+    const Span in[] = {{q, r * hk * esize(qkv_dtype), "q"}, {k, r * hk * esize(qkv_dtype), "k"},
+                       {v, r * hv * esize(qkv_dtype), "v"}, {g, r * hk * g_esz, "g"},
+                       {beta, r * H * b_esz, "beta"},      {gate, gate ? r * hv * esize(gate_dtype) : 0, "gate"},
+                       {norm_w, norm_w ? (size_t)V * 4 : 0, "norm_w"}};
+    const Span out[] = {{o, r * hv * esize(o_dtype), "o"},
+                        {y, y ? r * hv * esize(o_dtype) : 0, "y"},
+                        {states, states ? r * hk * V * 4 : 0, "states"}};
+    return check_overlaps(fn, in, 7, out, 3, Span{s0, s0 ? st : 0, "initial_state"},
+                          Span{sT, sT ? st : 0, "final_state"});
+}
+
 
 // Checks shared by the prefill entry points; fills the sequence count.
 kda_status check_seq_args(const char *fn, const void *q, const void *k, const void *v, int qkv_dtype,
@@ -136,6 +206,7 @@ kda::SeqParams make_params(const void *q, const void *k, const void *v, int qkv_
     p.qkv_bf16 = qkv_dtype == KDA_BF16;
     p.o_bf16 = o_dtype == KDA_BF16;
     p.gate_bf16 = gate_dtype == KDA_BF16;
+    p.polls = kda::wait_polls();
     return p;
 }
 
@@ -188,6 +259,10 @@ kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *
                                   norm_w, eps, y, N);
     if (s != KDA_OK) return s;
     if (gl && (s = check_logits(fn, *gl, (int64_t)B * T == 0)) != KDA_OK) return s;
+    s = check_call_overlaps(fn, q, k, v, qkv_dtype, gchk, gl ? esize(gl->z_dtype) : 4, bchk,
+                            gl ? esize(gl->b_dtype) : 4, initial_state, final_state, o, o_dtype, nullptr, gate,
+                            gate_dtype, norm_w, y, (int64_t)B * T, N, H, K, V);
+    if (s != KDA_OK) return s;
     KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, KDA_ERR_UNSUPPORTED, "%s: chunk=%d (supported: 16, 32, 64)",
                 fn, chunk);
     KDA_REQUIRE(mode == KDA_MODE_AUTO || mode == KDA_MODE_TENSOR || mode == KDA_MODE_FP32, KDA_ERR_INVALID_ARG,
@@ -231,6 +306,10 @@ kda_status step_impl(const char *fn, const void *q, const void *k, const void *v
                                   nullptr, 0, B, 1, H, K, V, scale, gate, gate_dtype, norm_w, eps, y, N);
     if (s != KDA_OK) return s;
     if (gl && (s = check_logits(fn, *gl, false)) != KDA_OK) return s;
+    s = check_call_overlaps(fn, q, k, v, qkv_dtype, gchk, gl ? esize(gl->z_dtype) : 4, bchk,
+                            gl ? esize(gl->b_dtype) : 4, state_in, state_out, o, o_dtype, nullptr, gate, gate_dtype,
+                            norm_w, y, B, N, H, K, V);
+    if (s != KDA_OK) return s;
     kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, state_in, state_out, o, o_dtype, nullptr, nullptr, N,
                                    1, H, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y);
     set_logits(p, gl, K);
@@ -257,6 +336,35 @@ const char *kda_status_string(int s) {
 }
 
 uint64_t kda_launch_count(void) { return kda::g_launches.load(std::memory_order_relaxed); }
+
+kda_status kda_device_status(void *stream) {
+    kda::g_err[0] = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        set_error("kda_device_status: the stream failed: %s", cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    const int n_tc = kda::take_chunk_tc_timeouts(st);
+    const int n_dec = kda::take_decode_timeouts(st);
+    const int n_conv = kda::take_short_conv_timeouts(st);
+    if (n_tc < 0 || n_dec < 0 || n_conv < 0) return KDA_ERR_CUDA;
+    if (n_tc + n_dec + n_conv > 0) {
+        set_error("kda_device_status: bounded waits gave up in %d prefill, %d decode and %d short-convolution "
+                  "CTAs; their outputs hold NaN",
+                  n_tc, n_dec, n_conv);
+        return KDA_ERR_TIMEOUT;
+    }
+    return KDA_OK;
+}
+
+kda_status kda_set_wait_limit(int64_t polls) {
+    kda::g_err[0] = 0;
+    KDA_REQUIRE(polls <= (int64_t)UINT32_MAX, KDA_ERR_INVALID_ARG, "kda_set_wait_limit: at most %u polls",
+                UINT32_MAX);
+    kda::g_wait_polls.store(polls < 0 ? kda::kDefaultWaitPolls : (uint32_t)polls, std::memory_order_relaxed);
+    return KDA_OK;
+}
 
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
                          const float *g, const float *beta, const float *initial_state,
@@ -299,6 +407,9 @@ kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, kda_dt
                                   H, K, V, scale, gate, gate_dtype, norm_w, eps, y, N);
     if (s != KDA_OK) return s;
     KDA_REQUIRE(!states || aligned16(states), KDA_ERR_INVALID_ARG, "kda_recurrent_fwd: states must be 16-byte aligned");
+    s = check_call_overlaps("kda_recurrent_fwd", q, k, v, qkv_dtype, g, 4, beta, 4, initial_state, final_state, o,
+                            o_dtype, states, gate, gate_dtype, norm_w, y, (int64_t)B * T, N, H, K, V);
+    if (s != KDA_OK) return s;
     kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o, o_dtype,
                                    states, cu_seqlens, N, T, H, scale, use_qk_l2norm, gate, gate_dtype,
                                    norm_w, eps, y);

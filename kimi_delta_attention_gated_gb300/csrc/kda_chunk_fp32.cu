@@ -217,8 +217,9 @@ kda_status launch_kc(const SeqParams &p, int V, const int *order, cudaStream_t s
     using L = Smem<K, C>;
     const int units = p.N * p.H;
     if (units == 0) return KDA_OK;
-    static bool configured = false;  // benign race: the attribute call is idempotent
-    if (!configured) {
+    static DeviceOnce configured;  // benign race: the attribute call is idempotent
+    const int dev = current_device();
+    if (!configured.done(dev)) {
         cudaError_t e = cudaFuncSetAttribute(chunk_fp32_kernel<K, C>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
         if (e != cudaSuccess) {
@@ -226,7 +227,7 @@ kda_status launch_kc(const SeqParams &p, int V, const int *order, cudaStream_t s
                       cudaGetErrorString(e));
             return KDA_ERR_CUDA;
         }
-        configured = true;
+        configured.set(dev);
     }
     chunk_fp32_kernel<K, C><<<units * (V / VS), kThreads, L::bytes, st>>>(p, V, order);
     note_launch();

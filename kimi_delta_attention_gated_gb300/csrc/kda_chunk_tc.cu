@@ -110,7 +110,7 @@ static_assert(S_A % 1024 == 0 && S_SMALL % 16 == 0, "alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Set by a CTA whose bounded wait on the tensor core or the TMA gave up; that CTA
-// also writes NaN into its final state so the failure cannot pass unnoticed.
+// also writes NaN into its final state, o and y so the failure cannot pass unnoticed.
 __device__ int g_chunk_tc_timeouts = 0;
 
 struct TcParams {
@@ -1080,8 +1080,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         mbar_wait(drain_bar, 0, kPolls);
+        const float nan = __int_as_float(0x7fc00000);
         if (p.sT)
-            for (int e = tid; e < DK * DV; e += kThreads) p.sT[(size_t)unit * DK * DV + e] = __int_as_float(0x7fc00000);
+            for (int e = tid; e < DK * DV; e += kThreads) p.sT[(size_t)unit * DK * DV + e] = nan;
+        for (int e = tid; e < len * DV; e += kThreads) {  // every row of this (sequence, head)
+            const size_t idx = ((size_t)(bos + e / DV) * H + h) * DV + e % DV;
+            if (p.o) st_out(p.o, idx, nan, p.o_bf16);
+            if (NORM) st_out(p.y, idx, nan, p.o_bf16);
+        }
     } else if (p.sT) {  // final state: S[c][v] from S^T (lane v, column c)
         uint32_t s1[16], s2[16];
         const int c0 = wg * 32;
@@ -1121,6 +1127,20 @@ void *tensor_map_encoder() {
             fn = ptr;
     }
     return fn;
+}
+
+int take_chunk_tc_timeouts(cudaStream_t st) {
+    int n = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&n, g_chunk_tc_timeouts, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_chunk_tc_timeouts, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        set_error("chunk_tc: cannot read the timeout counter: %s", cudaGetErrorString(cudaGetLastError()));
+        return -1;
+    }
+    return n;
 }
 
 bool chunk_tc_supported(int K, int V, int chunk) { return K == DK && V == DV && chunk == C; }
@@ -1203,8 +1223,9 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
             tp.order[j + 1] = x;
         }
     }
-    static bool configured = false;
-    if (!configured) {
+    static DeviceOnce configured;
+    const int dev = current_device();
+    if (!configured.done(dev)) {
         for (void *fn : {(void *)chunk_tc_kernel<false, false>, (void *)chunk_tc_kernel<true, false>,
                          (void *)chunk_tc_kernel<false, true>, (void *)chunk_tc_kernel<true, true>}) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -1213,7 +1234,7 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
                 return KDA_ERR_CUDA;
             }
         }
-        configured = true;
+        configured.set(dev);
     }
     auto kern = p_in.g_logits ? (p_in.gate ? chunk_tc_kernel<true, true> : chunk_tc_kernel<true, false>)
                               : (p_in.gate ? chunk_tc_kernel<false, true> : chunk_tc_kernel<false, false>);

@@ -20,6 +20,32 @@ void note_launch(int n = 1);
 // Turns a pending CUDA error into KDA_ERR_CUDA with a message naming `what`.
 kda_status check_launch(const char *what);
 
+// Bound (in polls) on the first-line waits of the streaming kernels (decode step, short
+// convolution): kDefaultWaitPolls unless kda_set_wait_limit changed it.  The waits that
+// drain copies still in flight before a CTA exits always keep the default.
+constexpr uint32_t kDefaultWaitPolls = 1u << 26;
+uint32_t wait_polls();
+
+// The current device, or 0 if it cannot be read.
+int current_device();
+
+// A one-time setup done once per device (devices 0-63; above that it runs every time):
+// kernel attributes such as the dynamic shared-memory limit belong to one device.
+struct DeviceOnce {
+    unsigned long long bits = 0;  // guarded by the caller's idempotent setup: a race repeats it
+    bool done(int dev) const { return dev >= 0 && dev < 64 && ((bits >> dev) & 1ull); }
+    void set(int dev) {
+        if (dev >= 0 && dev < 64) __atomic_fetch_or(&bits, 1ull << dev, __ATOMIC_RELAXED);
+    }
+};
+
+// Device-side timeout counters of each translation unit, read and cleared on `st`
+// (after it has drained) for the current device; each returns the count it took, or -1
+// with the error message set when CUDA fails.
+int take_chunk_tc_timeouts(cudaStream_t st);
+int take_decode_timeouts(cudaStream_t st);
+int take_short_conv_timeouts(cudaStream_t st);
+
 // ---------------------------------------------------------------------------
 // parameter blocks
 
@@ -49,6 +75,7 @@ struct SeqParams {
     const void *beta_logits;     // [rows, H] or null
     float g_lower;               // -inf: no floor
     int g_logits_bf16, beta_logits_bf16;
+    uint32_t polls;              // bound on the streaming kernels' first-line waits (wait_polls())
 };
 
 // Token range of sequence n, clamped to [0, T] so a bad cu_seqlens cannot
@@ -80,9 +107,11 @@ __device__ __forceinline__ void st_out(void *base, size_t idx, float x, int is_b
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
 
-// softplus(x) = log(1 + e^x) as max(x, 0) + log(1 + e^-|x|); below x = -16.6 the second
-// term rounds to 0 (absolute error under 6e-8).
-__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x))); }
+// softplus(x) = log(1 + e^x) as max(x, 0) + log1p(e^-|x|).  log1pf keeps the relative
+// accuracy of the second term where e^-|x| is small (the decay logits sit near -4, where
+// log(1 + t) formed from a rounded 1 + t and the fast logarithm loses up to 1e-3 of it);
+// the result is then as accurate as the fast exponential, a few fp32 ulps.
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))); }
 
 // g of one key channel from its logit z (bias not yet added); a_h = exp(A_log[h]).
 __device__ __forceinline__ float gate_of_logit(float x, float a_h, float lower) { return fmaxf(lower, -a_h * softplus_f(x)); }

@@ -48,13 +48,15 @@ __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const void *o, 
 }  // namespace
 
 int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 1;
+    static int counts[64] = {0};  // per device; a race only repeats the query
+    const int dev = current_device();
+    if (dev >= 0 && dev < 64 && counts[dev] > 0) return counts[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = 1;
     }
+    if (dev >= 0 && dev < 64) counts[dev] = n;
     return n;
 }
 

@@ -239,7 +239,8 @@ struct DecodeSmem {
     static constexpr uint32_t bytes = bar + NS * 8;
 };
 
-// Set by a CTA whose bounded wait on its copies gave up; that unit's state becomes NaN.
+// Set by a CTA whose bounded wait on its copies gave up; that unit and every later unit
+// the CTA owned get NaN in their state, o and y.
 __device__ int g_decode_timeouts = 0;
 
 __device__ __forceinline__ float in_elem(const uint8_t *base, int i, int is_bf16) {
@@ -308,12 +309,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
     for (; u < units; u += stride, ++it) {
         const int st = it % NS;
         const uint8_t *buf = dsm + (uint32_t)st * kStage;
-        failed = __syncthreads_or(!tc::mbar_wait(bars + st, (uint32_t)((it / NS) & 1), kDecodePolls));
-        if (failed) {  // the copies never arrived: poison this unit's state and stop
-            if (tid == 0) atomicAdd(&g_decode_timeouts, 1);
-            for (int e = tid; e < kDK * kDK; e += NT) p.sT[(size_t)u * kDK * kDK + e] = __int_as_float(0x7fc00000);
-            break;
-        }
+        failed = __syncthreads_or(!tc::mbar_wait(bars + st, (uint32_t)((it / NS) & 1), p.polls));
+        if (failed) break;  // the copies did not arrive in time: this unit and the rest are poisoned below
         float s[RPW][VPL];
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
@@ -430,13 +427,27 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
         db_cur = db_next;
         __syncthreads();  // shared arrays are rewritten by the next unit
     }
-    // after a failure: give the copies still in flight (iterations it .. it + NS - 1) their
-    // bounded time before exiting
-    if (failed && tid == 0)
+    if (!failed) return;
+    // After a failure: the copies still in flight (iterations it .. it + NS - 1) get their
+    // full bounded time to land, then unit u and every later unit of this CTA is poisoned,
+    // so that no output of the call keeps an old value that would pass for a result (with
+    // the state updated in place, an unwritten unit would still hold its previous state).
+    if (tid == 0) {
+        atomicAdd(&g_decode_timeouts, 1);
         for (int k = 0; k < NS; ++k) {
             const int j = it + k, uj = blockIdx.x + j * stride;
             if (uj < units) tc::mbar_wait(bars + j % NS, (uint32_t)((j / NS) & 1), kDecodePolls);
         }
+    }
+    __syncthreads();
+    const float nan = __int_as_float(0x7fc00000);
+    for (; u < units; u += stride) {
+        for (int e = tid; e < kDK * kDK; e += NT) p.sT[(size_t)u * kDK * kDK + e] = nan;
+        if (tid < kDK) {
+            if (p.o) st_out(p.o, (size_t)u * kDK + tid, nan, p.o_bf16);
+            if (p.gate) st_out(p.y, (size_t)u * kDK + tid, nan, p.o_bf16);
+        }
+    }
 }
 
 // Decode configuration: NW warps per CTA, NS staging buffers (CTAs per SM follow from
@@ -451,8 +462,9 @@ kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
     if (units == 0) return KDA_OK;
     if (K == kDK && V == kDK && p.T == 1 && !p.cu_seqlens && !p.states && p.sT) {
         using L = DecodeSmem<kDecNW, kDecNS>;
-        static bool configured = false;
-        if (!configured) {
+        static DeviceOnce configured;
+        const int dev = current_device();
+        if (!configured.done(dev)) {
             for (void *fn : {(void *)decode_kernel<false, kDecNW, kDecNS>, (void *)decode_kernel<true, kDecNW, kDecNS>}) {
                 const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::bytes);
                 if (e != cudaSuccess) {
@@ -460,7 +472,7 @@ kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
                     return KDA_ERR_CUDA;
                 }
             }
-            configured = true;
+            configured.set(dev);
         }
         const int per_sm = kDecNW == 8 ? 2 : 1;
         const int grid = units < per_sm * sm_count() ? units : per_sm * sm_count();
@@ -480,6 +492,18 @@ kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
 }
 
 }  // namespace
+
+int take_decode_timeouts(cudaStream_t st) {
+    int n = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&n, g_decode_timeouts, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_decode_timeouts, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        set_error("decode: cannot read the timeout counter: %s", cudaGetErrorString(cudaGetLastError()));
+        return -1;
+    }
+    return n;
+}
 
 kda_status launch_recurrent(const SeqParams &p, int K, int V, cudaStream_t st) {
 #define KDA_CASE(KK, VV) \

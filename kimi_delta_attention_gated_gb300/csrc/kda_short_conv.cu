@@ -42,10 +42,11 @@ constexpr int kTile = 64;    // tokens per tile
 constexpr int kCh = 256;     // channels per tile (the TMA box width)
 constexpr int kVec = 4;      // channels per thread
 constexpr int kTokPer = 16;  // tokens per thread: 64 channel groups x 4 token quarters = 256 threads
-constexpr uint32_t kPolls = 1u << 24;  // bound on the tile's mbarrier wait
+constexpr uint32_t kPolls = 1u << 24;  // bound on the wait that drains a tile still in flight
 static_assert((kCh / kVec) * (kTile / kTokPer) == kThreads && kVec == 4, "thread map");
 
-// Set by a CTA whose wait for its TMA tile gave up (its outputs are then NaN).
+// Set by a CTA whose wait for its TMA tile gave up (its outputs, and the state of every
+// sequence ending in one of its remaining tiles, are then NaN).
 __device__ int g_short_conv_timeouts = 0;
 
 struct ConvParams {
@@ -58,6 +59,7 @@ struct ConvParams {
     const int32_t *cu;  // [N + 1] device or null (dense: sequence n = rows [n T, n T + T))
     int64_t rows;       // packed tokens
     int N, T, D, act;
+    uint32_t polls;     // bound on the wait for each tile
 };
 
 __device__ __forceinline__ int64_t clamp_row(int64_t v, int64_t rows) { return v < 0 ? 0 : (v > rows ? rows : v); }
@@ -317,37 +319,57 @@ __global__ void __launch_bounds__(kThreads) short_conv_tile_kernel(const __grid_
 
     int it = 0;
     bool ok = true;
+    int64_t first_bad = n_tiles;
     for (int64_t id = blockIdx.x; id < n_tiles; id += gridDim.x, ++it) {
         const int b = it & 1;
         const uint8_t *tile = smem + b * kBuf;
         const int cb = (int)(id % n_cb);
         const int64_t t0 = (id / n_cb) * kTile;
         const int c0 = cb * kCh + ch;
-        const bool tile_ok = tc::mbar_wait(&bar[b], (uint32_t)((it >> 1) & 1), kPolls);
+        const bool tile_ok = tc::mbar_wait(&bar[b], (uint32_t)((it >> 1) & 1), p.polls);
         if (tile_ok) ++n_seen[b];
-        ok = ok && tile_ok;
         const int64_t ta = t0 + qt * kTokPer;  // this thread's tokens [ta, tb)
         const int64_t t1 = t0 + kTile < p.rows ? t0 + kTile : p.rows;
         const int64_t tb = ta + kTokPer < t1 ? ta + kTokPer : t1;
-        if (c0 < p.D && ta < tb) {
-            if (!tile_ok) {  // the tile never arrived: make the failure visible
-                const float nan4[kVec] = {__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
-                                          __int_as_float(0x7fc00000), __int_as_float(0x7fc00000)};
-                for (int64_t t = ta; t < tb; ++t) st_vec<YB>(p.y, (size_t)t * D + c0, nan4);
-            } else if (p.act) {
+        if (tile_ok && c0 < p.D && ta < tb) {
+            if (p.act)
                 conv_tokens<W, XB, YB, true>(p, tile, t0, ta, tb, ch, c0);
-            } else {
+            else
                 conv_tokens<W, XB, YB, false>(p, tile, t0, ta, tb, ch, c0);
-            }
         }
-        ok = __syncthreads_and(ok);  // every thread is done with buffer b; a timeout anywhere stops the CTA
-        if (!ok) break;
+        ok = __syncthreads_and(tile_ok);  // every thread is done with buffer b; a timeout anywhere stops the CTA
+        if (!ok) {
+            first_bad = id;  // this whole tile is poisoned below, with the rest
+            break;
+        }
         if (tid == 0 && id + 2 * (int64_t)gridDim.x < n_tiles) issue(id + 2 * (int64_t)gridDim.x, b);
     }
-    if (!ok && tid == 0) {  // copies still in flight must land before the CTA exits
+    if (ok) return;
+    // A tile did not arrive in time: the copies still in flight get their full bounded time
+    // to land, then every tile this CTA still owned gets NaN outputs, and so does the state
+    // of each sequence whose last token lies in one of them.
+    if (tid == 0) {
         atomicAdd(&g_short_conv_timeouts, 1);
         for (int b = 0; b < 2; ++b)
             if (n_issued[b] > n_seen[b]) tc::mbar_wait(&bar[b], (uint32_t)(n_seen[b] & 1), kPolls);
+    }
+    __syncthreads();
+    const float nan = __int_as_float(0x7fc00000);
+    const float nan4[kVec] = {nan, nan, nan, nan};
+    for (int64_t id = first_bad; id < n_tiles; id += gridDim.x) {
+        const int c0 = (int)(id % n_cb) * kCh + ch;
+        const int64_t ta = (id / n_cb) * kTile + qt * kTokPer;
+        const int64_t t1 = (id / n_cb) * kTile + kTile < p.rows ? (id / n_cb) * kTile + kTile : p.rows;
+        const int64_t tb = ta + kTokPer < t1 ? ta + kTokPer : t1;
+        if (c0 >= p.D) continue;
+        for (int64_t t = ta; t < tb; ++t) {
+            st_vec<YB>(p.y, (size_t)t * D + c0, nan4);
+            int n;
+            int64_t bos, eos;
+            seq_of(p, t, n, bos, eos);
+            if (p.sT && eos == t + 1)
+                for (int j = 0; j < NH; ++j) st_state(p.sT, ((size_t)n * NH + j) * D + c0, nan4);
+        }
     }
 }
 
@@ -420,15 +442,16 @@ kda_status launch_wxy(const ConvParams &p, cudaStream_t st) {
         }
     }
     const int smem = 2 * (kTile + NH) * kCh * (XB ? 2 : 4);
-    static bool configured = false;
-    if (!configured) {
+    static DeviceOnce configured;
+    const int dev = current_device();
+    if (!configured.done(dev)) {
         const cudaError_t e = cudaFuncSetAttribute(short_conv_tile_kernel<W, XB, YB>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             set_error("short_conv: cannot reserve %d bytes of shared memory: %s", smem, cudaGetErrorString(e));
             return KDA_ERR_CUDA;
         }
-        configured = true;
+        configured.set(dev);
     }
     const int n_cb = (p.D + kCh - 1) / kCh;
     const int64_t n_tiles = tiles * n_cb;
@@ -451,6 +474,20 @@ kda_status launch_w(const ConvParams &p, bool xb, bool yb, cudaStream_t st) {
 
 }  // namespace
 
+int take_short_conv_timeouts(cudaStream_t st) {
+    int n = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&n, g_short_conv_timeouts, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_short_conv_timeouts, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        set_error("short_conv: cannot read the timeout counter: %s", cudaGetErrorString(cudaGetLastError()));
+        return -1;
+    }
+    return n;
+}
+
 kda_status launch_short_conv(const void *x, int x_bf16, const float *w, const float *bias, const float *s0,
                              float *sT, void *y, int y_bf16, const int32_t *cu, int N, int64_t rows, int T,
                              int D, int W, int act, cudaStream_t st) {
@@ -467,6 +504,7 @@ kda_status launch_short_conv(const void *x, int x_bf16, const float *w, const fl
     p.T = T;
     p.D = D;
     p.act = act;
+    p.polls = wait_polls();
     if (rows == 0 && (!sT || N == 0)) return KDA_OK;
     switch (W) {
         case 2: return launch_w<2>(p, x_bf16, y_bf16, st);

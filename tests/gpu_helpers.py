@@ -50,3 +50,19 @@ def oracle_run(d, heads=None, seqs=None, return_states=False):
             raise ValueError("sample varlen inputs by slicing cu_seqlens in the test")
     return oracle.recurrent(q, k, v, g, beta, s0, scale=d["scale"], cu_seqlens=cu,
                             return_states=return_states)
+
+
+def assert_bf16_close(a, ref, c):
+    """A bf16 output against the fp64 oracle, element by element: within the rounding to
+    bf16 (half an ulp is 2^-9 relative; 2^-8 leaves a factor two) plus c * rms(oracle)
+    for the path's own fp32 error before the rounding."""
+    a = np.asarray(a.detach().double().cpu().numpy() if torch.is_tensor(a) else a, np.float64)
+    ref = np.asarray(ref, np.float64)
+    a = a.reshape(ref.shape)
+    assert np.all(np.isfinite(a)), "non-finite values in the CUDA result"
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = 2.0 ** -8 * np.abs(ref) + c * rms
+    excess = np.abs(a - ref) - bound
+    worst = int(np.argmax(excess))
+    assert excess.flat[worst] <= 0, (f"element {np.unravel_index(worst, ref.shape)}: got {a.flat[worst]!r}, "
+                                     f"oracle {ref.flat[worst]!r}, bound {bound.flat[worst]!r}")

@@ -36,7 +36,7 @@ def declared_symbols():
 def test_header_declares_the_entry_points():
     names = declared_symbols()
     for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
-               "kda_short_conv_fwd"):
+               "kda_short_conv_fwd", "kda_device_status", "kda_set_wait_limit"):
         assert fn in names
 
 
@@ -53,9 +53,16 @@ def test_version_and_status_strings(lib):
     assert lib.kda_status_string(99) == b"KDA_ERR_UNKNOWN"
 
 
+SPAN = 1 << 24  # fake tensors of one call lie this far apart, so that none overlaps another
+
+
+def fake(i):
+    return FAKE + i * SPAN
+
+
 def chunk_call(lib, **over):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, qkv=BF16, g=FAKE, beta=FAKE, s0=None, sT=None, o=FAKE, odt=F32,
-             cu=None, cu_host=None, n_seqs=0, B=1, T=64, H=2, K=128, V=128, chunk=64, scale=0.088,
+    a = dict(q=fake(0), k=fake(1), v=fake(2), qkv=BF16, g=fake(3), beta=fake(4), s0=None, sT=None, o=fake(5),
+             odt=F32, cu=None, cu_host=None, n_seqs=0, B=1, T=64, H=2, K=128, V=128, chunk=64, scale=0.088,
              l2=1, gate=None, gdt=BF16, w=None, eps=1e-5, y=None, mode=0)
     a.update(over)
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["s0"], a["sT"], a["o"],
@@ -97,6 +104,30 @@ def cu_host(values):
 def test_chunk_fwd_rejects(lib, over, code):
     assert chunk_call(lib, **over) == code
     assert lib.kda_last_error()
+
+
+@pytest.mark.parametrize("over,what", [
+    (dict(o=fake(0) + 4096), b"o must not overlap q"),             # o inside q
+    (dict(o=fake(3) - 16), b"o must not overlap g"),               # o runs into g
+    (dict(gate=fake(6), w=fake(7), y=fake(2)), b"y must not overlap v"),
+    (dict(gate=fake(6), w=fake(7), y=fake(5) + 1024), b"o must not overlap y"),
+    (dict(s0=fake(8), sT=fake(8) + 64), b"partly overlap"),         # states offset, not equal
+    (dict(sT=fake(1) + 256), b"final state must not overlap k"),
+    (dict(s0=fake(8), o=fake(8)), b"o must not overlap the state"),
+])
+def test_chunk_fwd_rejects_overlapping_buffers(lib, over, what):
+    """The prefill kernels read their inputs chunk by chunk while writing outputs, so an
+    output sharing bytes with an input (or with another output) is refused before any
+    launch; only final_state == initial_state (the same pointer) is allowed."""
+    assert chunk_call(lib, **over) == INVALID
+    assert what in lib.kda_last_error()
+
+
+def test_set_wait_limit_range(lib):
+    lib.kda_set_wait_limit.argtypes = [ctypes.c_int64]
+    assert lib.kda_set_wait_limit(ctypes.c_int64(1 << 33)) == INVALID
+    assert lib.kda_set_wait_limit(ctypes.c_int64(0)) == OK
+    assert lib.kda_set_wait_limit(ctypes.c_int64(-1)) == OK  # back to the default
 
 
 @pytest.mark.parametrize("values,T", [([0, 5, 3, 8], 8), ([1, 4, 8], 8), ([0, 4, 7], 8), ([0, -1, 8], 8)])
