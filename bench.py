@@ -44,7 +44,7 @@ PREFILL_LONG_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 512  # q,k,v bf16 + g fp32
 MEASURED_TRAFFIC = {
     # B=1 T=2048 H=96 capture, mean of two launches: (328.259712 MB - 6.29 MB of final state)
     # / (2048 * 96) token-heads
-    "prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
+    "prefill_fused": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
                 "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
                 "bytes_per_unit": (328.259712e6 - 6.291456e6) / (2048 * 96),
                 "capture": "ncu, B=1 T=2048 H=96, g and beta given"},
@@ -77,16 +77,26 @@ MEASURED_TRAFFIC = {
 }
 
 
-def measured_traffic(kind: str, units: float, fixed: float = 0.0):
-    """Traffic of one launch scaled from the capture, or None if the kernel changed."""
+def sources_sha256(sources):
+    """SHA-256 over the named source files, concatenated in order."""
     import hashlib
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kind: str, units: float, fixed: float = 0.0):
+    """Traffic of one launch (or one call's launches) scaled from the capture, or None if
+    a kernel source changed since the counters were taken."""
     m = MEASURED_TRAFFIC.get(kind)
     if m is None:
         return None
+    srcs = m["sources"] if "sources" in m else [m["source"]]
     try:
-        with open(os.path.join(ROOT, m["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != m["sha256"]:
-                return None
+        if sources_sha256(srcs) != m["sha256"]:
+            return None
     except OSError:
         return None
     return m["bytes_per_unit"] * units + fixed
@@ -230,19 +240,23 @@ def prefill_inputs(device, T=None):
     return make_inputs("prefill", device=device, T=T)
 
 
-def bench_prefill(args, world, rank, peaks):
+def bench_prefill(args, world, rank, peaks, fused=False):
+    """The headline prefill: the split tensor-core form (state-independent pre-pass over all
+    chunks and heads, then the per-head chain kernel) unless fused=True (one kernel per
+    (sequence, head), no workspace).  `kernel_ms` is the device time of the whole call,
+    both kernels of the split form together."""
     import torch
     import kimi_delta_attention_gated_gb300 as kda
     d = prefill_inputs("cuda", args.prefill_T)
     B, T, H, K, V = d["B"], d["T"], d["H"], d["K"], d["V"]
     o = torch.empty((B, T, H, V), device="cuda", dtype=torch.float32)
     fs = torch.empty((B, H, K, V), device="cuda", dtype=torch.float32)
+    ws = None if fused else torch.empty(kda.workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
     fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, scale=d["scale"], chunk=64,
-                               o=o, final_state=fs, mode=args.mode)
-    r = time_steps(fn, args.steps, args.warmup, world, clocks_index=torch.cuda.current_device())
+                               o=o, final_state=fs, mode=args.mode, workspace=ws)
+    r = time_steps(fn, args.steps, args.warmup, world, clocks_index=None if fused else torch.cuda.current_device())
     th = B * T * H
-    launches_per_step = max(1, r["launches"] // args.steps)
-    kernel_ms = r["call_ms"] / launches_per_step
+    kernel_ms = r["call_ms"]
     algo_bytes = th * PREFILL_BYTES_PER_TH + B * H * STATE_BYTES
     algo_flop = th * PREFILL_FLOP_PER_TH
     achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
@@ -253,9 +267,11 @@ def bench_prefill(args, world, rank, peaks):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("prefill", th, B * H * STATE_BYTES),
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": measured_traffic("prefill_fused" if fused else "prefill", th, B * H * STATE_BYTES),
                      "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
-                     "peak_source": peaks["source"]},
+                     "kernels": "chunk_tc_kernel" if fused else "chunk_prep_kernel + chunk_chain_kernel, one call",
+                     "launches_per_call": max(1, r["launches"] // args.steps), "peak_source": peaks["source"]},
         "roofline_tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": tflops / peaks["bf16_tflops"], "algorithmic_flop_per_launch": algo_flop},
         "config": {"workload": f"prefill B={B} T={T} H={H} d={K} chunk=64 zero initial state",
@@ -300,8 +316,7 @@ def bench_prefill_workload(args, world, peaks, name):
         traffic = None
     steps = max(3, args.steps // (4 if name == "long" else 1))
     r = time_steps(fn, steps, args.warmup, world)
-    launches_per_step = max(1, r["launches"] // steps)
-    kernel_ms = r["call_ms"] / launches_per_step
+    kernel_ms = r["call_ms"]  # the call's device time (both kernels of the split form)
     algo_bytes = th * per_th + state_bytes
     achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
     tflops = th * PREFILL_FLOP_PER_TH / (kernel_ms * 1e-3) / 1e12
@@ -356,7 +371,7 @@ def bench_prefill_logits(args, world, peaks):
                                       dt_bias=d["dt_bias"], g_lower_bound=d["g_lower_bound"], scale=d["scale"],
                                       mode=args.mode, o=o, final_state=fs)
     r = time_steps(fn, args.steps, args.warmup, world)
-    kernel_ms = r["call_ms"] / max(1, r["launches"] // args.steps)
+    kernel_ms = r["call_ms"]  # the call's device time (both kernels of the split form)
     th = B * T * H
     algo_bytes = th * PREFILL_LOGITS_BYTES_PER_TH + B * H * STATE_BYTES
     achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
@@ -390,7 +405,7 @@ def bench_prefill_norm(args, world, peaks):
                                gate=gate, norm_w=norm_w, eps=1e-5, out_dtype=torch.bfloat16, return_o=False, y=y,
                                final_state=fs)
     r = time_steps(fn, args.steps, args.warmup, world)
-    kernel_ms = r["call_ms"] / max(1, r["launches"] // args.steps)
+    kernel_ms = r["call_ms"]  # the call's device time (both kernels of the split form)
     th = B * T * H
     algo_bytes = th * PREFILL_NORM_BYTES_PER_TH + B * H * STATE_BYTES
     achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
@@ -625,6 +640,7 @@ def main():
             print(json.dumps(res), flush=True)
         return
     pre, d = bench_prefill(args, world, rank, peaks)
+    fused = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, fused=True)[0]
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
     conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
     logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
@@ -651,12 +667,14 @@ def main():
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
         "short_conv": conv, "prefill_gate_logits": logits, "prefill_gated_norm": norm, "o_proj": oproj,
         "prefill_varlen": varlen, "prefill_long_norm": long_, "gpu": torch.cuda.get_device_name(),
+        "prefill_fused_one_kernel": None if fused is None else {
+            "value": fused["value"], "ms_per_step": fused["ms_per_step"], "roofline": fused["roofline"]},
     }
-    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj)
+    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj, fused)
     print(json.dumps(line), flush=True)
 
 
-def summary(pre, dec, varlen, long_, logits, norm, conv, oproj):
+def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, fused=None):
     """Every timed workload in a few numbers, last on the line so that a reader of the
     line's tail sees all of them: kernel ms per launch, throughput and the fraction of
     the binding roofline (of the measured peak)."""
@@ -668,7 +686,8 @@ def summary(pre, dec, varlen, long_, logits, norm, conv, oproj):
                 "frac": round(f["frac"], 4), "bound": f["bound"]}
     out = {"prefill_T8192": row(pre, 1e6, "Mtok_s"), "prefill_varlen": row(varlen, 1e6, "Mtok_s"),
            "prefill_long_norm": row(long_, 1e6, "Mtok_s"), "decode_B256": row(dec, 1e3, "Ktok_s"),
-           "prefill_logits": row(logits, 1e6, "Mtok_s"), "prefill_norm_bf16": row(norm, 1e6, "Mtok_s")}
+           "prefill_logits": row(logits, 1e6, "Mtok_s"), "prefill_norm_bf16": row(norm, 1e6, "Mtok_s"),
+           "prefill_T8192_fused": row(fused, 1e6, "Mtok_s")}
     if conv:
         out["conv_prefill"] = row(conv["conv_prefill"], 1e6, "Mtok_s")
         out["conv_decode"] = row(conv["conv_decode"], 1e6, "Mtok_s")

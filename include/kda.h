@@ -148,6 +148,15 @@ kda_status kda_set_wait_limit(int64_t polls);
  * chunk: tokens per chunk, 16, 32 or 64 (the tensor path needs 64).
  * scale: applied to q^ (1/sqrt(K) for the layer).  use_qk_l2norm: 0 or 1.
  * Supported K, V: 32, 64, 128 (fp32 path); 128 (tensor path).
+ * workspace: caller-owned device scratch of workspace_bytes, or NULL.  On the
+ *   tensor path a workspace of at least kda_chunk_workspace_size(B, T, H, n_seqs)
+ *   bytes selects the split form: one kernel forms every chunk's state-independent
+ *   operands (grams, UT transform) in parallel over all chunks and heads and writes
+ *   them there, then one CTA per (sequence, head) runs the state through the chunks;
+ *   with NULL one fused kernel per (sequence, head) does both.  The two forms give
+ *   the same bits.  A workspace that is too small, misaligned or overlaps a tensor of
+ *   the call is KDA_ERR_INVALID_ARG; the fp32 path ignores it.  Its contents are
+ *   scratch: overwritten by the call, meaningless after it.
  * mode: a kda_mode.  Returns a kda_status.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
@@ -156,7 +165,16 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype 
                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
                          int B, int T, int H, int K, int V, int chunk, float scale,
                          int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
-                         const float *norm_w, float eps, void *y, int mode, void *stream);
+                         const float *norm_w, float eps, void *y, void *workspace,
+                         size_t workspace_bytes, int mode, void *stream);
+
+/*
+ * kda_chunk_workspace_size -- bytes of the workspace kda_chunk_fwd and
+ * kda_chunk_fwd_logits need for the split tensor-core form: 32 KiB per (chunk slot,
+ * head) for (ceil(B * T / 64) + N) slots, N = n_seqs in varlen mode (n_seqs > 0),
+ * else B.  0 for arguments no call accepts.  Host only; launches nothing.
+ */
+size_t kda_chunk_workspace_size(int B, int T, int H, int n_seqs);
 
 /*
  * kda_chunk_fwd_logits -- kda_chunk_fwd with the decay and the write strength
@@ -185,8 +203,8 @@ kda_status kda_chunk_fwd_logits(const void *q, const void *k, const void *v, kda
                                 void *o, kda_dtype o_dtype, const int32_t *cu_seqlens,
                                 const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int H, int K, int V,
                                 int chunk, float scale, int use_qk_l2norm, const void *gate,
-                                kda_dtype gate_dtype, const float *norm_w, float eps, void *y, int mode,
-                                void *stream);
+                                kda_dtype gate_dtype, const float *norm_w, float eps, void *y, void *workspace,
+                                size_t workspace_bytes, int mode, void *stream);
 
 /*
  * kda_recurrent_fwd -- the token-by-token form over T tokens (fp32 arithmetic).

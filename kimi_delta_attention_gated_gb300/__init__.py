@@ -24,6 +24,7 @@ import torch
 
 __all__ = ["chunk_fwd", "chunk_fwd_logits", "recurrent_fwd", "recurrent_step", "recurrent_step_logits",
            "gated_rmsnorm", "short_conv", "o_proj", "launch_count", "device_status", "set_wait_limit",
+           "workspace_size", "release_workspaces",
            "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -58,8 +59,11 @@ def _load():
                                "or python kimi_delta_attention_gated_gb300/build.py")
         lib = ctypes.CDLL(_LIB_PATH)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        Z = ctypes.c_size_t
         lib.kda_chunk_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I,
-                                      P, I, P, F, P, I, P]
+                                      P, I, P, F, P, P, Z, I, P]
+        lib.kda_chunk_workspace_size.argtypes = [I, I, I, I]
+        lib.kda_chunk_workspace_size.restype = Z
         lib.kda_recurrent_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I,
                                           P, I, P, F, P, P]
         lib.kda_recurrent_step.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, F,
@@ -67,7 +71,7 @@ def _load():
         lib.kda_gated_rmsnorm.argtypes = [P, I, P, I, P, F, P, I, ctypes.c_int64, I, I, P]
         lib.kda_short_conv_fwd.argtypes = [P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P]
         lib.kda_chunk_fwd_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, P, P, I, I, I, I, I, I,
-                                             I, F, I, P, I, P, F, P, I, P]
+                                             I, F, I, P, I, P, F, P, P, Z, I, P]
         lib.kda_recurrent_step_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, I, I, I, I, F, I,
                                                   P, I, P, F, P, P]
         lib.kda_o_proj.argtypes = [P, P, P, I, ctypes.c_int64, I, I, P, ctypes.c_size_t, P]
@@ -177,21 +181,26 @@ def _dev_out(t):
 
 def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use_qk_l2norm=True,
               cu_seqlens=None, output_final_state=True, gate=None, norm_w=None, eps=1e-5,
-              out_dtype=torch.float32, mode="auto", return_o=True, o=None, y=None, final_state=None):
+              out_dtype=torch.float32, mode="auto", return_o=True, o=None, y=None, final_state=None,
+              workspace="auto"):
     """Chunked prefill.  q, k [B,T,H,K]; v [B,T,H,V]; g [B,T,H,K] fp32; beta [B,T,H] fp32;
     initial_state [N,H,K,V] fp32 or None.  With ``cu_seqlens`` (int, n_seqs + 1) B must be 1.
     Returns (o, final_state) or, with ``gate``/``norm_w``, (o, final_state, y) where
     y [B,T,H*V] is the sigmoid-gated RMSNorm of o (o is None when return_o=False).
     Preallocated outputs may be passed as o / y / final_state (final_state may be
-    initial_state itself for an in-place update)."""
+    initial_state itself for an in-place update).  ``workspace``: "auto" (a per-device
+    buffer this binding keeps, which selects the split tensor-core form), a uint8 device
+    tensor of at least workspace_size(...) bytes, or None (the fused one-kernel form).
+    The kept buffer is shared by every "auto" call on a device: calls on streams that
+    may run at the same time need workspaces of their own."""
     return _chunk(q, k, v, (g, beta), None, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens,
-                  output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y, final_state)
+                  output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace)
 
 
 def chunk_fwd_logits(q, k, v, g_logits, beta_logits, A_log, initial_state=None, *, dt_bias=None,
                      g_lower_bound=-5.0, scale=None, chunk=64, use_qk_l2norm=True, cu_seqlens=None,
                      output_final_state=True, gate=None, norm_w=None, eps=1e-5, out_dtype=torch.float32,
-                     mode="auto", return_o=True, o=None, y=None, final_state=None):
+                     mode="auto", return_o=True, o=None, y=None, final_state=None, workspace="auto"):
     """chunk_fwd with g = max(g_lower_bound, -exp(A_log[h]) * softplus(g_logits + dt_bias)) and
     beta = sigmoid(beta_logits) computed inside the kernels.  g_logits [B,T,H,K] and
     beta_logits [B,T,H] in bf16 or fp32; A_log [H]; dt_bias [H,K] (or [H*K]) or None;
@@ -199,7 +208,37 @@ def chunk_fwd_logits(q, k, v, g_logits, beta_logits, A_log, initial_state=None, 
     lb = float("-inf") if g_lower_bound is None else float(g_lower_bound)
     return _chunk(q, k, v, None, (g_logits, beta_logits, A_log, dt_bias, lb), initial_state, scale, chunk,
                   use_qk_l2norm, cu_seqlens, output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y,
-                  final_state)
+                  final_state, workspace)
+
+
+def workspace_size(B, T, H, n_seqs=0) -> int:
+    """Bytes of workspace the split tensor-core prefill needs (kda_chunk_workspace_size)."""
+    return int(_load().kda_chunk_workspace_size(int(B), int(T), int(H), int(n_seqs)))
+
+
+_CHUNK_WS = {}
+
+
+def _chunk_workspace(spec, dev, B, T, H, n_seqs):
+    """(pointer, bytes) of the workspace for one call: None -> the fused form."""
+    if spec is None:
+        return None, 0
+    need = workspace_size(B, T, H, n_seqs)
+    if isinstance(spec, str):
+        if spec != "auto":
+            raise ValueError('workspace must be "auto", None or a device tensor')
+        key = dev.index if dev.index is not None else torch.cuda.current_device()
+        ws = _CHUNK_WS.get(key)
+        if ws is None or ws.numel() < need:
+            _CHUNK_WS.pop(key, None)
+            ws = _CHUNK_WS[key] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        return ctypes.c_void_p(ws.data_ptr()), ws.numel()
+    return ctypes.c_void_p(spec.data_ptr()), spec.numel() * spec.element_size()
+
+
+def release_workspaces():
+    """Drop the workspaces this binding keeps (the next call allocates again)."""
+    _CHUNK_WS.clear()
 
 
 def _pinned(t):
@@ -207,7 +246,7 @@ def _pinned(t):
 
 
 def _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, output_final_state, gate,
-                         norm_w, eps, out_dtype, mode, return_o, o, y, final_state):
+                         norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace="auto"):
     """A host-resident prompt (B = 1) through the device in HOST_SEGMENT-token segments on
     three streams: segment i+1's inputs are copied in while segment i runs (its state
     handed on in place on the device) and segment i-1's outputs are copied out, so the
@@ -261,6 +300,7 @@ def _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2
     done = [torch.cuda.Event() for _ in range(n_seg)]
     out_done = [torch.cuda.Event() for _ in range(n_seg)]
     mode_i = _MODES[mode] if isinstance(mode, str) else int(mode)
+    ws_ptr, ws_bytes = _chunk_workspace(workspace if mode_i != MODE_FP32 else None, dev, 1, seg, H, 0)
 
     def copy_in(i):
         a, b_ = i * seg, min(T, (i + 1) * seg)
@@ -287,7 +327,8 @@ def _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2
         tail = (_ptr(state), _ptr(state), _ptr(o_d), _dt(o_d if o_d is not None else y_d), None, None, 0, 1, n_tok,
                 H, K, V, int(chunk), float(scale), int(bool(use_qk_l2norm)),
                 _ptr(x["gate"][:, :n_tok]) if gate is not None else None,
-                _dt(x["gate"]) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y_d), mode_i, st)
+                _dt(x["gate"]) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y_d), ws_ptr, ws_bytes,
+                mode_i, st)
         qd, kd, vd = x["q"][:, :n_tok], x["k"][:, :n_tok], x["v"][:, :n_tok]
         if lg is None:
             _check(lib.kda_chunk_fwd(_ptr(qd), _ptr(kd), _ptr(vd), _dt(qd), _ptr(x["g"][:, :n_tok]),
@@ -331,14 +372,14 @@ HOST_SEGMENT = 1024
 
 
 def _chunk(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens, output_final_state, gate,
-           norm_w, eps, out_dtype, mode, return_o, o, y, final_state):
+           norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace="auto"):
     lib = _load()
     host = q.device.type != "cuda"
     if (host and cu_seqlens is None and q.shape[0] == 1 and q.shape[1] >= 2 * HOST_SEGMENT
             and torch.cuda.is_available()):
         return _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm,
                                     output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y,
-                                    final_state)
+                                    final_state, workspace)
     dev = _device_of(q, k, v)
     dests = (o, final_state, y) if host else None
     if host:
@@ -359,10 +400,12 @@ def _chunk(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, cu_seqle
         final_state = torch.empty((N, H, K, V), device=dev, dtype=torch.float32)
     if scale is None:
         scale = K ** -0.5
+    mode_i = _MODES[mode] if isinstance(mode, str) else int(mode)
+    ws_ptr, ws_bytes = _chunk_workspace(workspace if mode_i != MODE_FP32 else None, dev, B, T, H, n_seqs)
     tail = (_ptr(initial_state), _ptr(final_state), _ptr(o), _dt(o if o is not None else y), _ptr(cu_d), _ptr(cu_h),
             n_seqs, B, T, H, K, V, int(chunk), float(scale), int(bool(use_qk_l2norm)), _ptr(gate),
-            _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y),
-            _MODES[mode] if isinstance(mode, str) else int(mode), _stream())
+            _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y), ws_ptr, ws_bytes,
+            mode_i, _stream())
     if lg is None:
         g, beta = _prep(gb[0], dev, torch.float32), _prep(gb[1], dev, torch.float32)
         _check(lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), *tail))

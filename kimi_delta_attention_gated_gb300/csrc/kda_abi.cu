@@ -248,7 +248,8 @@ kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *
                       float *final_state, void *o, kda_dtype o_dtype, const int32_t *cu_seqlens,
                       const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int H, int K, int V, int chunk,
                       float scale, int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
-                      const float *norm_w, float eps, void *y, int mode, void *stream) {
+                      const float *norm_w, float eps, void *y, void *workspace, size_t workspace_bytes, int mode,
+                      void *stream) {
     kda::g_err[0] = 0;
     int N = 0;
     // with logits, g / beta are checked through them (the recurrence never reads g / beta then)
@@ -273,12 +274,36 @@ kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *
     cudaStream_t st = (cudaStream_t)stream;
     // an empty prompt only hands the state through: the fp32 path does that without a tensor map
     const bool use_tc = tc_ok && mode != KDA_MODE_FP32 && T > 0;
+    KDA_REQUIRE(!workspace || aligned16(workspace), KDA_ERR_INVALID_ARG, "%s: the workspace must be 16-byte aligned",
+                fn);
     if (use_tc) {
         kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, initial_state, final_state, o, o_dtype, nullptr,
                                        cu_seqlens, N, T, H, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y);
         p.cu_host = cu_seqlens_host;
         set_logits(p, gl, K);
-        return kda::launch_chunk_tc(p, K, V, chunk, st);
+        if (!workspace) return kda::launch_chunk_tc(p, K, V, chunk, st);
+        const int64_t rows = (int64_t)B * T;
+        const size_t need = kda::chunk_workspace_bytes(rows, N, H);
+        KDA_REQUIRE(workspace_bytes >= need, KDA_ERR_INVALID_ARG,
+                    "%s: the workspace holds %zu bytes, this call needs %zu (kda_chunk_workspace_size)", fn,
+                    workspace_bytes, need);
+        {  // the workspace is written while every tensor of the call is in use
+            const size_t r = (size_t)rows, qkv = esize(qkv_dtype), st_bytes = (size_t)N * H * K * V * 4;
+            const Span ws{workspace, need, "the workspace"};
+            const Span all[] = {{q, r * H * K * qkv, "q"}, {k, r * H * K * qkv, "k"}, {v, r * H * V * qkv, "v"},
+                                {gchk, r * H * K * (gl ? esize(gl->z_dtype) : 4), "g"},
+                                {bchk, r * H * (gl ? esize(gl->b_dtype) : 4), "beta"},
+                                {o, o ? r * H * V * esize(o_dtype) : 0, "o"},
+                                {y, y ? r * H * V * esize(o_dtype) : 0, "y"},
+                                {gate, gate ? r * H * V * esize(gate_dtype) : 0, "gate"},
+                                {initial_state, initial_state ? st_bytes : 0, "initial_state"},
+                                {final_state, final_state ? st_bytes : 0, "final_state"}};
+            for (const Span &x : all)
+                KDA_REQUIRE(!overlaps(ws, x), KDA_ERR_INVALID_ARG, "%s: the workspace must not overlap %s", fn, x.name);
+        }
+        s = kda::launch_chunk_prep(p, workspace, st);
+        if (s != KDA_OK) return s;
+        return kda::launch_chunk_chain(p, workspace, st);
     }
     // fp32 path: o goes to y's buffer when o is not wanted, then the norm runs in place.
     void *o_target = o ? o : y;
@@ -345,10 +370,13 @@ kda_status kda_device_status(void *stream) {
         set_error("kda_device_status: the stream failed: %s", cudaGetErrorString(e));
         return KDA_ERR_CUDA;
     }
-    const int n_tc = kda::take_chunk_tc_timeouts(st);
+    const int n_tc0 = kda::take_chunk_tc_timeouts(st);
+    const int n_prep = kda::take_chunk_prep_timeouts(st);
+    const int n_chain = kda::take_chunk_chain_timeouts(st);
     const int n_dec = kda::take_decode_timeouts(st);
     const int n_conv = kda::take_short_conv_timeouts(st);
-    if (n_tc < 0 || n_dec < 0 || n_conv < 0) return KDA_ERR_CUDA;
+    if (n_tc0 < 0 || n_prep < 0 || n_chain < 0 || n_dec < 0 || n_conv < 0) return KDA_ERR_CUDA;
+    const int n_tc = n_tc0 + n_prep + n_chain;
     if (n_tc + n_dec + n_conv > 0) {
         set_error("kda_device_status: bounded waits gave up in %d prefill, %d decode and %d short-convolution "
                   "CTAs; their outputs hold NaN",
@@ -372,10 +400,17 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype 
                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
                          int B, int T, int H, int K, int V, int chunk, float scale,
                          int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
-                         const float *norm_w, float eps, void *y, int mode, void *stream) {
+                         const float *norm_w, float eps, void *y, void *workspace, size_t workspace_bytes, int mode,
+                         void *stream) {
     return chunk_impl("kda_chunk_fwd", q, k, v, qkv_dtype, g, beta, nullptr, initial_state, final_state, o, o_dtype,
                       cu_seqlens, cu_seqlens_host, n_seqs, B, T, H, K, V, chunk, scale, use_qk_l2norm, gate,
-                      gate_dtype, norm_w, eps, y, mode, stream);
+                      gate_dtype, norm_w, eps, y, workspace, workspace_bytes, mode, stream);
+}
+
+size_t kda_chunk_workspace_size(int B, int T, int H, int n_seqs) {
+    if (B <= 0 || T < 0 || H <= 0 || n_seqs < 0) return 0;
+    const int N = n_seqs > 0 ? n_seqs : B;
+    return kda::chunk_workspace_bytes((int64_t)B * T, N, H);
 }
 
 kda_status kda_chunk_fwd_logits(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
@@ -385,12 +420,12 @@ kda_status kda_chunk_fwd_logits(const void *q, const void *k, const void *v, kda
                                 void *o, kda_dtype o_dtype, const int32_t *cu_seqlens,
                                 const int32_t *cu_seqlens_host, int n_seqs, int B, int T, int H, int K, int V,
                                 int chunk, float scale, int use_qk_l2norm, const void *gate,
-                                kda_dtype gate_dtype, const float *norm_w, float eps, void *y, int mode,
-                                void *stream) {
+                                kda_dtype gate_dtype, const float *norm_w, float eps, void *y, void *workspace,
+                                size_t workspace_bytes, int mode, void *stream) {
     const GateLogits gl{g_logits, g_logits_dtype, A_log, dt_bias, g_lower_bound, beta_logits, beta_logits_dtype};
     return chunk_impl("kda_chunk_fwd_logits", q, k, v, qkv_dtype, nullptr, nullptr, &gl, initial_state, final_state,
                       o, o_dtype, cu_seqlens, cu_seqlens_host, n_seqs, B, T, H, K, V, chunk, scale, use_qk_l2norm,
-                      gate, gate_dtype, norm_w, eps, y, mode, stream);
+                      gate, gate_dtype, norm_w, eps, y, workspace, workspace_bytes, mode, stream);
 }
 
 kda_status kda_recurrent_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,

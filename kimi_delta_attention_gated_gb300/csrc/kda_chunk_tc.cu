@@ -55,6 +55,7 @@
 #include <math.h>
 #include <string.h>
 
+#include "kda_chunk_common.cuh"
 #include "kda_internal.cuh"
 #include "kda_tc_ptx.cuh"
 
@@ -62,13 +63,9 @@ namespace kda {
 namespace {
 
 using namespace tc;
+using namespace chunk;
 
-constexpr int C = 64;            // tokens per chunk
-constexpr int DK = 128;          // key dim
-constexpr int DV = 128;          // value dim
 constexpr int kThreads = 512;    // 16 warps = 4 warpgroups
-constexpr float kRangeMax = 80.f;
-constexpr uint32_t kPolls = 1u << 26;  // bound on every mbarrier wait
 
 // TMEM columns
 constexpr uint32_t T_R = 0, T_O = 64, T_S = 128, T_SH = 256, T_SL = 320, T_G = 384;
@@ -83,7 +80,6 @@ constexpr uint32_t S_PKGL = 139264;     // [P ; Kg^T] lo
 constexpr uint32_t S_TBH = 163840;      // T diag(beta) hi, 64 x 64 (8 KB)
 constexpr uint32_t S_TBL = 172032;
 constexpr uint32_t S_ID = 180224;       // bf16 identity 64 x 64 (8 KB)
-constexpr int AP = 68;                  // fp32 pitch of A and T
 constexpr uint32_t S_A = 188416;        // A fp32 [64][AP] (17408 B)
 constexpr uint32_t S_T = S_A + 64 * AP * 4;  // T fp32 [64][AP]
 constexpr uint32_t S_SMALL = S_T + 64 * AP * 4;
@@ -119,62 +115,13 @@ struct TcParams {
     int order[64];
 };
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // barrier over warps 1-15 (the triangular solve, while warp 0 issues MMAs)
 __device__ __forceinline__ void tbar() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
 
-// Writes 8 consecutive columns (col % 8 == 0) of one row as hi/lo.
-__device__ __forceinline__ void st_tile8(uint32_t hi_base, uint32_t lo_base, uint32_t rows, uint32_t row,
-                                         uint32_t col, const float *x) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
-    const uint32_t off = sw128_off(row, col, rows);
-    st_shared_v4(hi_base + off, h[0], h[1], h[2], h[3]);
-    st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
-}
 
-// Kg^T rows c..c+3 (one per key channel) at columns j0..j0+3 (4 tokens) of the
-// [P ; Kg^T] tiles, hi and lo: x[t][e] is token j0 + t, channel c + e, c = 4 * lane.
-// Store e of a lane writes channel c + ((e + rot) & 3) with rot = (lane >> 1) & 3, so the
-// 32 rows of one store cover all 8 swizzle phases (4 wavefronts instead of 16).
-__device__ __forceinline__ void st_kgt(uint32_t sb, int c, int j0, const float (&x)[4][4]) {
-    const int rot = (c >> 3) & 3;
-    float y[4][4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        float a[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = (rot & 1) ? x[t][(e + 1) & 3] : x[t][e];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[t][e] = (rot & 2) ? a[(e + 2) & 3] : a[e];
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        uint32_t h0, l0, h1, l1;
-        split2(y[0][e], y[1][e], h0, l0);
-        split2(y[2][e], y[3][e], h1, l1);
-        const uint32_t off = sw128_off(64 + c + ((e + rot) & 3), j0, 192);
-        st_shared_v2(sb + S_PKGH + off, h0, h1);
-        st_shared_v2(sb + S_PKGL + off, l0, l1);
-    }
-}
 
-// SWIZZLE_128B shared-memory descriptor (the same fields as sdesc) of the operand at byte
-// offset off from the 1024-aligned shared base whose address / 16 is sb16: the address
-// field is sb16 + off / 16 (below 2^14, shared addresses being below 2^18 bytes), so with
-// compile-time off, lbo and sbo the whole descriptor is one add and a constant high word.
-__device__ __forceinline__ uint64_t sdesc_at(uint32_t sb16, uint32_t off, uint32_t lbo, uint32_t sbo) {
-    const uint32_t lo = (sb16 + (off >> 4)) | ((lbo >> 4) << 16);
-    const uint32_t hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
-    return ((uint64_t)hi << 32) | lo;
-}
 
-// hi*hi, hi*lo, lo*hi: (A part, B part) of the three products of a split operand pair
-__device__ __forceinline__ int combo_a(int cb) { return cb == 2 ? 1 : 0; }
-__device__ __forceinline__ int combo_b(int cb) { return cb == 1 ? 1 : 0; }
 
 // One 16 x 16 x 16 product of the triangular solve, 64 threads, each a 1 x 4 strip:
 // dst = (acc ? dst : 0) + sign * X Y, blocks addressed by their top-left element.
@@ -602,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return oor;
     };
 
-    auto st_kg = [&](const float (&kgv)[4][4]) { st_kgt(sb, l4, warp * 4, kgv); };
+    auto st_kg = [&](const float (&kgv)[4][4]) { st_kgt(sb + S_PKGH, sb + S_PKGL, l4, warp * 4, kgv); };
 
     // ---- first chunk's preparation (later chunks are prepared inside the previous
     // chunk's tensor-core waits)
@@ -714,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kg[r][c] = kv * fs[F_RK + i] * __expf(Gs[63 * 128 + l4 + c] - Gs[i * 128 + l4 + c]);
                     }
                 }
-                st_kgt(sb, l4, warp * 4, kg);
+                st_kgt(sb + S_PKGH, sb + S_PKGL, l4, warp * 4, kg);
             }
             float *Pf = Tsm;  // P in fp32, converted to the tile below
             for (int i = warp; i < C; i += 16) {
@@ -1107,10 +1054,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() { return reinterpret_cast<EncodeTiledFn>(tensor_map_encoder()); }
 

@@ -43,6 +43,8 @@ struct DeviceOnce {
 // (after it has drained) for the current device; each returns the count it took, or -1
 // with the error message set when CUDA fails.
 int take_chunk_tc_timeouts(cudaStream_t st);
+int take_chunk_prep_timeouts(cudaStream_t st);
+int take_chunk_chain_timeouts(cudaStream_t st);
 int take_decode_timeouts(cudaStream_t st);
 int take_short_conv_timeouts(cudaStream_t st);
 
@@ -144,6 +146,12 @@ kda_status launch_recurrent(const SeqParams &p, int K, int V, cudaStream_t st);
 kda_status launch_chunk_fp32(const SeqParams &p, int K, int V, int chunk, const int *order,
                              cudaStream_t st);
 kda_status launch_chunk_tc(const SeqParams &p, int K, int V, int chunk, cudaStream_t st);
+// The split tensor-core prefill: the state-independent pre-pass writes every chunk's
+// operand images into ws (chunk_workspace_bytes long), then the chain kernel runs the
+// state through the chunks.  Both need K = V = 128, chunk = 64, bf16 q/k/v.
+size_t chunk_workspace_bytes(int64_t rows, int N, int H);
+kda_status launch_chunk_prep(const SeqParams &p, void *ws, cudaStream_t st);
+kda_status launch_chunk_chain(const SeqParams &p, const void *ws, cudaStream_t st);
 kda_status launch_gated_rmsnorm(const void *o, int o_bf16, const void *gate, int gate_bf16,
                                 const float *w, float eps, void *y, int y_bf16, int64_t rows,
                                 int H, int V, cudaStream_t st);

@@ -240,6 +240,25 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (a multiple of 16; both addresses 16-byte
+// aligned) from shared into global memory, tracked by the issuing thread's bulk group.
+// The shared source must have been made visible to the async proxy (fence_async_smem
+// by its writers, then a barrier) before the issue.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every committed bulk store of this thread has read its shared source
+// (the buffer may then be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Waits until every committed bulk store of this thread has completed its writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // TMA: 2-D tiled load into shared memory, completion counted on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint64_t *bar, int x, int y) {
     asm volatile(

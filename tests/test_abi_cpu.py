@@ -63,12 +63,12 @@ def fake(i):
 def chunk_call(lib, **over):
     a = dict(q=fake(0), k=fake(1), v=fake(2), qkv=BF16, g=fake(3), beta=fake(4), s0=None, sT=None, o=fake(5),
              odt=F32, cu=None, cu_host=None, n_seqs=0, B=1, T=64, H=2, K=128, V=128, chunk=64, scale=0.088,
-             l2=1, gate=None, gdt=BF16, w=None, eps=1e-5, y=None, mode=0)
+             l2=1, gate=None, gdt=BF16, w=None, eps=1e-5, y=None, ws=None, ws_bytes=0, mode=0)
     a.update(over)
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["s0"], a["sT"], a["o"],
                              a["odt"], a["cu"], a["cu_host"], a["n_seqs"], a["B"], a["T"], a["H"], a["K"],
                              a["V"], a["chunk"], a["scale"], a["l2"], a["gate"], a["gdt"], a["w"], a["eps"],
-                             a["y"], a["mode"], None)
+                             a["y"], a["ws"], a["ws_bytes"], a["mode"], None)
 
 
 def cu_host(values):
@@ -119,6 +119,25 @@ def test_chunk_fwd_rejects_overlapping_buffers(lib, over, what):
     """The prefill kernels read their inputs chunk by chunk while writing outputs, so an
     output sharing bytes with an input (or with another output) is refused before any
     launch; only final_state == initial_state (the same pointer) is allowed."""
+    assert chunk_call(lib, **over) == INVALID
+    assert what in lib.kda_last_error()
+
+
+def test_workspace_size(lib):
+    """32 KiB per (chunk slot, head); ceil(rows / 64) + N slots (N = n_seqs in varlen mode)."""
+    lib.kda_chunk_workspace_size.restype = ctypes.c_size_t
+    assert lib.kda_chunk_workspace_size(1, 8192, 96, 0) == (128 + 1) * 96 * 32768
+    assert lib.kda_chunk_workspace_size(2, 65536, 96, 0) == (2048 + 2) * 96 * 32768
+    assert lib.kda_chunk_workspace_size(1, 100, 3, 4) == (2 + 4) * 3 * 32768
+    assert lib.kda_chunk_workspace_size(0, 64, 2, 0) == 0
+
+
+@pytest.mark.parametrize("over,what", [
+    (dict(ws=fake(8), ws_bytes=1024), b"workspace holds"),            # too small
+    (dict(ws=fake(8) + 4, ws_bytes=1 << 22), b"16-byte aligned"),
+    (dict(ws=fake(5), ws_bytes=1 << 22), b"workspace must not overlap o"),
+])
+def test_chunk_fwd_rejects_bad_workspace(lib, over, what):
     assert chunk_call(lib, **over) == INVALID
     assert what in lib.kda_last_error()
 
