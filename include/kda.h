@@ -177,6 +177,42 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype 
 size_t kda_chunk_workspace_size(int B, int T, int H, int n_seqs);
 
 /*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate device memory.
+ *
+ * The split tensor-core prefill keeps every chunk's state-independent operands in
+ * scratch memory between its two kernels, and kda_chunk_fwd takes that scratch from
+ * the caller as a workspace.  Some callers have no way to provide one: code behind a
+ * fixed operator or plugin interface that passes only input and output tensors, and
+ * code that runs where device allocation is not allowed or not possible (a memory
+ * pool owned by another component, a latency-critical path that must not allocate).
+ * This entry point takes the same arguments as kda_chunk_fwd without the workspace
+ * and uses a fixed 64 MiB array in the library's own device memory instead.  It makes
+ * no allocation of any kind: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ *   - Limit: a call may need at most 64 MiB of scratch, i.e. 2048 (chunk slot, head)
+ *     blobs of 32 KiB (kda_chunk_workspace_size gives a call's need); for example one
+ *     prompt of up to 1280 tokens at 96 heads.  A larger call returns
+ *     KDA_ERR_UNSUPPORTED with a message giving both sizes, and launches nothing.
+ *   - The array exists on every GPU that loads the library and stays there until the
+ *     process exits.  The first call on a device, with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress, once per device); make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind.  Nothing in it
+ *     needs to start at zero: the first kernel of a call writes every byte the second
+ *     reads.  Calls whose work can overlap on the GPU (different streams, different
+ *     host threads) race on the array and must be ordered by the caller.
+ *   - Results are identical to kda_chunk_fwd with a workspace (the same kernels).
+ * No counterpart on the pages: it is an interface for a class of callers.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                 const float *g, const float *beta, const float *initial_state,
+                                 float *final_state, void *o, kda_dtype o_dtype,
+                                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
+                                 int B, int T, int H, int K, int V, int chunk, float scale,
+                                 int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                                 const float *norm_w, float eps, void *y, int mode, void *stream);
+
+/*
  * kda_chunk_fwd_logits -- kda_chunk_fwd with the decay and the write strength
  * computed inside the kernels from the logits the layer's projections produce,
  * instead of read as fp32 g and beta (halves the g traffic with bf16 logits).

@@ -62,6 +62,9 @@ def _load():
         Z = ctypes.c_size_t
         lib.kda_chunk_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I,
                                       P, I, P, F, P, P, Z, I, P]
+        lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I,
+                                              P, I, P, F, P, I, P]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_workspace_size.argtypes = [I, I, I, I]
         lib.kda_chunk_workspace_size.restype = Z
         lib.kda_recurrent_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I,

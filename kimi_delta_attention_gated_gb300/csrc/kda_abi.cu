@@ -343,6 +343,21 @@ kda_status step_impl(const char *fn, const void *q, const void *k, const void *v
 
 }  // namespace
 
+namespace kda {
+
+kda_status chunk_fwd_entry(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                           const float *g, const float *beta, const float *initial_state, float *final_state, void *o,
+                           kda_dtype o_dtype, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
+                           int B, int T, int H, int K, int V, int chunk, float scale, int use_qk_l2norm,
+                           const void *gate, kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
+                           void *workspace, size_t workspace_bytes, int mode, void *stream) {
+    return chunk_impl(fn, q, k, v, qkv_dtype, g, beta, nullptr, initial_state, final_state, o, o_dtype, cu_seqlens,
+                      cu_seqlens_host, n_seqs, B, T, H, K, V, chunk, scale, use_qk_l2norm, gate, gate_dtype, norm_w,
+                      eps, y, workspace, workspace_bytes, mode, stream);
+}
+
+}  // namespace kda
+
 extern "C" {
 
 int kda_version(void) { return kda::kVersion; }

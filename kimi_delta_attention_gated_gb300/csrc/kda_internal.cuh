@@ -139,6 +139,14 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// kda_chunk_fwd's validation and dispatch, with the name `fn` in its error messages.
+kda_status chunk_fwd_entry(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                           const float *g, const float *beta, const float *initial_state, float *final_state, void *o,
+                           kda_dtype o_dtype, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int n_seqs,
+                           int B, int T, int H, int K, int V, int chunk, float scale, int use_qk_l2norm,
+                           const void *gate, kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
+                           void *workspace, size_t workspace_bytes, int mode, void *stream);
+
 // ---------------------------------------------------------------------------
 // launchers (one per translation unit); each returns KDA_OK or an error status
 
