@@ -484,7 +484,7 @@ def bench_o_proj(args, world, peaks):
         roof.update(kernel_ms=kernel_ms, peak_source=peaks["source"])
         out[name] = {"metric": "o_proj tokens/s", "value": world * rows / (r["ms_per_step"] * 1e-3), "unit": "tokens/s",
                      "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
-                     "config": {"workload": f"o_proj rows={rows} 12288->7168 bf16 (cuBLASLt)"}, "roofline": roof}
+                     "config": {"workload": f"o_proj rows={rows} 12288->7168 bf16 (tcgen05 GEMM)"}, "roofline": roof}
     return out
 
 
@@ -600,7 +600,7 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits", "norm", "varlen",
-                                       "long"], default="all",
+                                       "long", "oproj"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
@@ -625,8 +625,10 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "conv", "kernels", "logits", "norm", "varlen", "long"):
-        if args.only in ("varlen", "long"):
+    if args.only in ("decode", "conv", "kernels", "logits", "norm", "varlen", "long", "oproj"):
+        if args.only == "oproj":
+            res = bench_o_proj(args, world, peaks)
+        elif args.only in ("varlen", "long"):
             res = bench_prefill_workload(args, world, peaks, args.only)
         elif args.only == "kernels":  # decode step + short convolution (profiling runs)
             res = {"decode": bench_decode(args, world, peaks), "short_conv": bench_short_conv(args, world, peaks)}

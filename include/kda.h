@@ -361,15 +361,14 @@ kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *wei
  *   y     [rows, in_features] bf16 (the y of kda_chunk_fwd / kda_recurrent_step with a
  *         bf16 output dtype)
  *   w_o   [out_features, in_features] bf16 (the nn.Linear weight layout)
- *   out   [rows, out_features] out_dtype
- *   workspace: caller-owned device scratch for the GEMM, workspace_bytes long (NULL
- *         and 0 allowed; 32 MiB lets the library pick its fastest kernels).
- * A plain dense GEMM, run by cuBLASLt with bf16 operands and fp32 accumulation.  The
- * cuBLASLt handle is created on first use and kept for the process.  Feature counts
- * must be multiples of 8.
+ *   out   [rows, out_features] out_dtype; must not overlap y or w_o
+ * A dense GEMM on the tensor cores (this library's own tcgen05 kernel, bf16 operands,
+ * fp32 accumulation, one rounding to out_dtype).  in_features must be a multiple of
+ * 64 and out_features of 128 (KDA_ERR_UNSUPPORTED otherwise); rows may be 0.  Keeps
+ * no state between calls.
  */
 kda_status kda_o_proj(const void *y, const void *w_o, void *out, kda_dtype out_dtype, int64_t rows,
-                      int in_features, int out_features, void *workspace, size_t workspace_bytes, void *stream);
+                      int in_features, int out_features, void *stream);
 
 #ifdef __cplusplus
 }

@@ -77,7 +77,7 @@ def _load():
                                              I, F, I, P, I, P, F, P, P, Z, I, P]
         lib.kda_recurrent_step_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, I, I, I, I, F, I,
                                                   P, I, P, F, P, P]
-        lib.kda_o_proj.argtypes = [P, P, P, I, ctypes.c_int64, I, I, P, ctypes.c_size_t, P]
+        lib.kda_o_proj.argtypes = [P, P, P, I, ctypes.c_int64, I, I, P]
         for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
                    "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits", "kda_o_proj"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -560,14 +560,10 @@ def short_conv(x, weight, bias=None, conv_state=None, *, cu_seqlens=None, activa
     return _to_host((y, final_state), host, dests)
 
 
-_WORKSPACE = {}
-O_PROJ_WORKSPACE_BYTES = 32 << 20
-
-
-def o_proj(y, w_o, *, out_dtype=torch.bfloat16, out=None, workspace=None):
+def o_proj(y, w_o, *, out_dtype=torch.bfloat16, out=None):
     """out [rows, out_features] = y [rows, in_features] @ w_o[out_features, in_features]^T
-    (bf16 operands, fp32 accumulation).  y may carry extra leading dimensions.  The
-    GEMM workspace is a per-device tensor this binding keeps (32 MiB) unless one is given."""
+    (bf16 operands, fp32 accumulation, on the library's tcgen05 GEMM).  y may carry extra
+    leading dimensions."""
     lib = _load()
     host = y.device.type != "cuda"
     dev = _device_of(y, w_o)
@@ -580,13 +576,7 @@ def o_proj(y, w_o, *, out_dtype=torch.bfloat16, out=None, workspace=None):
     dest = out if host else None
     if out is None or host:
         out = torch.empty((rows, N), device=dev, dtype=out_dtype)
-    if workspace is None:
-        key = dev.index if dev.index is not None else torch.cuda.current_device()
-        workspace = _WORKSPACE.get(key)
-        if workspace is None:
-            workspace = _WORKSPACE[key] = torch.empty(O_PROJ_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
-    _check(lib.kda_o_proj(_ptr(y2), _ptr(w), _ptr(out), _dt(out), rows, K, N, _ptr(workspace),
-                          workspace.numel() * workspace.element_size(), _stream()))
+    _check(lib.kda_o_proj(_ptr(y2), _ptr(w), _ptr(out), _dt(out), rows, K, N, _stream()))
     res = out.reshape(*y.shape[:-1], N)
     if host:
         return _to_host((res,), True, (dest,))[0]

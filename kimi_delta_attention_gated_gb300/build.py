@@ -74,7 +74,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
         objs = list(ex.map(lambda s: _compile(s, extra, verbose or ptxas_info), srcs))
     if force or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt"]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

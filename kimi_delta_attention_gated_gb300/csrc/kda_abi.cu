@@ -390,12 +390,13 @@ kda_status kda_device_status(void *stream) {
     const int n_chain = kda::take_chunk_chain_timeouts(st);
     const int n_dec = kda::take_decode_timeouts(st);
     const int n_conv = kda::take_short_conv_timeouts(st);
-    if (n_tc0 < 0 || n_prep < 0 || n_chain < 0 || n_dec < 0 || n_conv < 0) return KDA_ERR_CUDA;
+    const int n_proj = kda::take_oproj_timeouts(st);
+    if (n_tc0 < 0 || n_prep < 0 || n_chain < 0 || n_dec < 0 || n_conv < 0 || n_proj < 0) return KDA_ERR_CUDA;
     const int n_tc = n_tc0 + n_prep + n_chain;
-    if (n_tc + n_dec + n_conv > 0) {
-        set_error("kda_device_status: bounded waits gave up in %d prefill, %d decode and %d short-convolution "
-                  "CTAs; their outputs hold NaN",
-                  n_tc, n_dec, n_conv);
+    if (n_tc + n_dec + n_conv + n_proj > 0) {
+        set_error("kda_device_status: bounded waits gave up in %d prefill, %d decode, %d short-convolution and %d "
+                  "output-projection CTAs; their outputs hold NaN",
+                  n_tc, n_dec, n_conv, n_proj);
         return KDA_ERR_TIMEOUT;
     }
     return KDA_OK;
@@ -560,23 +561,29 @@ kda_status kda_short_conv_fwd(const void *x, kda_dtype x_dtype, const float *wei
 }
 
 kda_status kda_o_proj(const void *y, const void *w_o, void *out, kda_dtype out_dtype, int64_t rows,
-                      int in_features, int out_features, void *workspace, size_t workspace_bytes, void *stream) {
+                      int in_features, int out_features, void *stream) {
     kda::g_err[0] = 0;
     const char *fn = "kda_o_proj";
     KDA_REQUIRE(rows >= 0 && in_features > 0 && out_features > 0, KDA_ERR_INVALID_ARG,
                 "%s: need rows >= 0 and positive feature counts", fn);
     KDA_REQUIRE(rows == 0 || (y && w_o && out), KDA_ERR_INVALID_ARG, "%s: y, w_o and out must not be NULL", fn);
     KDA_REQUIRE(dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED, "%s: unsupported out dtype", fn);
-    KDA_REQUIRE(in_features % 8 == 0 && out_features % 8 == 0, KDA_ERR_UNSUPPORTED,
-                "%s: feature counts must be multiples of 8", fn);
+    KDA_REQUIRE(kda::o_proj_supported(in_features, out_features), KDA_ERR_UNSUPPORTED,
+                "%s: in_features must be a multiple of 64 and out_features a multiple of 128", fn);
     KDA_REQUIRE(rows <= INT32_MAX, KDA_ERR_INVALID_ARG, "%s: too many rows", fn);
-    KDA_REQUIRE(workspace_bytes == 0 || workspace, KDA_ERR_INVALID_ARG, "%s: workspace_bytes > 0 needs a workspace", fn);
-    const void *ptrs[] = {y, w_o, out, workspace};
+    const void *ptrs[] = {y, w_o, out};
     for (const void *ptr : ptrs)
         KDA_REQUIRE(!ptr || aligned16(ptr), KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);
     if (rows == 0) return KDA_OK;
-    return kda::launch_o_proj(y, w_o, out, out_dtype == KDA_BF16, rows, in_features, out_features, workspace,
-                              workspace_bytes, (cudaStream_t)stream);
+    {
+        const size_t r = (size_t)rows, ob = out_dtype == KDA_BF16 ? 2 : 4;
+        const Span o{out, r * out_features * ob, "out"};
+        KDA_REQUIRE(!overlaps(o, Span{y, r * in_features * 2, "y"}) &&
+                        !overlaps(o, Span{w_o, (size_t)out_features * in_features * 2, "w_o"}),
+                    KDA_ERR_INVALID_ARG, "%s: out must not overlap y or w_o", fn);
+    }
+    return kda::launch_o_proj(y, w_o, out, out_dtype == KDA_BF16, rows, in_features, out_features,
+                              (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -55,9 +55,8 @@ constexpr uint32_t P_SMALL = 98304;
 constexpr uint32_t PF_BETA = 0;            // beta [64]
 constexpr uint32_t PF_RQ = 64;             // q scale per token (norm * scale) [64]
 constexpr uint32_t PF_RK = 128;            // k norm per token [64]
-constexpr uint32_t PF_TOT = 192;           // decay totals of the 16 groups of 4 tokens [16][128], then their prefix
-constexpr uint32_t PF_GAM = PF_TOT + 2048; // chunk total per channel [128]
-constexpr uint32_t PF_END = PF_GAM + 128;
+constexpr uint32_t PF_TOT = 192;           // decay totals of the 16 groups of 4 tokens [16][128]
+constexpr uint32_t PF_END = PF_TOT + 2048;
 constexpr uint32_t P_BARS = P_SMALL + PF_END * 4;  // 3 mbarriers + tmem slot
 constexpr uint32_t PREP_SMEM = P_BARS + 32 + 1024;
 // fallback (decay range too wide): exact G in the Km tile, P in fp32 where T goes
@@ -345,28 +344,33 @@ __global__ void __launch_bounds__(kPT, 2)
             stores_pending = false;
         }
         __syncthreads();
-        // ---- exclusive prefix of the 16 group totals per channel (in place) and the chunk total
-        if (tid < DK) {
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < 16; ++w) {
-                const float t = fs[PF_TOT + w * 128 + tid];
-                fs[PF_TOT + w * 128 + tid] = acc;
-                acc += t;
-            }
-            fs[PF_GAM + tid] = acc;
-        }
-        __syncthreads();
-
-        // ---- operand tiles: [-Kd ; Qd] and Km, hi and lo
+        // ---- operand tiles: [-Kd ; Qd] and Km, hi and lo.  Each thread forms the exclusive
+        // prefix of the 16 group totals for its channels and the chunk total itself, summing
+        // the totals in order (the fused kernel's order, so the same bits) with no barrier
         int oor = 0;
         {
-            const float4 u = *reinterpret_cast<const float4 *>(fs + PF_GAM + l4);
-            oor = (-u.x > kRangeMax) | (-u.y > kRangeMax) | (-u.z > kRangeMax) | (-u.w > kRangeMax);
+            float o4[2][4], gam[4] = {0.f, 0.f, 0.f, 0.f};
+            auto add_total = [&](int w) {
+                const float4 t = *reinterpret_cast<const float4 *>(fs + PF_TOT + w * 128 + l4);
+                gam[0] += t.x;
+                gam[1] += t.y;
+                gam[2] += t.z;
+                gam[3] += t.w;
+            };
+#pragma unroll 1
+            for (int w = 0; w < 2 * warp; ++w) add_total(w);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                const float4 t = *reinterpret_cast<const float4 *>(fs + PF_TOT + (2 * warp + half) * 128 + l4);
-                float2 o2[2] = {make_float2(t.x, t.y), make_float2(t.z, t.w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o4[half][e] = gam[e];
+                add_total(2 * warp + half);
+            }
+#pragma unroll 1
+            for (int w = 2 * warp + 2; w < 16; ++w) add_total(w);
+            oor = (-gam[0] > kRangeMax) | (-gam[1] > kRangeMax) | (-gam[2] > kRangeMax) | (-gam[3] > kRangeMax);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float2 o2[2] = {make_float2(o4[half][0], o4[half][1]), make_float2(o4[half][2], o4[half][3])};
 #pragma unroll
                 for (int rr = 0; rr < 4; ++rr) {
                     const int r = 4 * half + rr, i = warp * 8 + r;

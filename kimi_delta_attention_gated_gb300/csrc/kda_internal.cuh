@@ -45,6 +45,7 @@ struct DeviceOnce {
 int take_chunk_tc_timeouts(cudaStream_t st);
 int take_chunk_prep_timeouts(cudaStream_t st);
 int take_chunk_chain_timeouts(cudaStream_t st);
+int take_oproj_timeouts(cudaStream_t st);
 int take_decode_timeouts(cudaStream_t st);
 int take_short_conv_timeouts(cudaStream_t st);
 
@@ -166,8 +167,9 @@ kda_status launch_gated_rmsnorm(const void *o, int o_bf16, const void *gate, int
 kda_status launch_short_conv(const void *x, int x_bf16, const float *w, const float *bias, const float *s0,
                              float *sT, void *y, int y_bf16, const int32_t *cu, int N, int64_t rows, int T,
                              int D, int W, int act, cudaStream_t st);
-kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, int64_t M, int K, int N, void *ws,
-                         size_t ws_bytes, cudaStream_t st);
+kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, int64_t M, int K, int N,
+                         cudaStream_t st);
+bool o_proj_supported(int K, int N);
 bool chunk_tc_supported(int K, int V, int chunk);
 // cuTensorMapEncodeTiled from the driver (no link against libcuda), or null.
 void *tensor_map_encoder();

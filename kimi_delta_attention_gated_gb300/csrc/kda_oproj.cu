@@ -1,4 +1,4 @@
-// kda_oproj.cu -- the layer's output projection of the gated-norm output.
+// kda_oproj.cu -- the layer's output projection of the gated-norm output, on the tensor cores.
 //
 // Page: Kimi-K3 atlas "gate-project (decode, P = 1000)", sections "Parameters"
 // (output projection 88,080,384 weights = 12288 inputs x 7168 outputs) and "Code"
@@ -6,93 +6,309 @@
 //
 //   out[r][n] = sum_c y[r][c] * w_o[n][c]      (nn.Linear, no bias)
 //
-// A plain dense GEMM: it runs in cuBLASLt (bf16 operands, fp32 accumulation) on the
-// caller's workspace.  In column-major terms out^T [N, M] = (W [K, N])^T y^T [K, M],
-// i.e. A = w_o read transposed, B = y, with M = rows, N = out_features, K = in_features.
-// The cuBLASLt handle is created once per process (host state); the plan for the
-// last shape is cached.
-#include <cublasLt.h>
+// A dense GEMM with bf16 operands and fp32 accumulation, written for tcgen05.  Each tile
+// is 128 output features (the MMA M dimension: the rows of w_o, so the accumulator's
+// TMEM lane is the feature) by BN rows of y (the MMA N dimension: tokens); both operands
+// are K-major, as nn.Linear stores them, and arrive by TMA in 64-wide K slices with the
+// 128-byte swizzle.  Warp-specialised persistent CTAs, one per SM:
+//   warp 0    TMA producer: a ring of stages, each the w_o slice and the y slice
+//   warp 1    MMA issuer: four 128 x BN x 16 products per stage into one of two TMEM
+//             accumulators, a commit per stage releases it to the producer
+//   warps 2-5 epilogue: TMEM -> registers -> out, then the accumulator goes back to
+//             the MMA warp, so a tile's epilogue overlaps the next tile's products
+// Tiles are visited in groups of 8 feature tiles across every token tile, so the CTAs
+// running at one time share their w_o and y slices through L2.  BN = 256 when there are
+// enough tiles to fill the GPU (prompts), else 128 (the decode batch: 256 rows give 112
+// tiles over 7168 features, each streaming its 3 MB slice of w_o once).
+#include <cuda.h>
+#include <string.h>
 
-#include <mutex>
-
+#include "kda_chunk_common.cuh"
 #include "kda_internal.cuh"
+#include "kda_tc_ptx.cuh"
 
 namespace kda {
 namespace {
 
-std::mutex g_lt_mutex;
-cublasLtHandle_t g_lt = nullptr;
+using namespace tc;
+using chunk::sdesc_at;
 
-struct Plan {
-    int64_t M = -1;
-    int N = 0, K = 0, out_bf16 = -1;
-    size_t ws = 0;
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t a = nullptr, b = nullptr, c = nullptr;
-    cublasLtMatmulAlgo_t algo;
-    void release() {
-        if (op) cublasLtMatmulDescDestroy(op);
-        if (a) cublasLtMatrixLayoutDestroy(a);
-        if (b) cublasLtMatrixLayoutDestroy(b);
-        if (c) cublasLtMatrixLayoutDestroy(c);
-        op = nullptr;
-        a = b = c = nullptr;
-        M = -1;
-    }
+constexpr int BM = 128;                // output features per tile
+constexpr int BK = 64;                 // K per stage: one 128-byte swizzle row of bf16
+constexpr int kWarps = 6;              // 0: TMA, 1: MMA, 2-5: epilogue
+constexpr int kFeatureGroup = 8;       // feature tiles per raster group
+constexpr uint32_t kPolls = 1u << 26;  // bound on every mbarrier wait
+
+// Set by a CTA whose bounded wait gave up; its remaining output tiles hold NaN.
+__device__ int g_oproj_timeouts = 0;
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;  // w_o slice, 16 KB
+    static constexpr uint32_t B_BYTES = BN * BK * 2;  // y slice
+    static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+    static constexpr uint32_t BARS = STAGES * STAGE;  // full[S], empty[S], acc_full[2], acc_empty[2], drain
+    static constexpr uint32_t SMEM = BARS + (2 * STAGES + 5) * 8 + 16 + 1024;  // + tmem slot, abort flag
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
-Plan g_plan;
+static_assert(Cfg<256>::SMEM <= 232448 && Cfg<128>::SMEM <= 232448, "shared memory budget");
 
-kda_status lt_fail(const char *what, cublasStatus_t s) {
-    set_error("o_proj: %s failed (cublas status %d)", what, (int)s);
-    return KDA_ERR_CUDA;
+struct GemmArgs {
+    void *out;
+    int out_bf16;
+    int M, N, K;
+    int n_ft, n_tt, n_tiles;  // feature tiles, token tiles, all tiles
+};
+
+// Feature and token tile of tile id: groups of kFeatureGroup feature tiles, the feature
+// index fastest inside a group, then every token tile, then the next group.
+__device__ __forceinline__ void tile_coords(int id, int n_ft, int n_tt, int &f, int &t) {
+    const int per_group = kFeatureGroup * n_tt;
+    const int g = id / per_group, r = id % per_group;
+    const int f0 = g * kFeatureGroup, gsz = min(kFeatureGroup, n_ft - f0);
+    f = f0 + r % gsz;
+    t = r / gsz;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    oproj_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_y,
+                 const __grid_constant__ GemmArgs a) {
+    using L = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm), sb16 = sb >> 4;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BARS);
+    uint64_t *empty = full + L::STAGES;
+    uint64_t *acc_full = empty + L::STAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);  // a warp's bounded wait gave up
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KB = a.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full + i, 1);
+            mbar_init(acc_empty + i, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tb = *tmem_slot;
+    int failed = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---- TMA producer
+            uint32_t it = 0;
+            for (int id = blockIdx.x; id < a.n_tiles && !failed; id += gridDim.x) {
+                int f, t;
+                tile_coords(id, a.n_ft, a.n_tt, f, t);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % L::STAGES, use = it / L::STAGES;
+                    // the stage's previous use must have been read by its MMAs
+                    if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, kPolls)) {
+                        failed = 1;
+                        *abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + s, L::STAGE);
+                    tma_load_2d(sb + s * L::STAGE, &tmap_w, full + s, kb * BK, f * BM);
+                    tma_load_2d(sb + s * L::STAGE + L::A_BYTES, &tmap_y, full + s, kb * BK, t * BN);
+                }
+            }
+            // every load issued lands before the CTA may exit: wait for each stage's last use
+            const uint32_t n_issued = it;
+            for (uint32_t s = 0; s < (uint32_t)L::STAGES && s < n_issued; ++s) {
+                const uint32_t last = n_issued - 1 - ((n_issued - 1 + L::STAGES - s) % L::STAGES);
+                mbar_wait(full + s, (last / L::STAGES) & 1, kPolls);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---- MMA issuer
+            const uint32_t idesc = idesc_bf16(BM, BN, false, false);
+            uint32_t it = 0, tc = 0;
+            for (int id = blockIdx.x; id < a.n_tiles && !failed; id += gridDim.x, ++tc) {
+                const uint32_t acc = tc & 1, use = tc >> 1;
+                if (use > 0 && !mbar_wait(acc_empty + acc, (use - 1) & 1, kPolls)) {  // the epilogue has read it
+                    failed = 1;
+                    *abort_flag = 1;
+                    break;
+                }
+                fence_after_sync();
+                const uint32_t d = tb + acc * BN;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % L::STAGES;
+                    if (!mbar_wait(full + s, (it / L::STAGES) & 1, kPolls)) {
+                        failed = 1;
+                        *abort_flag = 1;
+                        break;
+                    }
+                    fence_after_sync();
+                    const uint32_t sa = s * L::STAGE, sbb = sa + L::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_ss(d, sdesc_at(sb16, sa + k * 32, 16, 1024), sdesc_at(sb16, sbb + k * 32, 16, 1024), idesc,
+                               (kb | k) ? 1u : 0u);
+                    mma_commit(empty + s);  // the stage is free once these products have read it
+                }
+                if (failed) break;
+                mma_commit(acc_full + acc);
+            }
+            // nothing issued may still run when the accumulators are freed
+            mma_commit(drain);
+            mbar_wait(drain, 0, kPolls);
+        }
+    } else {  // ---- epilogue, warps 2-5: TMEM lane quarter warp % 4
+        const int q = warp & 3, m = q * 32 + lane;
+        const uint32_t lane_base = tb + ((uint32_t)(q * 32) << 16);
+        uint32_t tc = 0;
+        for (int id = blockIdx.x; id < a.n_tiles; id += gridDim.x, ++tc) {
+            int f, t;
+            tile_coords(id, a.n_ft, a.n_tt, f, t);
+            const uint32_t acc = tc & 1, use = tc >> 1;
+            const bool ok = !failed && !*abort_flag && mbar_wait(acc_full + acc, use & 1, kPolls);
+            if (!ok) failed = 1;
+            fence_after_sync();
+            const int feat = f * BM + m;
+            const int t0 = t * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r0[16], r1[16];
+                if (ok) {
+                    tmem_ld16(lane_base + acc * BN + c0, r0);
+                    tmem_ld16(lane_base + acc * BN + c0 + 16, r1);
+                    tmem_wait_ld();
+                }
+                const int nrow = min(32, a.M - (t0 + c0));
+                if (a.out_bf16) {
+                    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(a.out) + (size_t)(t0 + c0) * a.N + feat;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nrow)
+                            o[(size_t)j * a.N] = __float2bfloat16_rn(
+                                ok ? __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) : __int_as_float(0x7fc00000));
+                } else {
+                    float *o = reinterpret_cast<float *>(a.out) + (size_t)(t0 + c0) * a.N + feat;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nrow) o[(size_t)j * a.N] = ok ? __uint_as_float(j < 16 ? r0[j] : r1[j - 16]) : __int_as_float(0x7fc00000);
+                }
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(acc_empty + acc);
+        }
+    }
+    fence_before_sync();
+    if (__syncthreads_or(failed) && threadIdx.x == 0) atomicAdd(&g_oproj_timeouts, 1);
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tb, L::TMEM_COLS);
 }
 
 }  // namespace
 
-kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, int64_t M, int K, int N, void *ws,
-                         size_t ws_bytes, cudaStream_t st) {
-    std::lock_guard<std::mutex> lock(g_lt_mutex);
-    cublasStatus_t s;
-    if (!g_lt && (s = cublasLtCreate(&g_lt)) != CUBLAS_STATUS_SUCCESS) return lt_fail("cublasLtCreate", s);
-    Plan &pl = g_plan;
-    if (pl.M != M || pl.N != N || pl.K != K || pl.out_bf16 != out_bf16 || pl.ws != ws_bytes) {
-        pl.release();
-        if ((s = cublasLtMatmulDescCreate(&pl.op, CUBLAS_COMPUTE_32F, CUDA_R_32F)) != CUBLAS_STATUS_SUCCESS)
-            return lt_fail("cublasLtMatmulDescCreate", s);
-        const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-        cublasLtMatmulDescSetAttribute(pl.op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta));
-        cublasLtMatmulDescSetAttribute(pl.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb));
-        if ((s = cublasLtMatrixLayoutCreate(&pl.a, CUDA_R_16BF, K, N, K)) != CUBLAS_STATUS_SUCCESS ||
-            (s = cublasLtMatrixLayoutCreate(&pl.b, CUDA_R_16BF, K, M, K)) != CUBLAS_STATUS_SUCCESS ||
-            (s = cublasLtMatrixLayoutCreate(&pl.c, out_bf16 ? CUDA_R_16BF : CUDA_R_32F, N, M, N)) !=
-                CUBLAS_STATUS_SUCCESS) {
-            pl.release();
-            return lt_fail("cublasLtMatrixLayoutCreate", s);
-        }
-        cublasLtMatmulPreference_t pref = nullptr;
-        cublasLtMatmulPreferenceCreate(&pref);
-        cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes, sizeof(ws_bytes));
-        cublasLtMatmulHeuristicResult_t res;
-        int found = 0;
-        s = cublasLtMatmulAlgoGetHeuristic(g_lt, pl.op, pl.a, pl.b, pl.c, pl.c, pref, 1, &res, &found);
-        cublasLtMatmulPreferenceDestroy(pref);
-        if (s != CUBLAS_STATUS_SUCCESS || found == 0) {
-            pl.release();
-            set_error("o_proj: no cuBLASLt algorithm for M=%lld N=%d K=%d", (long long)M, N, K);
-            return KDA_ERR_UNSUPPORTED;
-        }
-        pl.algo = res.algo;
-        pl.M = M;
-        pl.N = N;
-        pl.K = K;
-        pl.out_bf16 = out_bf16;
-        pl.ws = ws_bytes;
+int take_oproj_timeouts(cudaStream_t st) {
+    int n = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&n, g_oproj_timeouts, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_oproj_timeouts, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        set_error("o_proj: cannot read the timeout counter: %s", cudaGetErrorString(cudaGetLastError()));
+        return -1;
     }
-    const float alpha = 1.f, beta = 0.f;
-    s = cublasLtMatmul(g_lt, pl.op, &alpha, w, pl.a, y, pl.b, &beta, out, pl.c, out, pl.c, &pl.algo, ws, ws_bytes, st);
-    if (s != CUBLAS_STATUS_SUCCESS) return lt_fail("cublasLtMatmul", s);
+    return n;
+}
+
+bool o_proj_supported(int K, int N) { return K % BK == 0 && N % BM == 0; }
+
+kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, int64_t M, int K, int N,
+                         cudaStream_t st) {
+    if (!o_proj_supported(K, N)) {
+        set_error("o_proj: in_features must be a multiple of %d and out_features of %d", BK, BM);
+        return KDA_ERR_UNSUPPORTED;
+    }
+    if (M == 0) return KDA_OK;
+    chunk::EncodeTiledFn enc = reinterpret_cast<chunk::EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) {
+        set_error("o_proj: cuTensorMapEncodeTiled is not available from the driver");
+        return KDA_ERR_CUDA;
+    }
+    const int sms = sm_count();
+    const int n_ft = N / BM;
+    const int n_tt256 = (int)((M + 255) / 256);
+    const int BN = (int64_t)n_ft * n_tt256 >= sms ? 256 : 128;
+    const int n_tt = (int)((M + BN - 1) / BN);
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap tw, ty;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+        const CUresult r = enc(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w), dims, strides, box,
+                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            set_error("o_proj: cuTensorMapEncodeTiled failed for w_o (%d)", (int)r);
+            return KDA_ERR_CUDA;
+        }
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
+        const CUresult r = enc(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(y), dims, strides, box,
+                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            set_error("o_proj: cuTensorMapEncodeTiled failed for y (%d)", (int)r);
+            return KDA_ERR_CUDA;
+        }
+    }
+    static DeviceOnce configured;
+    const int dev = current_device();
+    if (!configured.done(dev)) {
+        cudaError_t e = cudaFuncSetAttribute(oproj_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<256>::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(oproj_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::SMEM);
+        if (e != cudaSuccess) {
+            set_error("o_proj: cannot reserve shared memory: %s", cudaGetErrorString(e));
+            return KDA_ERR_CUDA;
+        }
+        configured.set(dev);
+    }
+    GemmArgs ga;
+    memset(&ga, 0, sizeof(ga));
+    ga.out = out;
+    ga.out_bf16 = out_bf16;
+    ga.M = (int)M;
+    ga.N = N;
+    ga.K = K;
+    ga.n_ft = n_ft;
+    ga.n_tt = n_tt;
+    ga.n_tiles = n_ft * n_tt;
+    const int grid = ga.n_tiles < sms ? ga.n_tiles : sms;
+    if (BN == 256)
+        oproj_kernel<256><<<grid, kWarps * 32, Cfg<256>::SMEM, st>>>(tw, ty, ga);
+    else
+        oproj_kernel<128><<<grid, kWarps * 32, Cfg<128>::SMEM, st>>>(tw, ty, ga);
     note_launch();
-    return check_launch("o_proj (cuBLASLt)");
+    return check_launch("oproj_kernel");
 }
 
 }  // namespace kda

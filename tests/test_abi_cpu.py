@@ -243,10 +243,11 @@ def test_short_conv_rejects_bad_cu_seqlens(lib):
 
 def test_o_proj_rejects(lib):
     f = lib.kda_o_proj
-    ws = ctypes.c_size_t
-    assert f(None, FAKE, FAKE, BF16, ctypes.c_int64(4), 64, 64, None, ws(0), None) == INVALID
-    assert f(FAKE, FAKE, FAKE, BF16, ctypes.c_int64(4), 60, 64, None, ws(0), None) == UNSUPPORTED
-    assert f(FAKE, FAKE, FAKE, 9, ctypes.c_int64(4), 64, 64, None, ws(0), None) == UNSUPPORTED
-    assert f(FAKE, FAKE, FAKE, BF16, ctypes.c_int64(4), 64, 64, None, ws(1024), None) == INVALID
-    assert f(FAKE + 4, FAKE, FAKE, BF16, ctypes.c_int64(4), 64, 64, None, ws(0), None) == INVALID
-    assert f(None, None, None, BF16, ctypes.c_int64(0), 64, 64, None, ws(0), None) == OK  # nothing to do
+    rows = ctypes.c_int64
+    assert f(None, fake(1), fake(2), BF16, rows(4), 64, 128, None) == INVALID
+    assert f(fake(0), fake(1), fake(2), BF16, rows(4), 96, 128, None) == UNSUPPORTED   # in_features % 64
+    assert f(fake(0), fake(1), fake(2), BF16, rows(4), 64, 64, None) == UNSUPPORTED    # out_features % 128
+    assert f(fake(0), fake(1), fake(2), 9, rows(4), 64, 128, None) == UNSUPPORTED
+    assert f(fake(0) + 4, fake(1), fake(2), BF16, rows(4), 64, 128, None) == INVALID   # misaligned
+    assert f(fake(0), fake(1), fake(0) + 256, BF16, rows(4), 64, 128, None) == INVALID  # out overlaps y
+    assert f(None, None, None, BF16, rows(0), 64, 128, None) == OK                      # nothing to do

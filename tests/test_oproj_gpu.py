@@ -1,7 +1,7 @@
-"""GPU parity of the output projection (kda_o_proj, cuBLASLt bf16 GEMM, fp32 accumulation)
-against the oracle's fp64 matmul of the same bf16 inputs: a ragged small case in fp32 and
-bf16 output, and the decode / prefill shapes of the layer (12288 -> 7168) on sampled
-output columns.  Tolerance: fp32 accumulation over K terms of unit-scale products
+"""GPU parity of the output projection (kda_o_proj, the library's tcgen05 GEMM: bf16
+operands, fp32 accumulation) against the oracle's fp64 matmul of the same bf16 inputs:
+ragged small cases in fp32 and bf16 output on both tile widths, the decode shape of the
+layer (256 x 12288 -> 7168) element by element and the prefill shape on sampled outputs.  Tolerance: fp32 accumulation over K terms of unit-scale products
 (max|diff| / rms 1e-4); bf16 outputs add one rounding per element (2^-8 relative)."""
 import numpy as np
 import pytest
@@ -22,9 +22,43 @@ def _data(rows, K, N, seed):
     return y, w
 
 
+def _check(out, ref, out_dtype):
+    if out_dtype == torch.float32:
+        assert rel_err(out, ref) <= 1e-4
+    else:  # one bf16 rounding of each output (half an ulp: 2^-9 relative) on top of fp32 accumulation
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        assert np.all(np.abs(out.double().cpu().numpy() - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * rms)
+
+
+@pytest.mark.parametrize("rows,K,N", [(1, 512, 1024), (129, 512, 1024), (300, 256, 640),
+                                      (700, 256, 7168)])  # the last one fills the GPU: 256-row tiles
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_tile_edges(rows, K, N, out_dtype):
+    """Row counts that end inside a token tile, on the 128- and 256-row tile widths."""
+    y, w = _data(rows, K, N, rows)
+    out = kda.o_proj(y, w, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    _check(out, oracle.o_proj(y.float().cpu().numpy(), w.float().cpu().numpy()), out_dtype)
+
+
+def test_decode_shape_every_element():
+    """The decode batch of the layer: 256 rows x 12288 -> 7168, every output element."""
+    y, w = _data(256, 12288, 7168, 11)
+    out = kda.o_proj(y, w, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    kda.device_status()
+    assert rel_err(out, oracle.o_proj(y.float().cpu().numpy(), w.float().cpu().numpy())) <= 1e-4
+
+
+def test_unsupported_feature_counts():
+    y, w = _data(4, 1000, 768, 3)
+    with pytest.raises(kda.KDAError):
+        kda.o_proj(y, w)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_small_ragged(out_dtype):
-    y, w = _data(37, 1024, 776, 0)
+    y, w = _data(37, 1024, 768, 0)
     out = kda.o_proj(y, w, out_dtype=out_dtype)
     torch.cuda.synchronize()
     ref = oracle.o_proj(y.float().cpu().numpy(), w.float().cpu().numpy())
