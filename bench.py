@@ -240,11 +240,11 @@ def prefill_inputs(device, T=None):
     return make_inputs("prefill", device=device, T=T)
 
 
-def bench_prefill(args, world, rank, peaks, fused=False):
-    """The headline prefill: the split tensor-core form (state-independent pre-pass over all
-    chunks and heads, then the per-head chain kernel) unless fused=True (one kernel per
-    (sequence, head), no workspace).  `kernel_ms` is the device time of the whole call,
-    both kernels of the split form together."""
+def bench_prefill(args, world, rank, peaks, fused=True):
+    """The headline prefill: the fused tensor-core form (one kernel per (sequence, head), no
+    workspace), or with fused=False the split form (state-independent pre-pass over all
+    chunks and heads, then the per-head chain kernel).  `kernel_ms` is the device time of
+    the whole call, both kernels of the split form together."""
     import torch
     import kimi_delta_attention_gated_gb300 as kda
     d = prefill_inputs("cuda", args.prefill_T)
@@ -254,7 +254,7 @@ def bench_prefill(args, world, rank, peaks, fused=False):
     ws = None if fused else torch.empty(kda.workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
     fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, scale=d["scale"], chunk=64,
                                o=o, final_state=fs, mode=args.mode, workspace=ws)
-    r = time_steps(fn, args.steps, args.warmup, world, clocks_index=None if fused else torch.cuda.current_device())
+    r = time_steps(fn, args.steps, args.warmup, world, clocks_index=torch.cuda.current_device() if fused else None)
     th = B * T * H
     kernel_ms = r["call_ms"]
     algo_bytes = th * PREFILL_BYTES_PER_TH + B * H * STATE_BYTES
@@ -641,8 +641,8 @@ def main():
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
-    pre, d = bench_prefill(args, world, rank, peaks)
-    fused = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, fused=True)[0]
+    pre, d = bench_prefill(args, world, rank, peaks, fused=True)
+    split = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, fused=False)[0]
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
     conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
     logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
@@ -669,14 +669,14 @@ def main():
         "e2e": e2e, "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "decode": dec,
         "short_conv": conv, "prefill_gate_logits": logits, "prefill_gated_norm": norm, "o_proj": oproj,
         "prefill_varlen": varlen, "prefill_long_norm": long_, "gpu": torch.cuda.get_device_name(),
-        "prefill_fused_one_kernel": None if fused is None else {
-            "value": fused["value"], "ms_per_step": fused["ms_per_step"], "roofline": fused["roofline"]},
+        "prefill_split_two_kernels": None if split is None else {
+            "value": split["value"], "ms_per_step": split["ms_per_step"], "roofline": split["roofline"]},
     }
-    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj, fused)
+    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split)
     print(json.dumps(line), flush=True)
 
 
-def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, fused=None):
+def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split=None):
     """Every timed workload in a few numbers, last on the line so that a reader of the
     line's tail sees all of them: kernel ms per launch, throughput and the fraction of
     the binding roofline (of the measured peak)."""
@@ -689,7 +689,7 @@ def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, fused=None):
     out = {"prefill_T8192": row(pre, 1e6, "Mtok_s"), "prefill_varlen": row(varlen, 1e6, "Mtok_s"),
            "prefill_long_norm": row(long_, 1e6, "Mtok_s"), "decode_B256": row(dec, 1e3, "Ktok_s"),
            "prefill_logits": row(logits, 1e6, "Mtok_s"), "prefill_norm_bf16": row(norm, 1e6, "Mtok_s"),
-           "prefill_T8192_fused": row(fused, 1e6, "Mtok_s")}
+           "prefill_T8192_split": row(split, 1e6, "Mtok_s")}
     if conv:
         out["conv_prefill"] = row(conv["conv_prefill"], 1e6, "Mtok_s")
         out["conv_decode"] = row(conv["conv_decode"], 1e6, "Mtok_s")

@@ -185,17 +185,19 @@ def _dev_out(t):
 def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use_qk_l2norm=True,
               cu_seqlens=None, output_final_state=True, gate=None, norm_w=None, eps=1e-5,
               out_dtype=torch.float32, mode="auto", return_o=True, o=None, y=None, final_state=None,
-              workspace="auto"):
+              workspace=None):
     """Chunked prefill.  q, k [B,T,H,K]; v [B,T,H,V]; g [B,T,H,K] fp32; beta [B,T,H] fp32;
     initial_state [N,H,K,V] fp32 or None.  With ``cu_seqlens`` (int, n_seqs + 1) B must be 1.
     Returns (o, final_state) or, with ``gate``/``norm_w``, (o, final_state, y) where
     y [B,T,H*V] is the sigmoid-gated RMSNorm of o (o is None when return_o=False).
     Preallocated outputs may be passed as o / y / final_state (final_state may be
-    initial_state itself for an in-place update).  ``workspace``: "auto" (a per-device
-    buffer this binding keeps, which selects the split tensor-core form), a uint8 device
-    tensor of at least workspace_size(...) bytes, or None (the fused one-kernel form).
-    The kept buffer is shared by every "auto" call on a device: calls on streams that
-    may run at the same time need workspaces of their own."""
+    initial_state itself for an in-place update).  ``workspace``: None (the default: the
+    fused one-kernel tensor-core form, the faster one on every measured workload), a uint8
+    device tensor of at least workspace_size(...) bytes, or "auto" (a per-device buffer this
+    binding keeps); either of the last two selects the split form (a state-independent
+    pre-pass over all chunks and heads, then the per-head chain kernel).  The kept buffer is
+    shared by every "auto" call on a device: calls on streams that may run at the same time
+    need workspaces of their own."""
     return _chunk(q, k, v, (g, beta), None, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens,
                   output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace)
 
@@ -203,7 +205,7 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
 def chunk_fwd_logits(q, k, v, g_logits, beta_logits, A_log, initial_state=None, *, dt_bias=None,
                      g_lower_bound=-5.0, scale=None, chunk=64, use_qk_l2norm=True, cu_seqlens=None,
                      output_final_state=True, gate=None, norm_w=None, eps=1e-5, out_dtype=torch.float32,
-                     mode="auto", return_o=True, o=None, y=None, final_state=None, workspace="auto"):
+                     mode="auto", return_o=True, o=None, y=None, final_state=None, workspace=None):
     """chunk_fwd with g = max(g_lower_bound, -exp(A_log[h]) * softplus(g_logits + dt_bias)) and
     beta = sigmoid(beta_logits) computed inside the kernels.  g_logits [B,T,H,K] and
     beta_logits [B,T,H] in bf16 or fp32; A_log [H]; dt_bias [H,K] (or [H*K]) or None;
@@ -249,7 +251,7 @@ def _pinned(t):
 
 
 def _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, output_final_state, gate,
-                         norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace="auto"):
+                         norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace=None):
     """A host-resident prompt (B = 1) through the device in HOST_SEGMENT-token segments on
     three streams: segment i+1's inputs are copied in while segment i runs (its state
     handed on in place on the device) and segment i-1's outputs are copied out, so the
@@ -375,7 +377,7 @@ HOST_SEGMENT = 1024
 
 
 def _chunk(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens, output_final_state, gate,
-           norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace="auto"):
+           norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace=None):
     lib = _load()
     host = q.device.type != "cuda"
     if (host and cu_seqlens is None and q.shape[0] == 1 and q.shape[1] >= 2 * HOST_SEGMENT

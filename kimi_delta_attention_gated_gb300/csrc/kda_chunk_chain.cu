@@ -53,13 +53,18 @@ using namespace chunk;
 constexpr int kThreads = 512;  // 16 warps: pass warps 0-7, prep warps 8-15
 constexpr int kGroup = 256;    // threads per group
 
-// TMEM columns (the fused kernel's, with the gram's columns holding D)
-constexpr uint32_t T_R = 0, T_O = 64, T_S = 128, T_SH = 256, T_SL = 320, T_D = 384;
+// TMEM columns.  The R/O product writes [R_hh | O_hh | R_hl | O_hl] over [0, 256): the hi
+// part of S^T against the hi and lo [-Kd ; Qd] rows stacked along N (one N = 256 product
+// per K step), then the lo part against the hi rows onto [R | O] at [0, 128).  The R pass
+// folds R_hl into R (split into hi/lo in place at [0, 64)) and O_hh into O at [192, 256),
+// which lies just before S^T so that the O/S product writes [O | S] as one N = 192 block;
+// the D accumulator takes the columns [64, 192) the R pass has freed.
+constexpr uint32_t T_R = 0, T_D = 64, T_O = 192, T_S = 256, T_SH = 384, T_SL = 448;
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t S_V = 0;          // V tile, two TMA boxes of 64 tokens x 64 values (16 KB)
-constexpr uint32_t S_KQH = 16384;    // [-Kd ; Qd] hi, 128 rows x 128 (32 KB)
-constexpr uint32_t S_KQL = 49152;    // [-Kd ; Qd] lo
+constexpr uint32_t S_KQ = 16384;     // [-Kd ; Qd], 128 rows x 128 (64 KB): per 64 key channels, the hi rows
+                                     // then the lo rows (16 KB each), i.e. one 256-row operand per K block
 constexpr uint32_t S_GT = 81920;     // g (or logits) tile of the chunk being prepared, 64 tokens x 128 (32 KB)
 constexpr uint32_t S_PKGH = 114688;  // [P ; Kg^T] hi, 192 rows (i, then c) x 64 (j) (24 KB), K-major B
 constexpr uint32_t S_PKGL = 139264;  // [P ; Kg^T] lo
@@ -217,8 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_tb(0);
             issue_p(0);
         }
-        {  // initial state -> S^T accumulator and its hi/lo copy; O^T = 0 (channels 64 hf..)
+        // The fp32 accumulator holds the state already decayed by the chunk about to be
+        // processed (S^T exp(gamma), ready for the O/S product), while the hi/lo copy that the
+        // R/O product reads holds it undecayed: each state pass writes both.  The first
+        // chunk's exp(gamma) comes from the prep warps, published with its tiles.
+        const bool have_first = nchunks > 0 && mbar_wait(tiles_bar, 0u, kPolls);
+        if (nchunks > 0 && !have_first) failed = 1;
+        {  // initial state -> S^T accumulator and its hi/lo copy (channels 64 hf..)
             const int c0 = hf * 64;
+            const float *ge = fs + F_GEXP + c0;  // exp(gamma) of chunk 0 (parity 0)
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
                 float s[32];
@@ -229,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) r[c] = __float_as_uint(s[half * 16 + c]);
+                    for (int c = 0; c < 16; ++c)
+                        r[c] = __float_as_uint(have_first ? s[half * 16 + c] * ge[qq * 32 + half * 16 + c] : s[half * 16 + c]);
                     tmem_st16(tb + lane_off + T_S + c0 + qq * 32 + half * 16, r);
                 }
 #pragma unroll
@@ -237,11 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st16(tb + lane_off + T_SH + (c0 + qq * 32) / 2, hi);
                 tmem_st16(tb + lane_off + T_SL + (c0 + qq * 32) / 2, lo);
             }
-            uint32_t z[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) z[c] = 0u;
-            tmem_st16(tb + lane_off + T_O + hf * 32, z);
-            tmem_st16(tb + lane_off + T_O + hf * 32 + 16, z);
             tmem_wait_st();
         }
         auto wait_bar = [&](uint64_t *bar, int parity) {
@@ -249,11 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_after_sync();
             return ok;
         };
-        // splits 16 fp32 columns (two blocks of 8 pairs) in place into [hi x 8 | lo x 8]
-        auto split_block = [&](uint32_t col) {
-            uint32_t r[16], hi[8], lo[8];
-            tmem_ld16(tb + lane_off + col, r);
-            tmem_wait_ld();
+        // splits 16 fp32 columns (two blocks of 8 pairs) already in registers into [hi x 8 | lo x 8]
+        auto split_store = [&](uint32_t col, const uint32_t (&r)[16]) {
+            uint32_t hi[8], lo[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) split2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
             tmem_st8(tb + lane_off + col, hi);
@@ -276,20 +282,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     failed = 1;
                 fence_after_sync();
+                const uint32_t id256 = idesc_bf16(128, 256, false, false), id128 = idesc_bf16(128, 128, false, false);
                 const uint32_t id_mn = idesc_bf16(128, 64, true, false);
 #pragma unroll 1
-                for (int s = 0; s < 4; ++s)
-                    mma_ss(tb + T_R, sdesc_at(sb16, S_V + s * 2048, 8192, 1024), sdesc_at(sb16, S_ID + s * 32, 16, 1024),
-                           id_mn, s ? 1u : 0u);
-                const uint32_t id128 = idesc_bf16(128, 128, false, false);
-#pragma unroll
-                for (int cb = 0; cb < 3; ++cb)
+                for (int s = 0; s < 8; ++s) {  // S^T_hi [KQ_hi ; KQ_lo]^T -> [R_hh | O_hh | R_hl | O_hl]
+                    const uint32_t koff = (s >> 2) * 32768 + (s & 3) * 32;
+                    mma_ts(tb + T_R, tb + T_SH + s * 8, sdesc_at(sb16, S_KQ + koff, 16, 1024), id256, s ? 1u : 0u);
+                }
 #pragma unroll 1
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t a = tb + (combo_a(cb) ? T_SL : T_SH) + s * 8;
-                        const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
-                        mma_ts(tb + T_R, a, sdesc_at(sb16, (combo_b(cb) ? S_KQL : S_KQH) + koff, 16, 1024), id128, 1u);
-                    }
+                for (int s = 0; s < 4; ++s)  // + V^T (exact bf16 identity) onto R
+                    mma_ss(tb + T_R, sdesc_at(sb16, S_V + s * 2048, 8192, 1024), sdesc_at(sb16, S_ID + s * 32, 16, 1024),
+                           id_mn, 1u);
+#pragma unroll 1
+                for (int s = 0; s < 8; ++s) {  // S^T_lo KQ_hi^T onto [R | O]
+                    const uint32_t koff = (s >> 2) * 32768 + (s & 3) * 32;
+                    mma_ts(tb + T_R, tb + T_SL + s * 8, sdesc_at(sb16, S_KQ + koff, 16, 1024), id128, 1u);
+                }
                 mma_commit(bar_r);
                 // fused norm, bf16 gate: this chunk's gate tile, read by the O pass (the previous
                 // O pass has finished with the buffer)
@@ -304,8 +312,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ================= R pass: R^T (lane v, tokens 32 hf..) -> hi/lo in place
             if (!wait_bar(bar_r, par)) failed = 1;
             if (tid == 0 && ch + 1 < nchunks && !failed) issue_v(ch + 1);  // the V tile has been read
-            split_block(T_R + hf * 32);
-            split_block(T_R + hf * 32 + 16);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {  // tokens 32 hf + 16 b ..: R = R_hh + R_hl, O = O_hh + O_hl
+                const uint32_t col = hf * 32 + b * 16;
+                uint32_t rh[16], rl[16], oh[16], ol[16];
+                tmem_ld16(tb + lane_off + T_R + col, rh);
+                tmem_ld16(tb + lane_off + T_R + 128 + col, rl);
+                tmem_ld16(tb + lane_off + T_R + 64 + col, oh);
+                tmem_ld16(tb + lane_off + T_R + 192 + col, ol);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    const float2 rv = __fadd2_rn(make_float2(__uint_as_float(rh[c]), __uint_as_float(rh[c + 1])),
+                                                 make_float2(__uint_as_float(rl[c]), __uint_as_float(rl[c + 1])));
+                    const float2 ov = __fadd2_rn(make_float2(__uint_as_float(oh[c]), __uint_as_float(oh[c + 1])),
+                                                 make_float2(__uint_as_float(ol[c]), __uint_as_float(ol[c + 1])));
+                    rh[c] = __float_as_uint(rv.x); rh[c + 1] = __float_as_uint(rv.y);
+                    oh[c] = __float_as_uint(ov.x); oh[c + 1] = __float_as_uint(ov.y);
+                }
+                split_store(T_R + col, rh);
+                tmem_st16(tb + lane_off + T_O + col, oh);
+            }
             tmem_wait_st();
             fence_before_sync();
             if (group_sync_or<1, kGroup>(failed)) break;
@@ -330,44 +357,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
 
-            // ================= D pass (D = D_a + D_b -> hi/lo in place) and S decay by exp(gamma)
+            // ================= D pass: D = D_a + D_b -> hi/lo in place
             if (!wait_bar(bar_d, par)) failed = 1;
             if (tid == 0 && ch + 1 < nchunks && !failed) issue_tb(ch + 1);  // the T diag(beta) tile has been read
             {
+                const uint32_t col = T_D + hf * 32;
+                uint32_t a0[16], a1[16], b0[16], b1[16];
+                tmem_ld16(tb + lane_off + col, a0);
+                tmem_ld16(tb + lane_off + col + 16, a1);
+                tmem_ld16(tb + lane_off + col + 64, b0);
+                tmem_ld16(tb + lane_off + col + 80, b1);
+                tmem_wait_ld();
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const uint32_t col = T_D + hf * 32 + b * 16;
-                    uint32_t r[16], rb[16], hi[8], lo[8];
-                    tmem_ld16(tb + lane_off + col, r);
-                    tmem_ld16(tb + lane_off + col + 64, rb);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float2 v = __fadd2_rn(make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])),
-                                                    make_float2(__uint_as_float(rb[2 * c]), __uint_as_float(rb[2 * c + 1])));
-                        split2(v.x, v.y, hi[c], lo[c]);
-                    }
-                    tmem_st8(tb + lane_off + col, hi);
-                    tmem_st8(tb + lane_off + col + 8, lo);
+                for (int c = 0; c < 16; c += 2) {
+                    const float2 v0 = __fadd2_rn(make_float2(__uint_as_float(a0[c]), __uint_as_float(a0[c + 1])),
+                                                 make_float2(__uint_as_float(b0[c]), __uint_as_float(b0[c + 1])));
+                    const float2 v1 = __fadd2_rn(make_float2(__uint_as_float(a1[c]), __uint_as_float(a1[c + 1])),
+                                                 make_float2(__uint_as_float(b1[c]), __uint_as_float(b1[c + 1])));
+                    a0[c] = __float_as_uint(v0.x); a0[c + 1] = __float_as_uint(v0.y);
+                    a1[c] = __float_as_uint(v1.x); a1[c + 1] = __float_as_uint(v1.y);
                 }
-                const float *ge = fs + F_GEXP + par * 128 + hf * 64;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    uint32_t s1[16];
-                    tmem_ld16(tb + lane_off + T_S + hf * 64 + qq * 16, s1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const float4 a = *reinterpret_cast<const float4 *>(ge + qq * 16 + c4 * 4);
-                        const float2 x0 = __fmul2_rn(make_float2(__uint_as_float(s1[4 * c4]), __uint_as_float(s1[4 * c4 + 1])),
-                                                     make_float2(a.x, a.y));
-                        const float2 x1 = __fmul2_rn(
-                            make_float2(__uint_as_float(s1[4 * c4 + 2]), __uint_as_float(s1[4 * c4 + 3])), make_float2(a.z, a.w));
-                        s1[4 * c4 + 0] = __float_as_uint(x0.x); s1[4 * c4 + 1] = __float_as_uint(x0.y);
-                        s1[4 * c4 + 2] = __float_as_uint(x1.x); s1[4 * c4 + 3] = __float_as_uint(x1.y);
-                    }
-                    tmem_st16(tb + lane_off + T_S + hf * 64 + qq * 16, s1);
-                }
+                split_store(col, a0);
+                split_store(col + 16, a1);
                 tmem_wait_st();
             }
             fence_before_sync();
@@ -396,33 +407,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ================= O pass (+ gated norm) and state pass
             if (!wait_bar(bar_s, par)) failed = 1;
             if (tid == 0 && ch + 1 < nchunks && !failed) issue_p(ch + 1);  // the P rows have been read
+            // the next chunk's exp(gamma), published by the prep warps with its tiles
+            const bool next = ch + 1 < nchunks;
+            if (next && !mbar_wait(tiles_bar, (uint32_t)((ch + 1) & 1), kPolls)) failed = 1;
             {
-                // S^T channels 64 hf.. as packed hi/lo pairs
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    uint32_t s1[16], hi[8], lo[8];
-                    tmem_ld16(tb + lane_off + T_S + hf * 64 + qq * 16, s1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        split2(__uint_as_float(s1[2 * c]), __uint_as_float(s1[2 * c + 1]), hi[c], lo[c]);
-                    tmem_st8(tb + lane_off + T_SH + hf * 32 + qq * 8, hi);
-                    tmem_st8(tb + lane_off + T_SL + hf * 32 + qq * 8, lo);
-                }
+                const float *ge = fs + F_GEXP + ((ch + 1) & 1) * 128 + hf * 64;
                 uint32_t r[32];
-                {
-                    uint32_t a[16], b[16];
-                    tmem_ld16(tb + lane_off + T_O + hf * 32, a);
-                    tmem_ld16(tb + lane_off + T_O + hf * 32 + 16, b);
-                    tmem_wait_ld();
+                // S^T channels 64 hf..: the hi/lo copy of the state the next chunk starts from,
+                // and the fp32 accumulator decayed by that chunk's exp(gamma)
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        r[c] = a[c];
-                        r[16 + c] = b[c];
-                        a[c] = 0u;
+                for (int qh = 0; qh < 2; ++qh) {
+                    uint32_t s0[16], s1[16];
+                    tmem_ld16(tb + lane_off + T_S + hf * 64 + qh * 32, s0);
+                    tmem_ld16(tb + lane_off + T_S + hf * 64 + qh * 32 + 16, s1);
+                    if (qh == 0) {
+                        uint32_t o0[16], o1[16];  // (the next R/O product overwrites these columns)
+                        tmem_ld16(tb + lane_off + T_O + hf * 32, o0);
+                        tmem_ld16(tb + lane_off + T_O + hf * 32 + 16, o1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            r[c] = o0[c];
+                            r[16 + c] = o1[c];
+                        }
+                    } else {
+                        tmem_wait_ld();
                     }
-                    tmem_st16(tb + lane_off + T_O + hf * 32, a);  // O^T starts from zero next chunk
-                    tmem_st16(tb + lane_off + T_O + hf * 32 + 16, a);
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        uint32_t(&sv)[16] = b ? s1 : s0;
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            split2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), hi[c], lo[c]);
+                        tmem_st8(tb + lane_off + T_SH + hf * 32 + qh * 16 + b * 8, hi);
+                        tmem_st8(tb + lane_off + T_SL + hf * 32 + qh * 16 + b * 8, lo);
+                        if (next) {
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                const float4 a = *reinterpret_cast<const float4 *>(ge + qh * 32 + b * 16 + c4 * 4);
+                                const float2 x0 = __fmul2_rn(
+                                    make_float2(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), make_float2(a.x, a.y));
+                                const float2 x1 = __fmul2_rn(
+                                    make_float2(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])), make_float2(a.z, a.w));
+                                sv[4 * c4 + 0] = __float_as_uint(x0.x); sv[4 * c4 + 1] = __float_as_uint(x0.y);
+                                sv[4 * c4 + 2] = __float_as_uint(x1.x); sv[4 * c4 + 3] = __float_as_uint(x1.y);
+                            }
+                            tmem_st16(tb + lane_off + T_S + hf * 64 + qh * 32 + b * 16, sv);
+                        }
+                    }
                 }
                 const int v = m, i0 = hf * 32;
                 const int rows = min(32, cn - i0);
@@ -691,16 +724,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 kgv[r][e] = ke * rk * __expf(gam[e] - ge);
                             }
                     }
-                    const uint32_t off = sw128_off(i, l4, 128);  // rows i and 64 + i share the swizzle phase
+                    // rows i and 64 + i share the swizzle phase; each 64-channel block holds the
+                    // 128 hi rows, then the 128 lo rows
+                    const uint32_t off = sw128_off(i, l4 & 63, 128) + (uint32_t)(l4 >> 6) * 32768u;
                     uint32_t h0, lo0, h1, lo1;
                     split2(kd[0].x, kd[0].y, h0, lo0);
                     split2(kd[1].x, kd[1].y, h1, lo1);
-                    st_shared_v2(sb + S_KQH + off, h0, h1);
-                    st_shared_v2(sb + S_KQL + off, lo0, lo1);
+                    st_shared_v2(sb + S_KQ + off, h0, h1);
+                    st_shared_v2(sb + S_KQ + off + 16384, lo0, lo1);
                     split2(qd[0].x, qd[0].y, h0, lo0);
                     split2(qd[1].x, qd[1].y, h1, lo1);
-                    st_shared_v2(sb + S_KQH + off + 8192, h0, h1);
-                    st_shared_v2(sb + S_KQL + off + 8192, lo0, lo1);
+                    st_shared_v2(sb + S_KQ + off + 8192, h0, h1);
+                    st_shared_v2(sb + S_KQ + off + 8192 + 16384, lo0, lo1);
                 }
             }
             fence_async_smem();

@@ -987,15 +987,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ssl = red[(wg * 4 + 0) * 16 + cl] + red[(wg * 4 + 1) * 16 + cl] +
                                   red[(wg * 4 + 2) * 16 + cl] + red[(wg * 4 + 3) * 16 + cl];
                 const float invl = rsqrtf(ssl * (1.f / DV) + p.eps);
+                // rows i0.. of this head: one base address and a constant row stride, the output
+                // type chosen once for the pass
+                const size_t base = ((size_t)(bos + t0 + i0) * H + h) * DV + v, stride = (size_t)H * DV;
+                const int rows = min(16, cn - i0);
+                if (p.o_bf16) {
+                    __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(p.y) + base;
+                    __nv_bfloat16 *ob = p.o ? reinterpret_cast<__nv_bfloat16 *>(p.o) + base : nullptr;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int i = i0 + c;
-                    const float inv = __shfl_sync(0xffffffffu, invl, c);
-                    if (i < cn) {
-                        const size_t idx = ((size_t)(bos + t0 + i) * H + h) * DV + v;
+                    for (int c = 0; c < 16; ++c) {
+                        const float inv = __shfl_sync(0xffffffffu, invl, c);
                         const float x = __uint_as_float(r[c]);
-                        st_out(p.y, idx, x * inv * w * sg[c], p.o_bf16);
-                        if (p.o) st_out(p.o, idx, x, p.o_bf16);
+                        if (c < rows) {
+                            yb[c * stride] = __float2bfloat16_rn(x * inv * w * sg[c]);
+                            if (ob) ob[c * stride] = __float2bfloat16_rn(x);
+                        }
+                    }
+                } else {
+                    float *yf = reinterpret_cast<float *>(p.y) + base;
+                    float *of = p.o ? reinterpret_cast<float *>(p.o) + base : nullptr;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float inv = __shfl_sync(0xffffffffu, invl, c);
+                        const float x = __uint_as_float(r[c]);
+                        if (c < rows) {
+                            yf[c * stride] = x * inv * w * sg[c];
+                            if (of) of[c * stride] = x;
+                        }
                     }
                 }
             } else if (p.o) {

@@ -220,6 +220,152 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     if (warp == 1) tmem_dealloc(tb, L::TMEM_COLS);
 }
 
+// Cluster helpers for the split-K form: this CTA's rank in its cluster, a shared-memory
+// address mapped into another CTA of the cluster, a store there, and the cluster barrier
+// (every thread of both CTAs passes each one exactly once).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The decode batch (at most 256 rows, few feature tiles): one 128-feature x 256-row tile per
+// pair of CTAs in a cluster, each pair member running half of K, so that twice as many SMs
+// run the products.  Rank 1 adds its fp32 accumulator into rank 0's shared memory (the
+// stage buffers are idle by then) between two cluster barriers; rank 0 sums and writes.
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    oproj_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_y,
+                        const __grid_constant__ GemmArgs a) {
+    constexpr int BN = 256;
+    using L = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm), sb16 = sb >> 4;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BARS);
+    uint64_t *empty = full + L::STAGES;
+    uint64_t *acc_full = empty + L::STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 2);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int f = blockIdx.x >> 1;  // feature tile of the pair
+    const int KB = a.K / BK, kb0 = (int)rank * (KB / 2), kb1 = kb0 + KB / 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, BN);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tb = *tmem_slot;
+    int failed = 0;
+
+    if (warp == 0 && lane == 0) {  // ---- TMA producer
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const uint32_t s = it % L::STAGES, use = it / L::STAGES;
+            if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, kPolls)) {
+                failed = 1;
+                break;
+            }
+            mbar_arrive_expect_tx(full + s, L::STAGE);
+            tma_load_2d(sb + s * L::STAGE, &tmap_w, full + s, kb * BK, f * BM);
+            tma_load_2d(sb + s * L::STAGE + L::A_BYTES, &tmap_y, full + s, kb * BK, 0);
+        }
+        const uint32_t n_issued = it;
+        for (uint32_t s = 0; s < (uint32_t)L::STAGES && s < n_issued; ++s) {
+            const uint32_t last = n_issued - 1 - ((n_issued - 1 + L::STAGES - s) % L::STAGES);
+            mbar_wait(full + s, (last / L::STAGES) & 1, kPolls);
+        }
+    } else if (warp == 1 && lane == 0) {  // ---- MMA issuer
+        const uint32_t idesc = idesc_bf16(BM, BN, false, false);
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const uint32_t s = it % L::STAGES;
+            if (!mbar_wait(full + s, (it / L::STAGES) & 1, kPolls)) {
+                failed = 1;
+                break;
+            }
+            fence_after_sync();
+            const uint32_t sa = s * L::STAGE, sbb = sa + L::A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+                mma_ss(tb, sdesc_at(sb16, sa + k * 32, 16, 1024), sdesc_at(sb16, sbb + k * 32, 16, 1024), idesc,
+                       (it | k) ? 1u : 0u);
+            mma_commit(empty + s);
+        }
+        mma_commit(acc_full);  // also an arrival after a failure: nothing issued may still run
+    }
+    __syncwarp();  // the producer and MMA warps reconverge before the cluster barriers
+    // every MMA of this CTA has completed once acc_full does
+    const int q = warp & 3, m = q * 32 + lane;
+    const uint32_t lane_base = tb + ((uint32_t)(q * 32) << 16);
+    if (warp >= 2 && !mbar_wait(acc_full, 0, kPolls)) failed = 1;
+    fence_after_sync();
+    cluster_sync();  // both halves' products done: rank 0's stage buffers are idle
+    // rank 1's partial sums in rank 0's shared memory: [128 lanes][kPartPitch] fp32 (130 KB), a
+    // lane's 256 columns contiguous, rows padded so that 16-byte accesses of consecutive lanes
+    // fall in different banks
+    constexpr int kPartPitch = BN + 4;
+    static_assert(128 * kPartPitch * 4 <= L::STAGES * L::STAGE, "the partial sums fit in the stage buffers");
+    const float *part = reinterpret_cast<const float *>(sm) + m * kPartPitch;
+    if (warp >= 2 && rank == 1) {
+        const uint32_t remote = map_to_rank(sb, 0) + (uint32_t)(m * kPartPitch * 4);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_base + c0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) st_cluster_v4(remote + (uint32_t)((c0 + j) * 4), r[j], r[j + 1], r[j + 2], r[j + 3]);
+        }
+    }
+    cluster_sync();  // rank 1's partial sums are in rank 0's shared memory
+    if (warp >= 2 && rank == 0) {
+        const int feat = f * BM + m;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_base + c0, r);
+            tmem_wait_ld();
+            const int nrow = min(16, a.M - c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (j >= nrow) continue;
+                const float v = failed ? __int_as_float(0x7fc00000) : __uint_as_float(r[j]) + part[c0 + j];
+                if (a.out_bf16)
+                    reinterpret_cast<__nv_bfloat16 *>(a.out)[(size_t)(c0 + j) * a.N + feat] = __float2bfloat16_rn(v);
+                else
+                    reinterpret_cast<float *>(a.out)[(size_t)(c0 + j) * a.N + feat] = v;
+            }
+        }
+    }
+    fence_before_sync();
+    if (__syncthreads_or(failed) && threadIdx.x == 0) atomicAdd(&g_oproj_timeouts, 1);
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tb, BN);
+}
+
 }  // namespace
 
 int take_oproj_timeouts(cudaStream_t st) {
@@ -291,6 +437,61 @@ kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, 
             return KDA_ERR_CUDA;
         }
         configured.set(dev);
+    }
+    const bool splitk = M <= 256 && (K / BK) % 2 == 0 && 2 * n_ft <= sms;
+    if (splitk) {
+        static DeviceOnce configured_sk;
+        if (!configured_sk.done(dev)) {
+            const cudaError_t e = cudaFuncSetAttribute(oproj_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       Cfg<256>::SMEM);
+            if (e != cudaSuccess) {
+                set_error("o_proj: cannot reserve shared memory: %s", cudaGetErrorString(e));
+                return KDA_ERR_CUDA;
+            }
+            configured_sk.set(dev);
+        }
+        CUtensorMap ty256;
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)BK, 256u};
+        const CUresult r = enc(&ty256, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(y), dims, strides, box,
+                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            set_error("o_proj: cuTensorMapEncodeTiled failed for y (%d)", (int)r);
+            return KDA_ERR_CUDA;
+        }
+        GemmArgs ga;
+        memset(&ga, 0, sizeof(ga));
+        ga.out = out;
+        ga.out_bf16 = out_bf16;
+        ga.M = (int)M;
+        ga.N = N;
+        ga.K = K;
+        ga.n_ft = n_ft;
+        ga.n_tt = 1;
+        ga.n_tiles = n_ft;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(2 * n_ft, 1, 1);
+        cfg.blockDim = dim3(kWarps * 32, 1, 1);
+        cfg.dynamicSmemBytes = Cfg<256>::SMEM;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, oproj_splitk_kernel, tw, ty256, ga);
+        note_launch();
+        if (e != cudaSuccess) {
+            set_error("oproj_splitk_kernel: %s", cudaGetErrorString(e));
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        return check_launch("oproj_splitk_kernel");
     }
     GemmArgs ga;
     memset(&ga, 0, sizeof(ga));

@@ -1,8 +1,11 @@
 """GPU tests of the split tensor-core prefill (a workspace given): the state-independent
-pre-pass over every chunk and head, then the per-head chain kernel.  The pre-pass repeats
-the fused kernel's arithmetic operation for operation, so wherever no chunk needs the
-exact decay-range fallback the two forms must agree bit for bit; the fallback cases are
-checked against the fp64 oracle (max|diff| / rms(oracle) <= 5e-3)."""
+pre-pass over every chunk and head, then the per-head chain kernel.  The two forms run the
+same products at the same split-bf16 precision; the split form accumulates the R/O product's
+hi and lo parts in separate TMEM columns and adds them afterwards, so its fp32 sums differ
+from the fused kernel's only in their order.  Every case is checked against the fp64 oracle
+(max|diff| / rms(oracle) <= 5e-3) and, where no chunk needs the exact decay-range fallback,
+against the fused form to 1e-3 of rms (five times tighter); the full-size prefill workload is
+compared with the fused form, which its own full-size test checks against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -31,41 +34,47 @@ def both(d, **kw):
     return fused, split
 
 
-def assert_same_bits(a, b):
+def assert_agrees(a, b):
+    """The split form's outputs against the fused form's: within 1e-3 of the fused one's rms
+    (both carry about 6e-5 of split-bf16 error; they differ in fp32 summation order), plus
+    one bf16 ulp where the output is bf16 (the two may round a value to neighbouring bf16s)."""
     for x, y in zip(a, b):
         if x is None:
             assert y is None
             continue
         assert x.dtype == y.dtype and x.shape == y.shape
-        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
-                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+        xf, yf = x.double(), y.double()
+        assert torch.isfinite(yf).all()
+        rms = float(torch.sqrt(torch.mean(xf * xf)))
+        ulp = 2.0 ** -7 * xf.abs() if x.dtype == torch.bfloat16 else 0.0
+        assert bool(((yf - xf).abs() <= ulp + 1e-3 * rms).all())
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 333])
-def test_split_equals_fused_bitwise(T):
+def test_split_matches_fused(T):
     d = make_inputs("varlen", device="cuda", lengths=[T], H=3)  # one sequence with an initial state
     fused, split = both(d)
-    assert_same_bits(fused, split)
+    assert_agrees(fused, split)
     oo, so = oracle_run(d)
     assert rel_err(split[0], oo) <= PARITY
     assert rel_err(split[1], so) <= PARITY
 
 
-def test_split_equals_fused_varlen_with_empty_sequences():
+def test_split_matches_fused_varlen_with_empty_sequences():
     d = make_inputs("varlen", device="cuda", lengths=[0, 70, 1, 0, 128, 191], H=2)
     fused, split = both(d)
-    assert_same_bits(fused, split)
+    assert_agrees(fused, split)
     oo, so = oracle_run(d)
     assert rel_err(split[0], oo) <= PARITY
     assert rel_err(split[1], so) <= PARITY
 
 
 @pytest.mark.parametrize("gdt,odt", [(torch.bfloat16, torch.bfloat16), (torch.float32, torch.float32)])
-def test_split_equals_fused_with_norm(gdt, odt):
+def test_split_matches_fused_with_norm(gdt, odt):
     d = make_inputs("long", device="cuda", B=2, T=150, H=3)
     gate = d["gate"].to(gdt)
     fused, split = both(d, gate=gate, norm_w=d["norm_w"], eps=d["eps"], out_dtype=odt)
-    assert_same_bits(fused, split)
+    assert_agrees(fused, split)
     oo, so = oracle_run(d)
     yo = oracle.gated_rmsnorm(oo, np32(gate), np32(d["norm_w"]), eps=d["eps"])
     if odt == torch.float32:
@@ -74,21 +83,21 @@ def test_split_equals_fused_with_norm(gdt, odt):
         assert_bf16_close(split[2], yo, 5e-4)
 
 
-def test_split_equals_fused_norm_without_o():
+def test_split_matches_fused_norm_without_o():
     d = make_inputs("long", device="cuda", B=1, T=190, H=2)
     fused, split = both(d, gate=d["gate"], norm_w=d["norm_w"], eps=d["eps"], return_o=False)
     assert fused[0] is None and split[0] is None
-    assert_same_bits(fused, split)
+    assert_agrees(fused, split)
 
 
-def test_split_equals_fused_gate_logits():
+def test_split_matches_fused_gate_logits():
     d = make_logit_inputs("prefill", device="cuda", T=300, H=3)
     args = (d["q"], d["k"], d["v"], d["g_logits"], d["beta_logits"], d["A_log"])
     kw = dict(dt_bias=d["dt_bias"], g_lower_bound=d["g_lower_bound"], scale=d["scale"], mode="tensor")
     fused = kda.chunk_fwd_logits(*args, workspace=None, **kw)
     split = kda.chunk_fwd_logits(*args, workspace="auto", **kw)
     kda.device_status()
-    assert_same_bits(fused, split)
+    assert_agrees(fused, split)
     g, beta = oracle.gates(np32(d["g_logits"]), np32(d["A_log"]), np32(d["beta_logits"]), np32(d["dt_bias"]),
                            d["g_lower_bound"])
     oo, so = oracle.recurrent(np32(d["q"]), np32(d["k"]), np32(d["v"]), g, beta, scale=d["scale"])
@@ -96,11 +105,11 @@ def test_split_equals_fused_gate_logits():
     assert rel_err(split[1], so) <= PARITY
 
 
-def test_split_equals_fused_prefill_workload_full_size():
-    """The benchmark's prefill (B=1, T=8192, H=96) through both forms: the same bits."""
+def test_split_matches_fused_prefill_workload_full_size():
+    """The benchmark's prefill (B=1, T=8192, H=96) through both forms."""
     d = make_inputs("prefill", device="cuda")
     fused, split = both(d)
-    assert_same_bits(fused, split)
+    assert_agrees(fused, split)
 
 
 def test_split_fallback_every_chunk():
@@ -137,7 +146,7 @@ def test_split_workspace_tensor_and_reuse():
                             cu_seqlens=d.get("cu_seqlens"), workspace=ws, mode="tensor")
         ref = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("initial_state"), scale=d["scale"],
                             cu_seqlens=d.get("cu_seqlens"), workspace=None, mode="tensor")
-        assert_same_bits(ref, out)
+        assert_agrees(ref, out)
     kda.device_status()
 
 
