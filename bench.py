@@ -34,6 +34,10 @@ PREFILL_BYTES_PER_TH = 3 * 256 + 512 + 4 + 512   # q,k,v bf16 + g fp32 + beta + 
 PREFILL_FLOP_PER_TH = 10 * 64 * 128 + 6 * 128 * 128 + (2 * 64 * 64) // 3  # 182,955 at C=64, d=128
 STATE_BYTES = 128 * 128 * 4
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256 + 512  # + gate bf16, y fp32
+# the decode step with the q, k, v short convolutions fused: + three histories of W-1 = 3
+# rows of 128 fp32 channels read and written per unit; the filters (3 x 128 x W fp32 per
+# head) are counted once per call
+DECODE_CONV_BYTES_PER_UNIT = DECODE_BYTES_PER_UNIT + 2 * 3 * 3 * 128 * 4
 PREFILL_LOGITS_BYTES_PER_TH = 3 * 256 + 256 + 2 + 512  # q,k,v bf16 + g logits bf16 + beta logit bf16 + o fp32
 PREFILL_NORM_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 256  # q,k,v bf16 + g fp32 + beta + gate bf16 + y bf16
 PREFILL_LONG_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 512  # q,k,v bf16 + g fp32 + beta + gate bf16 + y fp32
@@ -357,6 +361,37 @@ def bench_decode(args, world, peaks):
                          "peak_source": peaks["source"]}}
 
 
+def bench_decode_conv(args, world, peaks):
+    """The decode step with the q, k, v short convolutions (+ SiLU) fused ahead of it
+    (kda_recurrent_step_conv): raw bf16 projections in, state and the three histories
+    updated in place, the gated norm fused, y fp32 out."""
+    import torch
+    import kimi_delta_attention_gated_gb300 as kda
+    from kimi_delta_attention_gated_gb300.inputs import make_decode_conv_inputs
+    B = args.decode_B or 256
+    d = make_decode_conv_inputs(B=B, H=96, W=4, device="cuda")
+    state = d["initial_state"]
+    _, H, K, V = state.shape
+    y = torch.empty((B, H * V), device="cuda", dtype=torch.float32)
+    conv = (d["conv_weight"], d["conv_state"], d["conv_state"])
+    fn = lambda: kda.recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, state_out=state,
+                                    gate=d["gate"], norm_w=d["norm_w"], eps=d["eps"], y=y, return_o=False,
+                                    conv=conv)
+    r = time_steps(fn, max(args.steps, 20), args.warmup, world)
+    kernel_ms = r["call_ms"] / max(1, r["launches"] // max(args.steps, 20))
+    algo_bytes = B * H * DECODE_CONV_BYTES_PER_UNIT + H * 3 * 128 * d["W"] * 4
+    achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+    return {"metric": "KDA decode tokens/s, short convolutions fused", "value": world * B / (r["ms_per_step"] * 1e-3),
+            "unit": "tokens/s", "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
+            "config": {"workload": f"decode B={B} H={H} d={K} W=4: raw q/k/v projections through the fused short "
+                                   "convolutions, fp32 state and histories in place, fused sigmoid-gated RMSNorm",
+                       "l2_flush": "state 1.61 GB > L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("decode_conv", B * H),
+                         "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
+                         "peak_source": peaks["source"]}}
+
+
 def bench_prefill_logits(args, world, peaks):
     """The same prefill with g and beta computed in the kernel from bf16 logits
     (kda_chunk_fwd_logits), sharing the prefill's shapes and q, k, v."""
@@ -599,8 +634,8 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "kernels", "logits", "norm", "varlen",
-                                       "long", "oproj"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode_conv", "conv", "kernels", "logits", "norm",
+                                       "varlen", "long", "oproj"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
@@ -625,7 +660,7 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "conv", "kernels", "logits", "norm", "varlen", "long", "oproj"):
+    if args.only in ("decode", "decode_conv", "conv", "kernels", "logits", "norm", "varlen", "long", "oproj"):
         if args.only == "oproj":
             res = bench_o_proj(args, world, peaks)
         elif args.only in ("varlen", "long"):
@@ -636,6 +671,8 @@ def main():
             res = bench_prefill_logits(args, world, peaks)
         elif args.only == "norm":  # the prefill with the fused gated norm alone (profiling runs)
             res = bench_prefill_norm(args, world, peaks)
+        elif args.only == "decode_conv":
+            res = bench_decode_conv(args, world, peaks)
         else:
             res = bench_decode(args, world, peaks) if args.only == "decode" else bench_short_conv(args, world, peaks)
         if rank == 0:
@@ -644,6 +681,8 @@ def main():
     pre, d = bench_prefill(args, world, rank, peaks, fused=True)
     split = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, fused=False)[0]
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
+    if dec is not None:
+        dec["fused_short_conv"] = bench_decode_conv(args, world, peaks)
     conv = None if (args.no_conv or args.only == "prefill") else bench_short_conv(args, world, peaks)
     logits = None if (args.no_logits or args.only == "prefill") else bench_prefill_logits(args, world, peaks)
     norm = None if (args.no_norm or args.only == "prefill") else bench_prefill_norm(args, world, peaks)
@@ -690,6 +729,8 @@ def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split=None):
            "prefill_long_norm": row(long_, 1e6, "Mtok_s"), "decode_B256": row(dec, 1e3, "Ktok_s"),
            "prefill_logits": row(logits, 1e6, "Mtok_s"), "prefill_norm_bf16": row(norm, 1e6, "Mtok_s"),
            "prefill_T8192_split": row(split, 1e6, "Mtok_s")}
+    if dec and dec.get("fused_short_conv"):
+        out["decode_conv_B256"] = row(dec["fused_short_conv"], 1e3, "Ktok_s")
     if conv:
         out["conv_prefill"] = row(conv["conv_prefill"], 1e6, "Mtok_s")
         out["conv_decode"] = row(conv["conv_decode"], 1e6, "Mtok_s")

@@ -298,6 +298,46 @@ kda_status kda_recurrent_step_logits(const void *q, const void *k, const void *v
                                      const float *norm_w, float eps, void *y, void *stream);
 
 /*
+ * kda_recurrent_step_conv -- the decode step with the q, k and v short
+ * convolutions (+ SiLU) fused ahead of it, in one kernel.
+ *
+ * Pages: nnterp encyclopedia "Kimi-Linear", section 03 "Kimi Delta Attention
+ * decays each key channel" (a width-4 convolution before the delta rule, whose
+ * last inputs are carried outside the recurrent state) and section "Printout"
+ * (depthwise Conv1d, kernel 4, padding 3, no bias); Kimi-K3 atlas "gate-project
+ * (decode, P = 1000)", section "Code" (q_conv1d, k_conv1d, v_conv1d =
+ * ShortConvolution(..., activation='silu') applied to the projections).
+ *
+ * As kda_recurrent_step (or kda_recurrent_step_logits: give exactly one of the
+ * pairs g, beta / g_logits, beta_logits with A_log; the other pointers NULL), but
+ *   q, k  [B, H, K] qkv_dtype, v [B, H, V] qkv_dtype are the RAW projections of
+ *         this token; the step uses silu(conv(.)) of each, then (optionally) the
+ *         L2 norm of q and k, as the layer does.
+ *   conv_weight[f]    [H*128, W] float: f = 0 for q, 1 for k, 2 for v (the Conv1d
+ *                     weight [D, 1, W] without its middle axis); no bias.
+ *   conv_state_in[f]  [B, W-1, H*128] float: the W-1 raw inputs before this token,
+ *                     oldest first, as kda_short_conv_fwd keeps them; the array
+ *                     pointer NULL (or all three entries NULL) = zero history.
+ *   conv_state_out[f] [B, W-1, H*128] float, required: the new history (the old
+ *                     one shifted by this token).  Each may be conv_state_in[f]
+ *                     itself (in place); no other overlap is allowed.
+ * conv_weight, conv_state_in and conv_state_out are HOST arrays of three device
+ * pointers, read during the call only.  The convolution output stays in fp32 in
+ * the kernel (no rounding to qkv_dtype between the two steps).  Supported: K = V =
+ * 128, W in {2, 3, 4}; other shapes return KDA_ERR_UNSUPPORTED.  Returns a kda_status.
+ */
+kda_status kda_recurrent_step_conv(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                   const float *const conv_weight[3], int W,
+                                   const float *const conv_state_in[3], float *const conv_state_out[3],
+                                   const float *g, const float *beta,
+                                   const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                   const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                   kda_dtype beta_logits_dtype, const float *state_in, float *state_out,
+                                   void *o, kda_dtype o_dtype, int B, int H, int K, int V, float scale,
+                                   int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                                   const float *norm_w, float eps, void *y, void *stream);
+
+/*
  * kda_gated_rmsnorm -- the head-wise sigmoid-gated RMSNorm on its own.
  *
  * Page: Kimi-K3 atlas "gate-project (decode, P = 1000)", sections "Parameters"

@@ -78,8 +78,12 @@ def _load():
         lib.kda_recurrent_step_logits.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, I, I, I, I, F, I,
                                                   P, I, P, F, P, P]
         lib.kda_o_proj.argtypes = [P, P, P, I, ctypes.c_int64, I, I, P]
+        P3 = ctypes.POINTER(ctypes.c_void_p)  # a host array of three device pointers, or NULL
+        lib.kda_recurrent_step_conv.argtypes = [P, P, P, I, P3, I, P3, P3, P, P, P, I, P, P, F, P, I, P, P, P, I,
+                                                I, I, I, I, F, I, P, I, P, F, P, P]
         for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
-                   "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits", "kda_o_proj"):
+                   "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits", "kda_o_proj",
+                   "kda_recurrent_step_conv"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.kda_device_status.argtypes = [P]
         lib.kda_device_status.restype = ctypes.c_int
@@ -460,25 +464,49 @@ def recurrent_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, use_qk_l2
 
 
 def recurrent_step(q, k, v, g, beta, state, *, scale=None, use_qk_l2norm=True, gate=None, norm_w=None,
-                   eps=1e-5, out_dtype=torch.float32, state_out=None, return_o=True, o=None, y=None):
+                   eps=1e-5, out_dtype=torch.float32, state_out=None, return_o=True, o=None, y=None, conv=None):
     """One decode token per sequence.  q, k [B,H,K]; v [B,H,V]; g [B,H,K]; beta [B,H];
     state [B,H,K,V] fp32 (or None).  ``state_out=state`` updates the state in place.
-    Returns (o, state_out[, y])."""
+
+    ``conv=(weights, states_in[, states_out])`` fuses the q, k, v short convolutions
+    (+ SiLU) ahead of the step (K = V = 128): q, k, v are then the raw projections,
+    weights three [H*128, W] (or [H*128, 1, W]) filters, states_in three [B, W-1, H*128]
+    fp32 histories (or None: zero history), states_out three buffers for the new ones
+    (default: fresh; ``states_in`` itself updates them in place).
+    Returns (o, state_out[, y][, conv_states_out])."""
     return _step(q, k, v, (g, beta), None, state, scale, use_qk_l2norm, gate, norm_w, eps, out_dtype, state_out,
-                 return_o, o, y)
+                 return_o, o, y, conv)
 
 
 def recurrent_step_logits(q, k, v, g_logits, beta_logits, A_log, state, *, dt_bias=None, g_lower_bound=-5.0,
                           scale=None, use_qk_l2norm=True, gate=None, norm_w=None, eps=1e-5, out_dtype=torch.float32,
-                          state_out=None, return_o=True, o=None, y=None):
+                          state_out=None, return_o=True, o=None, y=None, conv=None):
     """recurrent_step with g and beta computed from their logits (see chunk_fwd_logits):
     g_logits [B,H,K], beta_logits [B,H]."""
     lb = float("-inf") if g_lower_bound is None else float(g_lower_bound)
     return _step(q, k, v, None, (g_logits, beta_logits, A_log, dt_bias, lb), state, scale, use_qk_l2norm, gate,
-                 norm_w, eps, out_dtype, state_out, return_o, o, y)
+                 norm_w, eps, out_dtype, state_out, return_o, o, y, conv)
 
 
-def _step(q, k, v, gb, lg, state, scale, use_qk_l2norm, gate, norm_w, eps, out_dtype, state_out, return_o, o, y):
+def _conv_args(conv, dev, B, H):
+    """Marshal the fused convolutions' (weights, states_in[, states_out]) for the C call."""
+    weights, s_in = conv[0], conv[1]
+    s_out = conv[2] if len(conv) > 2 else None
+    if len(weights) != 3 or (s_in is not None and len(s_in) != 3) or (s_out is not None and len(s_out) != 3):
+        raise ValueError("conv takes three filters (q, k, v), three histories and three outputs")
+    ws = [_prep(w[:, 0, :] if w.dim() == 3 else w, dev, torch.float32) for w in weights]
+    W = ws[0].shape[1]
+    sin = None if s_in is None else [_prep(x, dev, torch.float32) for x in s_in]
+    if s_out is None:
+        s_out = [torch.empty((B, W - 1, H * 128), device=dev, dtype=torch.float32) for _ in range(3)]
+    P3 = ctypes.c_void_p * 3
+    ptr3 = lambda ts: P3(*[t.data_ptr() for t in ts])
+    keep = (ws, sin, s_out)  # the tensors stay alive through the call
+    return ptr3(ws), W, (ptr3(sin) if sin is not None else None), ptr3(s_out), tuple(s_out), keep
+
+
+def _step(q, k, v, gb, lg, state, scale, use_qk_l2norm, gate, norm_w, eps, out_dtype, state_out, return_o, o, y,
+          conv=None):
     lib = _load()
     host = q.device.type != "cuda"
     dev = _device_of(q, k, v, state)
@@ -499,6 +527,20 @@ def _step(q, k, v, gb, lg, state, scale, use_qk_l2norm, gate, norm_w, eps, out_d
     tail = (_ptr(state), _ptr(state_out), _ptr(o), _dt(o if o is not None else y), B, H, K, V, float(scale),
             int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16, _ptr(norm_w), float(eps),
             _ptr(y), _stream())
+    if conv is not None:
+        cw, W, cin, cout_p, cout, _keep = _conv_args(conv, dev, B, H)
+        if lg is None:
+            g, beta = _prep(gb[0], dev, torch.float32), _prep(gb[1], dev, torch.float32)
+            gates = (_ptr(g), _ptr(beta), None, BF16, None, None, 0.0, None, BF16)
+        else:
+            z, b, A_log, dt_bias, lb = _logit_args(lg, dev)
+            gates = (None, None, _ptr(z), _dt(z), _ptr(A_log), _ptr(dt_bias), lb, _ptr(b), _dt(b))
+        _check(lib.kda_recurrent_step_conv(_ptr(q), _ptr(k), _ptr(v), _dt(q), cw, W, cin, cout_p, *gates, *tail))
+        res = (o, state_out, y) if gate is not None else (o, state_out)
+        if host:
+            res = _to_host(res + cout, True)
+            return res[:-3] + (res[-3:],)
+        return res + (cout,)
     if lg is None:
         g, beta = _prep(gb[0], dev, torch.float32), _prep(gb[1], dev, torch.float32)
         _check(lib.kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), *tail))

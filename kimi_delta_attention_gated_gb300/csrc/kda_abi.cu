@@ -207,6 +207,11 @@ kda::SeqParams make_params(const void *q, const void *k, const void *v, int qkv_
     p.o_bf16 = o_dtype == KDA_BF16;
     p.gate_bf16 = gate_dtype == KDA_BF16;
     p.polls = kda::wait_polls();
+    for (int f = 0; f < 3; ++f) {
+        p.cw[f] = p.cs_in[f] = nullptr;
+        p.cs_out[f] = nullptr;
+    }
+    p.conv_w = 0;
     return p;
 }
 
@@ -317,11 +322,73 @@ kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *
                                      o_dtype == KDA_BF16, (int64_t)B * T, H, V, st);
 }
 
+// The fused short convolutions of kda_recurrent_step_conv.
+struct ConvArgs {
+    const float *const *w;       // [3]
+    int W;
+    const float *const *s_in;    // [3] or null
+    float *const *s_out;         // [3]
+};
+
+// Arguments of the fused convolutions: shapes, alignment, and that no new history
+// overlaps anything but its own old history (then exactly), and no weight or old history
+// overlaps an output of the step.
+kda_status check_conv(const char *fn, const ConvArgs &cv, int B, int H, int K, int V, const Span *step_in, int n_in,
+                      const Span *step_out, int n_out) {
+    KDA_REQUIRE(K == 128 && V == 128, KDA_ERR_UNSUPPORTED,
+                "%s: the fused short convolutions are built for K = V = 128 (got K=%d V=%d)", fn, K, V);
+    KDA_REQUIRE(cv.W >= 2 && cv.W <= 4, KDA_ERR_UNSUPPORTED, "%s: W=%d (supported: 2, 3, 4)", fn, cv.W);
+    KDA_REQUIRE(cv.w && cv.s_out, KDA_ERR_INVALID_ARG, "%s: conv_weight and conv_state_out must not be NULL", fn);
+    const bool hist = cv.s_in && cv.s_in[0];
+    for (int f = 0; f < 3; ++f) {
+        KDA_REQUIRE(cv.w[f] && cv.s_out[f], KDA_ERR_INVALID_ARG,
+                    "%s: all three conv_weight and conv_state_out pointers are needed", fn);
+        KDA_REQUIRE(!cv.s_in || (cv.s_in[f] != nullptr) == hist, KDA_ERR_INVALID_ARG,
+                    "%s: conv_state_in gives all three histories or none", fn);
+        KDA_REQUIRE(aligned16(cv.w[f]) && aligned16(cv.s_out[f]) && (!hist || aligned16(cv.s_in[f])),
+                    KDA_ERR_INVALID_ARG, "%s: every pointer must be 16-byte aligned", fn);
+    }
+    const size_t D = (size_t)H * 128, wb = D * cv.W * 4, sb = (size_t)B * (cv.W - 1) * D * 4;
+    const char *names_w[3] = {"conv_weight[0]", "conv_weight[1]", "conv_weight[2]"};
+    const char *names_i[3] = {"conv_state_in[0]", "conv_state_in[1]", "conv_state_in[2]"};
+    const char *names_o[3] = {"conv_state_out[0]", "conv_state_out[1]", "conv_state_out[2]"};
+    for (int f = 0; f < 3; ++f) {
+        const Span so{cv.s_out[f], sb, names_o[f]};
+        for (int j = 0; j < n_in; ++j)
+            KDA_REQUIRE(!overlaps(so, step_in[j]), KDA_ERR_INVALID_ARG, "%s: %s must not overlap %s", fn, so.name,
+                        step_in[j].name);
+        for (int j = 0; j < n_out; ++j)
+            KDA_REQUIRE(!overlaps(so, step_out[j]), KDA_ERR_INVALID_ARG, "%s: %s must not overlap %s", fn, so.name,
+                        step_out[j].name);
+        for (int e = 0; e < 3; ++e) {
+            const Span we{cv.w[e], wb, names_w[e]};
+            KDA_REQUIRE(!overlaps(so, we), KDA_ERR_INVALID_ARG, "%s: %s must not overlap %s", fn, so.name, we.name);
+            if (hist) {
+                const Span si{cv.s_in[e], sb, names_i[e]};
+                KDA_REQUIRE(!overlaps(so, si) || (e == f && si.p == so.p), KDA_ERR_INVALID_ARG,
+                            "%s: %s may be %s itself but must not overlap any other history", fn, so.name,
+                            names_i[f]);
+            }
+            if (e > f) {
+                const Span so2{cv.s_out[e], sb, names_o[e]};
+                KDA_REQUIRE(!overlaps(so, so2), KDA_ERR_INVALID_ARG, "%s: %s must not overlap %s", fn, so.name,
+                            so2.name);
+            }
+        }
+        // the weights and old histories are inputs: no output of the step may overlap them
+        const Span we{cv.w[f], wb, names_w[f]}, si{hist ? cv.s_in[f] : nullptr, sb, names_i[f]};
+        for (int j = 0; j < n_out; ++j)
+            KDA_REQUIRE(!overlaps(we, step_out[j]) && !overlaps(si, step_out[j]), KDA_ERR_INVALID_ARG,
+                        "%s: %s must not overlap %s or %s", fn, step_out[j].name, we.name, si.name);
+    }
+    return KDA_OK;
+}
+
 kda_status step_impl(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
                      const float *g, const float *beta, const GateLogits *gl, const float *state_in,
                      float *state_out, void *o, kda_dtype o_dtype, int B, int H, int K, int V, float scale,
                      int use_qk_l2norm, const void *gate, kda_dtype gate_dtype, const float *norm_w, float eps,
-                     void *y, void *stream) {
+                     void *y, void *stream, const ConvArgs *cv = nullptr) {
     kda::g_err[0] = 0;
     int N = 0;
     KDA_REQUIRE(state_out, KDA_ERR_INVALID_ARG, "%s: state_out must not be NULL", fn);
@@ -335,9 +402,33 @@ kda_status step_impl(const char *fn, const void *q, const void *k, const void *v
                             gl ? esize(gl->b_dtype) : 4, state_in, state_out, o, o_dtype, nullptr, gate, gate_dtype,
                             norm_w, y, B, N, H, K, V);
     if (s != KDA_OK) return s;
+    if (cv) {
+        const size_t hk = (size_t)B * H * K, hv = (size_t)B * H * V, st = (size_t)B * H * K * V * 4;
+        const Span in[] = {{q, hk * esize(qkv_dtype), "q"},
+                           {k, hk * esize(qkv_dtype), "k"},
+                           {v, hv * esize(qkv_dtype), "v"},
+                           {gchk, hk * (gl ? esize(gl->z_dtype) : 4), gl ? "g_logits" : "g"},
+                           {bchk, (size_t)B * H * (gl ? esize(gl->b_dtype) : 4), gl ? "beta_logits" : "beta"},
+                           {gate, gate ? hv * esize(gate_dtype) : 0, "gate"},
+                           {norm_w, norm_w ? (size_t)V * 4 : 0, "norm_w"},
+                           {state_in, state_in ? st : 0, "state_in"}};
+        const Span out[] = {{o, o ? hv * esize(o_dtype) : 0, "o"},
+                            {y, y ? hv * esize(o_dtype) : 0, "y"},
+                            {state_out, st, "state_out"}};
+        if ((s = check_conv(fn, *cv, B, H, K, V, in, 8, out, 3)) != KDA_OK) return s;
+    }
     kda::SeqParams p = make_params(q, k, v, qkv_dtype, g, beta, state_in, state_out, o, o_dtype, nullptr, nullptr, N,
                                    1, H, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y);
     set_logits(p, gl, K);
+    if (cv) {
+        const bool hist = cv->s_in && cv->s_in[0];
+        for (int f = 0; f < 3; ++f) {
+            p.cw[f] = cv->w[f];
+            p.cs_in[f] = hist ? cv->s_in[f] : nullptr;
+            p.cs_out[f] = cv->s_out[f];
+        }
+        p.conv_w = cv->W;
+    }
     return kda::launch_recurrent(p, K, V, (cudaStream_t)stream);
 }
 
@@ -488,6 +579,30 @@ kda_status kda_recurrent_step_logits(const void *q, const void *k, const void *v
     const GateLogits gl{g_logits, g_logits_dtype, A_log, dt_bias, g_lower_bound, beta_logits, beta_logits_dtype};
     return step_impl("kda_recurrent_step_logits", q, k, v, qkv_dtype, nullptr, nullptr, &gl, state_in, state_out, o,
                      o_dtype, B, H, K, V, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y, stream);
+}
+
+kda_status kda_recurrent_step_conv(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                   const float *const conv_weight[3], int W, const float *const conv_state_in[3],
+                                   float *const conv_state_out[3], const float *g, const float *beta,
+                                   const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                   const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                   kda_dtype beta_logits_dtype, const float *state_in, float *state_out, void *o,
+                                   kda_dtype o_dtype, int B, int H, int K, int V, float scale, int use_qk_l2norm,
+                                   const void *gate, kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
+                                   void *stream) {
+    kda::g_err[0] = 0;
+    const char *fn = "kda_recurrent_step_conv";
+    const bool plain = g || beta, logits = g_logits || beta_logits || A_log;
+    KDA_REQUIRE(plain != logits, KDA_ERR_INVALID_ARG,
+                "%s: give either g and beta or g_logits, A_log and beta_logits, not both or neither", fn);
+    const ConvArgs cv{conv_weight, W, conv_state_in, conv_state_out};
+    if (logits) {
+        const GateLogits gl{g_logits, g_logits_dtype, A_log, dt_bias, g_lower_bound, beta_logits, beta_logits_dtype};
+        return step_impl(fn, q, k, v, qkv_dtype, nullptr, nullptr, &gl, state_in, state_out, o, o_dtype, B, H, K, V,
+                         scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y, stream, &cv);
+    }
+    return step_impl(fn, q, k, v, qkv_dtype, g, beta, nullptr, state_in, state_out, o, o_dtype, B, H, K, V, scale,
+                     use_qk_l2norm, gate, gate_dtype, norm_w, eps, y, stream, &cv);
 }
 
 kda_status kda_gated_rmsnorm(const void *o, kda_dtype o_dtype, const void *gate,

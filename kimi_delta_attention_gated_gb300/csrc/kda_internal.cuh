@@ -79,6 +79,14 @@ struct SeqParams {
     float g_lower;               // -inf: no floor
     int g_logits_bf16, beta_logits_bf16;
     uint32_t polls;              // bound on the streaming kernels' first-line waits (wait_polls())
+    // Short convolutions fused ahead of the decode step (decode kernel only; then q, k, v
+    // above are the raw projections).  Filter f (0 = q, 1 = k, 2 = v): weights cw[f]
+    // [H * 128, conv_w], history cs_in[f] [N, conv_w - 1, H * 128] (oldest first; all
+    // three null: zero history), new history cs_out[f] of the same shape.  conv_w = 0: off.
+    const float *cw[3];
+    const float *cs_in[3];
+    float *cs_out[3];
+    int conv_w;
 };
 
 // Token range of sequence n, clamped to [0, T] so a bad cu_seqlens cannot

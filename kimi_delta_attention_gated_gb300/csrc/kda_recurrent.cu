@@ -225,14 +225,19 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const SeqParams p) 
 // 128 KiB of reads in flight instead of stalling at every CTA's start.
 
 constexpr int kDK = 128;                 // K = V
-constexpr uint32_t kStage = 65536 + 5 * 512;  // one unit: state [128][128] fp32, then q, k, v, g, gate rows
+// One unit's staging buffer: state [128][128] fp32, then the q, k, v, g and gate rows; with
+// the fused short convolutions also the three filters' weights (128 channels x up to 4
+// taps each) and their histories (up to 3 rows of 128 channels each).
 constexpr uint32_t S_Q = 65536, S_K = S_Q + 512, S_V = S_K + 512, S_G = S_V + 512, S_GATE = S_G + 512;
+constexpr uint32_t S_CW = S_GATE + 512, S_CS = S_CW + 3 * 2048;
 constexpr uint32_t kDecodePolls = 1u << 26;
+template <bool CV>
+constexpr uint32_t kStage = CV ? S_CS + 9 * 512 : S_CW;
 
 // Shared-memory layout of the decode kernel with NW warps and NS staging buffers.
-template <int NW, int NS>
+template <int NW, int NS, bool CV>
 struct DecodeSmem {
-    static constexpr uint32_t arr = NS * kStage;               // sq, sk, se, sv, sd: [128] floats each
+    static constexpr uint32_t arr = NS * kStage<CV>;           // sq, sk, se, sv, sd: [128] floats each
     static constexpr uint32_t red = arr + 5 * 512;             // red_u, red_q: [NW][128] floats each
     static constexpr uint32_t misc = red + 2 * NW * 512;       // [NW][4] floats
     static constexpr uint32_t bar = misc + NW * 16;            // NS mbarriers
@@ -248,12 +253,35 @@ __device__ __forceinline__ float in_elem(const uint8_t *base, int i, int is_bf16
                    : reinterpret_cast<const float *>(base)[i];
 }
 
+// Fused short convolution of channel c through filter f of a staged unit:
+//   z = sum_{j < W-1} w[j] * hist[j] + w[W-1] * x,   returns SiLU(z) = z / (1 + e^-z)
+// (hist = the W-1 inputs before this token, oldest first; zero without history), and
+// writes the channel's new history (hist[1..], x) to out, rows out_stride floats apart.
+__device__ __forceinline__ float conv_silu(const uint8_t *buf, int f, int c, float x, int W, bool hist, float *out,
+                                           size_t out_stride) {
+    const float *w = reinterpret_cast<const float *>(buf + S_CW + f * 2048) + c * W;
+    const float *h = reinterpret_cast<const float *>(buf + S_CS + f * 3 * 512) + c;
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        if (j >= W - 1) break;
+        const float hj = hist ? h[j * kDK] : 0.f;
+        z = fmaf(w[j], hj, z);
+        out[j * out_stride] = j + 1 < W - 1 ? (hist ? h[(j + 1) * kDK] : 0.f) : x;
+    }
+    z = fmaf(w[W - 1], x, z);
+    return __fdividef(z, 1.f + __expf(-z));
+}
+
 // NW warps (warp w owns rows [w * 128 / NW, (w + 1) * 128 / NW) of the state, lane l the
 // columns 4l .. 4l+3) and NS staging buffers: the copies of the NS units after the one
-// being computed are in flight.
-template <bool GL, int NW, int NS>
+// being computed are in flight.  CV: q, k and v pass through their short convolutions
+// (+ SiLU) first, with the filters and histories staged alongside the unit.
+template <bool GL, bool CV, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const SeqParams p) {
-    using L = DecodeSmem<NW, NS>;
+    using L = DecodeSmem<NW, NS, CV>;
+    constexpr uint32_t kStg = kStage<CV>;
+    static_assert(!CV || NW * 32 >= 2 * kDK, "the fused convolutions give q, k and v to disjoint threads");
     constexpr int NT = NW * 32, RPW = kDK / NW, VPL = kDK / 32;
     extern __shared__ __align__(1024) uint8_t dsm[];
     const uint32_t sb = tc::smem_u32(dsm);
@@ -269,10 +297,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
     const uint32_t eq = p.qkv_bf16 ? 2 : 4;
     const void *gsrc = GL ? p.g_logits : static_cast<const void *>(p.g);
     const uint32_t eg = GL && p.g_logits_bf16 ? 2 : 4, eo = p.gate_bf16 ? 2 : 4;
-    const uint32_t tx = (p.s0 ? 65536u : 0u) + 3u * kDK * eq + kDK * eg + (p.gate ? kDK * eo : 0u);
+    const int W = CV ? p.conv_w : 0;
+    const bool hist = CV && p.cs_in[0];
+    const size_t cD = (size_t)H * kDK;  // channels of each convolution
+    const uint32_t tx = (p.s0 ? 65536u : 0u) + 3u * kDK * eq + kDK * eg + (p.gate ? kDK * eo : 0u) +
+                        (CV ? 3u * kDK * 4u * W + (hist ? 3u * (W - 1) * 512u : 0u) : 0u);
     auto issue = [&](int u, int st) {  // thread 0: every copy of unit u into buffer st
         uint64_t *bar = bars + st;
-        const uint32_t d = sb + (uint32_t)st * kStage;
+        const uint32_t d = sb + (uint32_t)st * kStg;
         tc::mbar_arrive_expect_tx(bar, tx);
         if (p.s0) tc::bulk_load(d, p.s0 + (size_t)u * kDK * kDK, 65536u, bar);
         tc::bulk_load(d + S_Q, static_cast<const uint8_t *>(p.q) + (size_t)u * kDK * eq, kDK * eq, bar);
@@ -281,6 +313,16 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
         tc::bulk_load(d + S_G, static_cast<const uint8_t *>(gsrc) + (size_t)u * kDK * eg, kDK * eg, bar);
         if (p.gate)
             tc::bulk_load(d + S_GATE, static_cast<const uint8_t *>(p.gate) + (size_t)u * kDK * eo, kDK * eo, bar);
+        if constexpr (CV) {
+            const int n = u / H, h = u - n * H;
+            for (int f = 0; f < 3; ++f) {
+                tc::bulk_load(d + S_CW + f * 2048, p.cw[f] + (size_t)h * kDK * W, kDK * 4u * W, bar);
+                if (hist)
+                    for (int j = 0; j < W - 1; ++j)
+                        tc::bulk_load(d + S_CS + (f * 3 + j) * 512,
+                                      p.cs_in[f] + ((size_t)n * (W - 1) + j) * cD + (size_t)h * kDK, 512u, bar);
+            }
+        }
     };
     // beta (or its logit) and, with logits, the head's A_log and this thread's dt_bias:
     // loaded one unit ahead, into registers
@@ -308,7 +350,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
     bool failed = false;
     for (; u < units; u += stride, ++it) {
         const int st = it % NS;
-        const uint8_t *buf = dsm + (uint32_t)st * kStage;
+        const uint8_t *buf = dsm + (uint32_t)st * kStg;
         failed = __syncthreads_or(!tc::mbar_wait(bars + st, (uint32_t)((it / NS) & 1), p.polls));
         if (failed) break;  // the copies did not arrive in time: this unit and the rest are poisoned below
         float s[RPW][VPL];
@@ -324,8 +366,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
         }
         // -- prologue from the staged rows: q, k, exp(g), v, the gate; partial norms
         float pq = 0.f, pk = 0.f, pqk = 0.f, gt = 0.f;
+        // the unit's row of each new convolution history: channel c of row j at [j * cD + c]
+        const size_t cs_row = CV ? ((size_t)(u / H) * (W - 1)) * cD + (size_t)(u % H) * kDK : 0;
         if (tid < kDK) {
-            const float qv = in_elem(buf + S_Q, tid, p.qkv_bf16), kv = in_elem(buf + S_K, tid, p.qkv_bf16);
+            float qv = in_elem(buf + S_Q, tid, p.qkv_bf16), kv = in_elem(buf + S_K, tid, p.qkv_bf16);
+            if constexpr (CV) {
+                qv = conv_silu(buf, 0, tid, qv, W, hist, p.cs_out[0] + cs_row + tid, cD);
+                kv = conv_silu(buf, 1, tid, kv, W, hist, p.cs_out[1] + cs_row + tid, cD);
+            }
             const float z = in_elem(buf + S_G, tid, GL ? p.g_logits_bf16 : 0);
             sq[tid] = qv;
             sk[tid] = kv;
@@ -335,7 +383,12 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
             pqk = qv * kv;
             if (p.gate) gt = in_elem(buf + S_GATE, tid, p.gate_bf16);
         }
-        if (tid >= NT - kDK) sv[tid - (NT - kDK)] = in_elem(buf + S_V, tid - (NT - kDK), p.qkv_bf16);
+        if (tid >= NT - kDK) {
+            const int c = tid - (NT - kDK);
+            float vv = in_elem(buf + S_V, c, p.qkv_bf16);
+            if constexpr (CV) vv = conv_silu(buf, 2, c, vv, W, hist, p.cs_out[2] + cs_row + c, cD);
+            sv[c] = vv;
+        }
         pq = warp_sum(pq);
         pk = warp_sum(pk);
         pqk = warp_sum(pqk);
@@ -446,6 +499,11 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) decode_kernel(const 
         if (tid < kDK) {
             if (p.o) st_out(p.o, (size_t)u * kDK + tid, nan, p.o_bf16);
             if (p.gate) st_out(p.y, (size_t)u * kDK + tid, nan, p.o_bf16);
+            if constexpr (CV) {
+                const size_t row = ((size_t)(u / H) * (W - 1)) * cD + (size_t)(u % H) * kDK + tid;
+                for (int f = 0; f < 3; ++f)
+                    for (int j = 0; j < W - 1; ++j) p.cs_out[f][row + j * cD] = nan;
+            }
         }
     }
 }
@@ -461,14 +519,22 @@ kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return KDA_OK;
     if (K == kDK && V == kDK && p.T == 1 && !p.cu_seqlens && !p.states && p.sT) {
-        using L = DecodeSmem<kDecNW, kDecNS>;
+        using L = DecodeSmem<kDecNW, kDecNS, false>;
+        using LC = DecodeSmem<kDecNW, kDecNS, true>;
         static DeviceOnce configured;
         const int dev = current_device();
         if (!configured.done(dev)) {
-            for (void *fn : {(void *)decode_kernel<false, kDecNW, kDecNS>, (void *)decode_kernel<true, kDecNW, kDecNS>}) {
-                const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::bytes);
+            const struct {
+                const void *fn;
+                uint32_t bytes;
+            } fns[] = {{(const void *)decode_kernel<false, false, kDecNW, kDecNS>, L::bytes},
+                       {(const void *)decode_kernel<true, false, kDecNW, kDecNS>, L::bytes},
+                       {(const void *)decode_kernel<false, true, kDecNW, kDecNS>, LC::bytes},
+                       {(const void *)decode_kernel<true, true, kDecNW, kDecNS>, LC::bytes}};
+            for (const auto &f : fns) {
+                const cudaError_t e = cudaFuncSetAttribute(f.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, f.bytes);
                 if (e != cudaSuccess) {
-                    set_error("decode: cannot reserve %u bytes of shared memory: %s", L::bytes, cudaGetErrorString(e));
+                    set_error("decode: cannot reserve %u bytes of shared memory: %s", f.bytes, cudaGetErrorString(e));
                     return KDA_ERR_CUDA;
                 }
             }
@@ -476,12 +542,22 @@ kda_status launch_kv(const SeqParams &p, cudaStream_t st) {
         }
         const int per_sm = kDecNW == 8 ? 2 : 1;
         const int grid = units < per_sm * sm_count() ? units : per_sm * sm_count();
-        if (p.g_logits)
-            decode_kernel<true, kDecNW, kDecNS><<<grid, kDecNW * 32, L::bytes, st>>>(p);
-        else
-            decode_kernel<false, kDecNW, kDecNS><<<grid, kDecNW * 32, L::bytes, st>>>(p);
+        if (p.conv_w) {
+            if (p.g_logits)
+                decode_kernel<true, true, kDecNW, kDecNS><<<grid, kDecNW * 32, LC::bytes, st>>>(p);
+            else
+                decode_kernel<false, true, kDecNW, kDecNS><<<grid, kDecNW * 32, LC::bytes, st>>>(p);
+        } else if (p.g_logits) {
+            decode_kernel<true, false, kDecNW, kDecNS><<<grid, kDecNW * 32, L::bytes, st>>>(p);
+        } else {
+            decode_kernel<false, false, kDecNW, kDecNS><<<grid, kDecNW * 32, L::bytes, st>>>(p);
+        }
         note_launch();
         return check_launch("decode_kernel");
+    }
+    if (p.conv_w) {
+        set_error("recurrent: the fused short convolutions need the decode step (K = V = 128, T = 1, dense)");
+        return KDA_ERR_UNSUPPORTED;
     }
     if (p.g_logits)
         recurrent_kernel<K, V, true><<<units, kThreads, 0, st>>>(p);

@@ -24,6 +24,13 @@ Conv1d's default initialisation for a depthwise filter of 4 taps, U(-1/2, 1/2)
 (bound 1/sqrt(fan_in), fan_in = 4); the conv state N(0, 1) (earlier inputs).
   conv_prefill  B=1   T=8192  D=36864  W=4, zero state
   conv_decode   B=256 T=1     D=36864  W=4, state given (updated in place)
+
+Decode with the convolutions fused (make_decode_conv_inputs): the decode workload's
+g, beta (or logits), state, gate and norm weight, with q, k, v replaced by the raw
+projections (N(0, 1) in bf16, [B, H, 128] each), three filters [H*128, W] drawn as
+above and three histories [B, W-1, H*128] of N(0, 1) values rounded to bf16 (earlier
+raw inputs), each held in fp32.
+  decode_conv   B=256 H=96 d=128 W=4, histories given (updated in place)
 """
 from __future__ import annotations
 
@@ -187,3 +194,26 @@ def make_conv_inputs(w: str | None = None, device="cpu", *, B: int | None = None
     b = torch.empty((D,), device=device).uniform_(-W ** -0.5, W ** -0.5, generator=gen) if bias else None
     s0 = torch.randn((N, W - 1, D), generator=gen, device=device) if state else None
     return dict(x=x, weight=weight, bias=b, conv_state=s0, cu_seqlens=cu, B=B, T=T, D=D, W=W, N=N)
+
+
+def make_decode_conv_inputs(B: int = 256, H: int = 96, W: int = 4, *, device="cpu", seed: int = 8,
+                            history: bool = True, logits: bool = False) -> dict:
+    """Seeded inputs of one decode step with the short convolutions fused: the decode
+    workload's inputs at [B, H, 128] (make_logit_inputs' with ``logits``), q, k, v
+    replaced by raw projections, plus conv_weight (three [H*128, W] fp32) and
+    conv_state (three [B, W-1, H*128] fp32, or None without ``history``)."""
+    make = make_logit_inputs if logits else make_inputs
+    d = make("decode", device, B=B, H=H, seed=seed)
+    d = {n: (t.squeeze(1) if torch.is_tensor(t) and t.dim() >= 3 and n != "initial_state" else t)
+         for n, t in d.items()}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(30_000 + seed)
+    D = H * d["K"]
+    d["q"], d["k"], d["v"] = (torch.randn((B, H, d["K"]), generator=gen, device=device).to(torch.bfloat16)
+                              for _ in range(3))
+    d["conv_weight"] = tuple(torch.empty((D, W), device=device).uniform_(-W ** -0.5, W ** -0.5, generator=gen)
+                             for _ in range(3))
+    d["conv_state"] = tuple(torch.randn((B, W - 1, D), generator=gen, device=device).to(torch.bfloat16).float()
+                            for _ in range(3)) if history else None
+    d["W"] = W
+    return d

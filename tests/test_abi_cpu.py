@@ -171,6 +171,43 @@ def test_recurrent_step_rejects(lib):
     assert f(*misaligned) == INVALID
 
 
+def conv_step_call(lib, *, W=4, K=128, s_in=None, s_out=None, w=None, gates="plain", q=None):
+    """kda_recurrent_step_conv on fake device pointers (B=4, H=2); returns the status."""
+    P3 = ctypes.c_void_p * 3
+    w = w or [fake(20), fake(21), fake(22)]
+    s_in = [fake(23), fake(24), fake(25)] if s_in is None else s_in
+    s_out = [fake(26), fake(27), fake(28)] if s_out is None else s_out
+    g = (fake(4), fake(5), None, BF16, None, None, -5.0, None, BF16)
+    lg = (None, None, fake(10), BF16, fake(11), fake(12), -5.0, fake(13), BF16)
+    both = (fake(4), fake(5), fake(10), BF16, fake(11), fake(12), -5.0, fake(13), BF16)
+    gate_args = {"plain": g, "logits": lg, "both": both}[gates]
+    return lib.kda_recurrent_step_conv(
+        q or fake(1), fake(2), fake(3), BF16, P3(*w), W, None if s_in == "none" else P3(*s_in),
+        None if s_out == "none" else P3(*s_out), *gate_args, fake(6), fake(7), fake(8), F32, 4, 2, K, 128, 0.088,
+        1, fake(14), BF16, fake(15), 1e-5, fake(16), None)
+
+
+def test_recurrent_step_conv_rejects(lib):
+    assert conv_step_call(lib, gates="both") == INVALID
+    assert b"either g and beta" in lib.kda_last_error()
+    assert conv_step_call(lib, W=5) == UNSUPPORTED
+    assert conv_step_call(lib, W=1) == UNSUPPORTED
+    assert conv_step_call(lib, K=64) == UNSUPPORTED
+    assert conv_step_call(lib, s_out="none") == INVALID
+    assert conv_step_call(lib, s_out=[fake(26), None, fake(28)]) == INVALID
+    assert conv_step_call(lib, s_in=[fake(23), None, fake(25)]) == INVALID
+    assert b"all three histories or none" in lib.kda_last_error()
+    assert conv_step_call(lib, w=[fake(20), fake(21) + 4, fake(22)]) == INVALID  # misaligned
+    # a new history over q, over another filter's history, or partly over its own
+    assert conv_step_call(lib, s_out=[fake(26), fake(1), fake(28)]) == INVALID
+    assert conv_step_call(lib, s_out=[fake(24), fake(27), fake(28)]) == INVALID
+    assert conv_step_call(lib, s_out=[fake(23) + 16, fake(27), fake(28)]) == INVALID
+    assert b"conv_state_in[0] itself" in lib.kda_last_error()
+    assert conv_step_call(lib, s_out=[fake(26), fake(26) + 1024, fake(28)]) == INVALID
+    # a weight under the step's output y
+    assert conv_step_call(lib, w=[fake(20), fake(16), fake(22)]) == INVALID
+
+
 def test_recurrent_fwd_rejects(lib):
     f = lib.kda_recurrent_fwd
     base = [FAKE, FAKE, FAKE, BF16, FAKE, FAKE, None, None, FAKE, F32, None, None, None, 0, 1, 16, 2, 64, 64,
