@@ -547,8 +547,8 @@ def bench_e2e(args, world, d):
     dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
     return {"value": world * B * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": dt * 1e3, "steps": steps,
-            "path": f"chunk_fwd on pinned host tensors: {kda.HOST_SEGMENT}-token segments, copy-in / compute / "
-                    "copy-out on three streams"}
+            "path": f"chunk_fwd on pinned host tensors -> the C entry kda_chunk_fwd_host: {kda.HOST_SEGMENT}-token "
+                    "segments, 2-D copies in / fused kernel / copies out on three streams"}
 
 
 def cpu_baseline(d, heads: int):

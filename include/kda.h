@@ -243,6 +243,51 @@ kda_status kda_chunk_fwd_logits(const void *q, const void *k, const void *v, kda
                                 size_t workspace_bytes, int mode, void *stream);
 
 /*
+ * kda_chunk_fwd_host / kda_chunk_fwd_logits_host -- kda_chunk_fwd (_logits) for a
+ * caller whose tensors are in HOST memory: a dense prompt (B sequences of T tokens)
+ * streamed through the device in segments of `segment` tokens.
+ *
+ * Page: nnterp encyclopedia "Kimi-Linear", section 03 "Loading" (the chunked kernel
+ * carries the state from one 64-token chunk to the next; a segment boundary is a
+ * chunk boundary, so the outputs equal those of one kda_chunk_fwd call on device
+ * copies of the same tensors, bit for bit).
+ *
+ * Every tensor argument -- q, k, v, g, beta (or g_logits, beta_logits, A_log,
+ * dt_bias), initial_state, final_state, o, gate, norm_w, y -- is a HOST pointer with
+ * the layout of kda_chunk_fwd (dense only: no cu_seqlens).  Page-locked memory
+ * (cudaHostAlloc / cudaHostRegister) lets the copies overlap the kernels; pageable
+ * memory works, with copies that do not overlap.  Outputs must not overlap inputs.
+ *
+ *   segment    tokens per segment, a multiple of 64; 0 = 1024.
+ *   workspace  DEVICE memory of at least kda_chunk_fwd_host_workspace_size(B, H, K,
+ *              V, segment) bytes, 256-byte aligned: the state, two buffers of each
+ *              tensor's segment, the small parameters.  Owned by the caller; in use
+ *              until `stream` reaches the end of the call.
+ *   stream     the caller's stream: the kernels run on it, the copies on two streams
+ *              the call creates and destroys, and `stream` waits for the last copy, so
+ *              the outputs are in host memory once `stream` has completed
+ *              (cudaStreamSynchronize).  The host buffers must stay valid until then.
+ * Other arguments and errors as kda_chunk_fwd.
+ */
+size_t kda_chunk_fwd_host_workspace_size(int B, int H, int K, int V, int segment);
+
+kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v, kda_dtype qkv_dtype, const float *g,
+                              const float *beta, const float *initial_state, float *final_state, void *o,
+                              kda_dtype o_dtype, int B, int T, int H, int K, int V, int chunk, float scale,
+                              int use_qk_l2norm, const void *gate, kda_dtype gate_dtype, const float *norm_w,
+                              float eps, void *y, int segment, void *workspace, size_t workspace_bytes, int mode,
+                              void *stream);
+
+kda_status kda_chunk_fwd_logits_host(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                     const void *g_logits, kda_dtype g_logits_dtype, const float *A_log,
+                                     const float *dt_bias, float g_lower_bound, const void *beta_logits,
+                                     kda_dtype beta_logits_dtype, const float *initial_state, float *final_state,
+                                     void *o, kda_dtype o_dtype, int B, int T, int H, int K, int V, int chunk,
+                                     float scale, int use_qk_l2norm, const void *gate, kda_dtype gate_dtype,
+                                     const float *norm_w, float eps, void *y, int segment, void *workspace,
+                                     size_t workspace_bytes, int mode, void *stream);
+
+/*
  * kda_recurrent_fwd -- the token-by-token form over T tokens (fp32 arithmetic).
  *
  * Pages: nnterp "Kimi-Linear" section 03 "Loading" (the token-by-token kernel;

@@ -67,6 +67,12 @@ def _load():
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_workspace_size.argtypes = [I, I, I, I]
         lib.kda_chunk_workspace_size.restype = Z
+        lib.kda_chunk_fwd_host_workspace_size.argtypes = [I, I, I, I, I]
+        lib.kda_chunk_fwd_host_workspace_size.restype = Z
+        lib.kda_chunk_fwd_host.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, I, P, F, P, I,
+                                           P, Z, I, P]
+        lib.kda_chunk_fwd_logits_host.argtypes = [P, P, P, I, P, I, P, P, F, P, I, P, P, P, I, I, I, I, I, I, I,
+                                                  F, I, P, I, P, F, P, I, P, Z, I, P]
         lib.kda_recurrent_fwd.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I,
                                           P, I, P, F, P, P]
         lib.kda_recurrent_step.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, F,
@@ -83,7 +89,7 @@ def _load():
                                                 I, I, I, I, F, I, P, I, P, F, P, P]
         for fn in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_recurrent_step", "kda_gated_rmsnorm",
                    "kda_short_conv_fwd", "kda_chunk_fwd_logits", "kda_recurrent_step_logits", "kda_o_proj",
-                   "kda_recurrent_step_conv"):
+                   "kda_recurrent_step_conv", "kda_chunk_fwd_host", "kda_chunk_fwd_logits_host"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.kda_device_status.argtypes = [P]
         lib.kda_device_status.restype = ctypes.c_int
@@ -255,112 +261,50 @@ def _pinned(t):
 
 
 def _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, output_final_state, gate,
-                         norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace=None):
-    """A host-resident prompt (B = 1) through the device in HOST_SEGMENT-token segments on
-    three streams: segment i+1's inputs are copied in while segment i runs (its state
-    handed on in place on the device) and segment i-1's outputs are copied out, so the
-    host link, not the kernel, sets the pace.  Same results as one call: the chunked
-    kernel carries the state between calls exactly as between chunks."""
+                         norm_w, eps, out_dtype, mode, return_o, o, y, final_state):
+    """A host-resident dense prompt through kda_chunk_fwd_host (_logits_host): the library
+    streams it through the device in HOST_SEGMENT-token segments, copies in and out on two
+    streams of its own while the kernels run on the current stream.  Inputs are made
+    page-locked (copied once if they are not); outputs are page-locked host tensors (or the
+    caller's).  The fused kernel runs each segment; the result equals one device call."""
     lib = _load()
     dev = torch.device("cuda", torch.cuda.current_device())
     B, T, H, K = q.shape
     V = v.shape[-1]
-    seg = HOST_SEGMENT
-    n_seg = (T + seg - 1) // seg
     if scale is None:
         scale = K ** -0.5
-    # host sources (pinned, so every copy is asynchronous) and host destinations
-    srcs = {"q": q, "k": k, "v": v}
-    if lg is None:
-        srcs.update(g=gb[0].to(torch.float32), beta=gb[1].to(torch.float32))
-    else:
-        srcs.update(z=lg[0], b=lg[1])
-    if gate is not None:
-        srcs["gate"] = gate
-    srcs = {n: _pinned(t.contiguous()) for n, t in srcs.items()}
+    pin = lambda t: None if t is None else _pinned(t.detach().contiguous())
+    host32 = lambda t: None if t is None else t.detach().to("cpu", torch.float32).contiguous()
+    q, k, v = pin(q), pin(k), pin(v)
     want_o = return_o or gate is None or o is not None
-    o_h = None
-    if want_o:
-        o_h = o if o is not None else torch.empty((B, T, H, V), dtype=out_dtype).pin_memory()
-    y_h = None
+    o_h = (o if o is not None else torch.empty((B, T, H, V), dtype=out_dtype).pin_memory()) if want_o else None
+    y_h = norm_h = None
     if gate is not None:
+        gate = pin(gate)
+        norm_h = host32(norm_w)
         y_h = y if y is not None else torch.empty((B, T, H * V), dtype=out_dtype).pin_memory()
     fs_h = final_state if final_state is not None else (
-        torch.empty((1, H, K, V), dtype=torch.float32).pin_memory() if output_final_state else None)
-    # device: double-buffered input / output segments, one state buffer updated in place
-    ins = [{n: torch.empty((1, seg) + tuple(t.shape[2:]), dtype=t.dtype, device=dev) for n, t in srcs.items()}
-           for _ in range(2)]
-    outs = [{"o": torch.empty((1, seg, H, V), dtype=out_dtype, device=dev) if want_o else None,
-             "y": torch.empty((1, seg, H * V), dtype=out_dtype, device=dev) if gate is not None else None}
-            for _ in range(2)]
-    state = torch.zeros((1, H, K, V), dtype=torch.float32, device=dev)
-    if initial_state is not None:
-        state.copy_(initial_state.to(torch.float32))
-    extras = {}
-    if lg is not None:
-        extras = dict(A_log=_prep(lg[2], dev, torch.float32), dt_bias=_prep(lg[3], dev, torch.float32), lb=lg[4])
-    if gate is not None:
-        norm_w = _prep(norm_w, dev, torch.float32)
-    main = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    s_in.wait_stream(main)
-    s_out.wait_stream(main)
-    in_ready = [torch.cuda.Event() for _ in range(n_seg)]
-    done = [torch.cuda.Event() for _ in range(n_seg)]
-    out_done = [torch.cuda.Event() for _ in range(n_seg)]
+        torch.empty((B, H, K, V), dtype=torch.float32).pin_memory() if output_final_state else None)
+    s0 = host32(initial_state)
+    need = int(lib.kda_chunk_fwd_host_workspace_size(B, H, K, V, HOST_SEGMENT))
+    key = ("host", dev.index)
+    ws = _CHUNK_WS.get(key)
+    if ws is None or ws.numel() < need:
+        _CHUNK_WS.pop(key, None)
+        ws = _CHUNK_WS[key] = torch.empty(need, dtype=torch.uint8, device=dev)
     mode_i = _MODES[mode] if isinstance(mode, str) else int(mode)
-    ws_ptr, ws_bytes = _chunk_workspace(workspace if mode_i != MODE_FP32 else None, dev, 1, seg, H, 0)
-
-    def copy_in(i):
-        a, b_ = i * seg, min(T, (i + 1) * seg)
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(done[i - 2])  # the kernel of segment i-2 read this buffer
-            for n, t in srcs.items():
-                ins[i % 2][n][:, :b_ - a].copy_(t[:, a:b_], non_blocking=True)
-            in_ready[i].record(s_in)
-
-    copy_in(0)
-    for i in range(n_seg):
-        if i + 1 < n_seg:
-            copy_in(i + 1)
-        a, b_ = i * seg, min(T, (i + 1) * seg)
-        n_tok = b_ - a
-        x, ob = ins[i % 2], outs[i % 2]
-        main.wait_event(in_ready[i])
-        if i >= 2:
-            main.wait_event(out_done[i - 2])  # segment i-2's outputs left this buffer
-        st = ctypes.c_void_p(main.cuda_stream)
-        o_d = ob["o"][:, :n_tok] if want_o else None
-        y_d = ob["y"][:, :n_tok] if gate is not None else None
-        tail = (_ptr(state), _ptr(state), _ptr(o_d), _dt(o_d if o_d is not None else y_d), None, None, 0, 1, n_tok,
-                H, K, V, int(chunk), float(scale), int(bool(use_qk_l2norm)),
-                _ptr(x["gate"][:, :n_tok]) if gate is not None else None,
-                _dt(x["gate"]) if gate is not None else BF16, _ptr(norm_w), float(eps), _ptr(y_d), ws_ptr, ws_bytes,
-                mode_i, st)
-        qd, kd, vd = x["q"][:, :n_tok], x["k"][:, :n_tok], x["v"][:, :n_tok]
-        if lg is None:
-            _check(lib.kda_chunk_fwd(_ptr(qd), _ptr(kd), _ptr(vd), _dt(qd), _ptr(x["g"][:, :n_tok]),
-                                     _ptr(x["beta"][:, :n_tok]), *tail))
-        else:
-            zd, bd = x["z"][:, :n_tok], x["b"][:, :n_tok]
-            _check(lib.kda_chunk_fwd_logits(_ptr(qd), _ptr(kd), _ptr(vd), _dt(qd), _ptr(zd), _dt(zd),
-                                            _ptr(extras["A_log"]), _ptr(extras["dt_bias"]), extras["lb"], _ptr(bd),
-                                            _dt(bd), *tail))
-        done[i].record(main)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done[i])
-            if want_o:
-                o_h[:, a:b_].copy_(o_d, non_blocking=o_h.is_pinned())
-            if gate is not None:
-                y_h[:, a:b_].copy_(y_d, non_blocking=y_h.is_pinned())
-            out_done[i].record(s_out)
-    if fs_h is not None:
-        with torch.cuda.stream(s_out):
-            s_out.wait_stream(main)
-            fs_h.copy_(state, non_blocking=fs_h.is_pinned())
-    s_out.synchronize()
-    main.synchronize()
+    tail = (_ptr(s0), _ptr(fs_h), _ptr(o_h), _dt(o_h if o_h is not None else y_h), B, T, H, K, V, int(chunk),
+            float(scale), int(bool(use_qk_l2norm)), _ptr(gate), _dt(gate) if gate is not None else BF16, _ptr(norm_h),
+            float(eps), _ptr(y_h), HOST_SEGMENT, ctypes.c_void_p(ws.data_ptr()), ws.numel(), mode_i, _stream())
+    if lg is None:
+        g, beta = pin(gb[0].to(torch.float32)), pin(gb[1].to(torch.float32))
+        _check(lib.kda_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), *tail))
+    else:
+        z, b, A_log, dt_bias, lb = lg
+        z, b, A_log, dt_bias = pin(z), pin(b), host32(A_log), host32(dt_bias)
+        _check(lib.kda_chunk_fwd_logits_host(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(z), _dt(z), _ptr(A_log),
+                                             _ptr(dt_bias), lb, _ptr(b), _dt(b), *tail))
+    torch.cuda.current_stream().synchronize()  # the outputs are in host memory once the stream is done
     o_ret = o_h if return_o or gate is None else None
     if gate is not None:
         return o_ret, fs_h, y_h
@@ -384,11 +328,12 @@ def _chunk(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm, cu_seqle
            norm_w, eps, out_dtype, mode, return_o, o, y, final_state, workspace=None):
     lib = _load()
     host = q.device.type != "cuda"
-    if (host and cu_seqlens is None and q.shape[0] == 1 and q.shape[1] >= 2 * HOST_SEGMENT
-            and torch.cuda.is_available()):
+    on_host = lambda t: t is None or t.device.type == "cpu"
+    if (host and cu_seqlens is None and q.shape[1] >= 2 * HOST_SEGMENT and workspace is None
+            and on_host(o) and on_host(y) and on_host(final_state) and torch.cuda.is_available()):
         return _chunk_host_streamed(q, k, v, gb, lg, initial_state, scale, chunk, use_qk_l2norm,
                                     output_final_state, gate, norm_w, eps, out_dtype, mode, return_o, o, y,
-                                    final_state, workspace)
+                                    final_state)
     dev = _device_of(q, k, v)
     dests = (o, final_state, y) if host else None
     if host:

@@ -215,15 +215,7 @@ kda::SeqParams make_params(const void *q, const void *k, const void *v, int qkv_
     return p;
 }
 
-// The decay / write-strength logits of the *_logits entry points.
-struct GateLogits {
-    const void *z;
-    int z_dtype;
-    const float *A_log, *dt_bias;
-    float lower;
-    const void *b;
-    int b_dtype;
-};
+using kda::GateLogits;
 
 kda_status check_logits(const char *fn, const GateLogits &gl, bool no_tokens) {
     KDA_REQUIRE(gl.A_log, KDA_ERR_INVALID_ARG, "%s: A_log must not be NULL", fn);
@@ -445,6 +437,16 @@ kda_status chunk_fwd_entry(const char *fn, const void *q, const void *k, const v
     return chunk_impl(fn, q, k, v, qkv_dtype, g, beta, nullptr, initial_state, final_state, o, o_dtype, cu_seqlens,
                       cu_seqlens_host, n_seqs, B, T, H, K, V, chunk, scale, use_qk_l2norm, gate, gate_dtype, norm_w,
                       eps, y, workspace, workspace_bytes, mode, stream);
+}
+
+kda_status chunk_call(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                      const float *g, const float *beta, const GateLogits *gl, const float *initial_state,
+                      float *final_state, void *o, kda_dtype o_dtype, int B, int T, int H, int K, int V, int chunk,
+                      float scale, int use_qk_l2norm, const void *gate, kda_dtype gate_dtype, const float *norm_w,
+                      float eps, void *y, int mode, void *stream) {
+    return chunk_impl(fn, q, k, v, qkv_dtype, g, beta, gl, initial_state, final_state, o, o_dtype, nullptr, nullptr,
+                      0, B, T, H, K, V, chunk, scale, use_qk_l2norm, gate, gate_dtype, norm_w, eps, y, nullptr, 0,
+                      mode, stream);
 }
 
 }  // namespace kda

@@ -171,6 +171,24 @@ kda_status chunk_fwd_entry(const char *fn, const void *q, const void *k, const v
                            const void *gate, kda_dtype gate_dtype, const float *norm_w, float eps, void *y,
                            void *workspace, size_t workspace_bytes, int mode, void *stream);
 
+// The decay / write-strength logits of the *_logits entry points.
+struct GateLogits {
+    const void *z;
+    int z_dtype;
+    const float *A_log, *dt_bias;
+    float lower;
+    const void *b;
+    int b_dtype;
+};
+
+// kda_chunk_fwd (gl null) or kda_chunk_fwd_logits (gl given) on device pointers, with
+// every check of those entry points and `fn` in the error messages.
+kda_status chunk_call(const char *fn, const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                      const float *g, const float *beta, const GateLogits *gl, const float *initial_state,
+                      float *final_state, void *o, kda_dtype o_dtype, int B, int T, int H, int K, int V, int chunk,
+                      float scale, int use_qk_l2norm, const void *gate, kda_dtype gate_dtype, const float *norm_w,
+                      float eps, void *y, int mode, void *stream);
+
 // ---------------------------------------------------------------------------
 // launchers (one per translation unit); each returns KDA_OK or an error status
 

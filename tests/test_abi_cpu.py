@@ -208,6 +208,27 @@ def test_recurrent_step_conv_rejects(lib):
     assert conv_step_call(lib, w=[fake(20), fake(16), fake(22)]) == INVALID
 
 
+def test_chunk_fwd_host_rejects(lib):
+    f = lib.kda_chunk_fwd_host
+    need = lib.kda_chunk_fwd_host_workspace_size(1, 2, 128, 128, 256)
+    assert need > 2 * 256 * 2 * (3 * 128 * 4)  # two buffers of every segment tensor
+    assert lib.kda_chunk_fwd_host_workspace_size(0, 2, 128, 128, 256) == 0
+
+    def call(seg=256, ws=fake(30), ws_bytes=need, o=fake(8), chunk=64):
+        return f(fake(1), fake(2), fake(3), BF16, fake(4), fake(5), None, fake(7), o, F32, 1, 1000, 2, 128, 128,
+                 chunk, 0.088, 1, None, BF16, None, 1e-5, None, seg, ws, ws_bytes, 0, None)
+    assert call(seg=100) == INVALID
+    assert b"multiple of 64" in lib.kda_last_error()
+    assert call(ws_bytes=4096) == INVALID
+    assert b"kda_chunk_fwd_host_workspace_size" in lib.kda_last_error()
+    assert call(ws=fake(30) + 16) == INVALID  # 256-byte alignment
+    assert call(ws=None) == INVALID
+    assert call(chunk=48) == UNSUPPORTED
+    assert call(o=fake(2) + 64) == INVALID  # o over the host k
+    assert b"must not overlap" in lib.kda_last_error()
+    assert call(o=None) == INVALID
+
+
 def test_recurrent_fwd_rejects(lib):
     f = lib.kda_recurrent_fwd
     base = [FAKE, FAKE, FAKE, BF16, FAKE, FAKE, None, None, FAKE, F32, None, None, None, 0, 1, 16, 2, 64, 64,
