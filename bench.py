@@ -517,9 +517,13 @@ def bench_o_proj(args, world, peaks):
             roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": ach / peaks["bf16_tflops"], "traffic": None, "algorithmic_flop_per_launch": flop}
         roof.update(kernel_ms=kernel_ms, peak_source=peaks["source"])
+        # context only: the same product through torch (cuBLAS) on the same device and inputs
+        lib_fn = lambda: torch.matmul(y, w.t(), out=o)
+        lib_ms = time_steps(lib_fn, steps, args.warmup, world)["call_ms"]
         out[name] = {"metric": "o_proj tokens/s", "value": world * rows / (r["ms_per_step"] * 1e-3), "unit": "tokens/s",
                      "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
-                     "config": {"workload": f"o_proj rows={rows} 12288->7168 bf16 (tcgen05 GEMM)"}, "roofline": roof}
+                     "config": {"workload": f"o_proj rows={rows} 12288->7168 bf16 (tcgen05 GEMM)"}, "roofline": roof,
+                     "torch_cublas_ms_same_inputs": lib_ms}
     return out
 
 
@@ -737,6 +741,8 @@ def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split=None):
     if oproj:
         out["o_proj_256"] = row(oproj["decode"], 1e6, "Mtok_s")
         out["o_proj_8192"] = row(oproj["prefill"], 1e6, "Mtok_s")
+        for k, n in (("o_proj_256", "decode"), ("o_proj_8192", "prefill")):
+            out[k]["cublas_ms"] = round(oproj[n]["torch_cublas_ms_same_inputs"], 4)
     return {k: v for k, v in out.items() if v is not None}
 
 
