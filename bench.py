@@ -46,29 +46,36 @@ PREFILL_LONG_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 512  # q,k,v bf16 + g fp32
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture, mean of two launches: (328.259712 MB - 6.29 MB of final state)
+    # B=1 T=2048 H=96 capture, mean of two launches: (328.503296 MB - 6.29 MB of final state)
     # / (2048 * 96) token-heads
     "prefill_fused": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
-                "bytes_per_unit": (328.259712e6 - 6.291456e6) / (2048 * 96),
-                "capture": "ncu, B=1 T=2048 H=96, g and beta given"},
+                      "sha256": "f60b1a4ae097431bfaeb993bd92996773133f3eebc1f8d8a4fb1e0bc2aacc6ee",
+                      "bytes_per_unit": (328.503296e6 - 6.291456e6) / (2048 * 96),
+                      "capture": "ncu, B=1 T=2048 H=96, g and beta given"},
     # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture, mean of two
-    # launches: (274.432128 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # launches: (274.30464 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                       "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
-                       "bytes_per_unit": (274.432128e6 - 6.291456e6) / (2048 * 96),
+                       "sha256": "f60b1a4ae097431bfaeb993bd92996773133f3eebc1f8d8a4fb1e0bc2aacc6ee",
+                       "bytes_per_unit": (274.30464e6 - 6.291456e6) / (2048 * 96),
                        "capture": "ncu, B=1 T=2048 H=96, bf16 logits"},
     # the same kernel with the fused gated norm (bf16 gate in, bf16 y out), B=1 T=2048 H=96
-    # capture, mean of two launches: (343.342848 MB - 6.29 MB of final state) / (2048 * 96)
+    # capture, mean of two launches: (342.888576 MB - 6.29 MB of final state) / (2048 * 96)
     "prefill_norm": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                     "sha256": "fedb89f23be42782fa8be8a86ddf7433335bce918b7dc466e69c56a08694ec58",
-                     "bytes_per_unit": (343.342848e6 - 6.291456e6) / (2048 * 96),
+                     "sha256": "f60b1a4ae097431bfaeb993bd92996773133f3eebc1f8d8a4fb1e0bc2aacc6ee",
+                     "bytes_per_unit": (342.888576e6 - 6.291456e6) / (2048 * 96),
                      "capture": "ncu, B=1 T=2048 H=96, fused gated norm"},
-    # B=64 capture: mean of two launches, 754.8 MB / (64 * 96) (sequence, head) units
+    # B=64 capture: mean of two launches, 754.667264 MB / (64 * 96) (sequence, head) units
+    # (part of the state written back stays in L2 at the kernel's end: below the algorithmic bytes)
     "decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
-               "sha256": "ede5158c131edfc4a652ea4d3a646abd27d6ef5093fa3bf7fdd0920d87253ef4",
-               "bytes_per_unit": 754.843776e6 / (64 * 96),
+               "sha256": "5b652beb9f24e8ee12b996eb18914cbb7bf46a2a94542e35fbb00fcbfeea303b",
+               "bytes_per_unit": 754.667264e6 / (64 * 96),
                "capture": "ncu, decode B=64 H=96"},
+    # the decode step with the short convolutions fused, B=64 capture: mean of two launches,
+    # 814.222592 MB / (64 * 96) units
+    "decode_conv": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_recurrent.cu",
+                    "sha256": "5b652beb9f24e8ee12b996eb18914cbb7bf46a2a94542e35fbb00fcbfeea303b",
+                    "bytes_per_unit": 814.222592e6 / (64 * 96),
+                    "capture": "ncu, decode B=64 H=96, short convolutions fused"},
     # full-size captures: mean of two launches per (token, channel) element
     "conv_prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
                      "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
@@ -244,27 +251,36 @@ def prefill_inputs(device, T=None):
     return make_inputs("prefill", device=device, T=T)
 
 
-def bench_prefill(args, world, rank, peaks, fused=True):
-    """The headline prefill: the fused tensor-core form (one kernel per (sequence, head), no
-    workspace), or with fused=False the split form (state-independent pre-pass over all
-    chunks and heads, then the per-head chain kernel).  `kernel_ms` is the device time of
-    the whole call, both kernels of the split form together."""
+def bench_prefill(args, world, rank, peaks, form="fused"):
+    """The prefill workload through one tensor-core form: "fused" (one kernel per (sequence,
+    head), no workspace), "concurrent" (the fused kernel with the pre-pass beside it on the
+    idle SMs, a workspace given) or "split" (the pre-pass over all chunks and heads, then
+    the per-head chain kernel).  `kernel_ms` is the device time of the whole call, every
+    kernel of it together (CUDA events around the call on the caller's stream, which the
+    concurrent form's second stream joins)."""
     import torch
     import kimi_delta_attention_gated_gb300 as kda
     d = prefill_inputs("cuda", args.prefill_T)
     B, T, H, K, V = d["B"], d["T"], d["H"], d["K"], d["V"]
     o = torch.empty((B, T, H, V), device="cuda", dtype=torch.float32)
     fs = torch.empty((B, H, K, V), device="cuda", dtype=torch.float32)
-    ws = None if fused else torch.empty(kda.workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
+    ws = None if form == "fused" else torch.empty(kda.workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
+    mode = "split" if form == "split" else args.mode
     fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, scale=d["scale"], chunk=64,
-                               o=o, final_state=fs, mode=args.mode, workspace=ws)
-    r = time_steps(fn, args.steps, args.warmup, world, clocks_index=torch.cuda.current_device() if fused else None)
+                               o=o, final_state=fs, mode=mode, workspace=ws)
+    if form == "concurrent":
+        kda.prepass_hits()
+    r = time_steps(fn, args.steps, args.warmup, world,
+                   clocks_index=torch.cuda.current_device() if form == args.headline else None)
+    hits = kda.prepass_hits() if form == "concurrent" else None
     th = B * T * H
     kernel_ms = r["call_ms"]
     algo_bytes = th * PREFILL_BYTES_PER_TH + B * H * STATE_BYTES
     algo_flop = th * PREFILL_FLOP_PER_TH
     achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
     tflops = algo_flop / (kernel_ms * 1e-3) / 1e12
+    kernels = {"fused": "chunk_tc_kernel", "concurrent": "chunk_tc_kernel + chunk_prep_kernel beside it, one call",
+               "split": "chunk_prep_kernel + chunk_chain_kernel, one call"}[form]
     out = {
         "value": world * B * T / (r["ms_per_step"] * 1e-3),
         "ms_per_step": r["ms_per_step"],
@@ -272,17 +288,19 @@ def bench_prefill(args, world, rank, peaks, fused=True):
         "clocks": r["clocks"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": measured_traffic("prefill_fused" if fused else "prefill", th, B * H * STATE_BYTES),
-                     "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms,
-                     "kernels": "chunk_tc_kernel" if fused else "chunk_prep_kernel + chunk_chain_kernel, one call",
+                     "traffic": measured_traffic("prefill_fused", th, B * H * STATE_BYTES) if form == "fused" else None,
+                     "algorithmic_bytes_per_launch": algo_bytes, "kernel_ms": kernel_ms, "kernels": kernels,
                      "launches_per_call": max(1, r["launches"] // args.steps), "peak_source": peaks["source"]},
         "roofline_tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": tflops / peaks["bf16_tflops"], "algorithmic_flop_per_launch": algo_flop},
         "config": {"workload": f"prefill B={B} T={T} H={H} d={K} chunk=64 zero initial state",
-                   "B": B, "T": T, "H": H, "d": K, "chunk": 64, "mode": args.mode,
+                   "B": B, "T": T, "H": H, "d": K, "chunk": 64, "mode": args.mode, "form": form,
                    "l2_flush": "inputs larger than L2 (1.42 GB read+written per step vs 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
     }
+    if hits is not None:
+        n_chunks = B * H * ((T + 63) // 64) * (args.warmup + args.steps)
+        out["prepass_share"] = hits / n_chunks  # chunks whose grams and UT transform came from the pre-pass
     return out, d
 
 
@@ -308,7 +326,7 @@ def bench_prefill_workload(args, world, peaks, name):
         lens = (cu[1:] - cu[:-1]).tolist()
         workload = f"varlen prefill, {N} packed sequences of {lens} tokens ({T} total), H={H} d={K}, fp32 initial " \
                    "and final states, fp32 o"
-        traffic = measured_traffic("prefill", th, state_bytes)
+        traffic = measured_traffic("prefill_fused", th, state_bytes)
     else:
         y = torch.empty((B, T, H * V), device="cuda", dtype=torch.float32)
         fn = lambda: kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, scale=d["scale"], chunk=64,
@@ -638,10 +656,12 @@ def main():
     ap.add_argument("--mode", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--cpu-heads", type=int, default=96, help="heads of the prefill workload the oracle baseline runs")
     ap.add_argument("--ref-heads", type=int, default=8, help="heads per step of the reference arm")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode_conv", "conv", "kernels", "logits", "norm",
-                                       "varlen", "long", "oproj"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "concurrent", "decode", "decode_conv", "conv", "kernels",
+                                       "logits", "norm", "varlen", "long", "oproj"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
+    ap.add_argument("--headline", choices=["fused", "concurrent"], default="fused",
+                    help="the prefill form timed as the headline value (the other is reported beside it)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
@@ -664,8 +684,11 @@ def main():
     from kimi_delta_attention_gated_gb300 import build as kbuild
     kbuild.build()
     peaks = load_peaks()
-    if args.only in ("decode", "decode_conv", "conv", "kernels", "logits", "norm", "varlen", "long", "oproj"):
-        if args.only == "oproj":
+    if args.only in ("concurrent", "decode", "decode_conv", "conv", "kernels", "logits", "norm", "varlen", "long",
+                     "oproj"):
+        if args.only == "concurrent":  # the prefill's concurrent form alone (profiling runs)
+            res = bench_prefill(args, world, rank, peaks, form="concurrent")[0]
+        elif args.only == "oproj":
             res = bench_o_proj(args, world, peaks)
         elif args.only in ("varlen", "long"):
             res = bench_prefill_workload(args, world, peaks, args.only)
@@ -682,8 +705,10 @@ def main():
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
-    pre, d = bench_prefill(args, world, rank, peaks, fused=True)
-    split = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, fused=False)[0]
+    pre, d = bench_prefill(args, world, rank, peaks, form=args.headline)
+    other_form = "fused" if args.headline == "concurrent" else "concurrent"
+    other = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, form=other_form)[0]
+    split = None if args.only == "prefill" else bench_prefill(args, world, rank, peaks, form="split")[0]
     dec = None if (args.no_decode or args.only == "prefill") else bench_decode(args, world, peaks)
     if dec is not None:
         dec["fused_short_conv"] = bench_decode_conv(args, world, peaks)
@@ -714,12 +739,17 @@ def main():
         "prefill_varlen": varlen, "prefill_long_norm": long_, "gpu": torch.cuda.get_device_name(),
         "prefill_split_two_kernels": None if split is None else {
             "value": split["value"], "ms_per_step": split["ms_per_step"], "roofline": split["roofline"]},
+        f"prefill_{other_form}": None if other is None else {
+            "value": other["value"], "ms_per_step": other["ms_per_step"], "roofline": other["roofline"],
+            "prepass_share": other.get("prepass_share")},
     }
-    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split)
+    if pre.get("prepass_share") is not None:
+        line["prepass_share"] = pre["prepass_share"]
+    line["summary"] = summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split, other, other_form)
     print(json.dumps(line), flush=True)
 
 
-def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split=None):
+def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split=None, other=None, other_form=None):
     """Every timed workload in a few numbers, last on the line so that a reader of the
     line's tail sees all of them: kernel ms per launch, throughput and the fraction of
     the binding roofline (of the measured peak)."""
@@ -733,6 +763,11 @@ def summary(pre, dec, varlen, long_, logits, norm, conv, oproj, split=None):
            "prefill_long_norm": row(long_, 1e6, "Mtok_s"), "decode_B256": row(dec, 1e3, "Ktok_s"),
            "prefill_logits": row(logits, 1e6, "Mtok_s"), "prefill_norm_bf16": row(norm, 1e6, "Mtok_s"),
            "prefill_T8192_split": row(split, 1e6, "Mtok_s")}
+    if other is not None:
+        out[f"prefill_T8192_{other_form}"] = row(other, 1e6, "Mtok_s")
+    for r, key in ((pre, "prefill_T8192"), (other, f"prefill_T8192_{other_form}")):
+        if r is not None and r.get("prepass_share") is not None:
+            out[key]["prepass_share"] = round(r["prepass_share"], 3)
     if dec and dec.get("fused_short_conv"):
         out["decode_conv_B256"] = row(dec["fused_short_conv"], 1e3, "Ktok_s")
     if conv:

@@ -72,7 +72,8 @@ typedef enum kda_dtype {
 typedef enum kda_mode {
     KDA_MODE_AUTO = 0,    /* tensor-core path where supported, else the fp32 path */
     KDA_MODE_TENSOR = 1,  /* tcgen05 path only (K = V = 128, chunk = 64); else UNSUPPORTED */
-    KDA_MODE_FP32 = 2     /* CUDA-core fp32 chunked path (any supported K, V, chunk) */
+    KDA_MODE_FP32 = 2,    /* CUDA-core fp32 chunked path (any supported K, V, chunk) */
+    KDA_MODE_SPLIT = 3    /* tcgen05 path, the two-kernel split form (needs a workspace) */
 } kda_mode;
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -121,6 +122,16 @@ kda_status kda_device_status(void *stream);
 kda_status kda_set_wait_limit(int64_t polls);
 
 /*
+ * kda_chunk_prepass_hits -- how many chunks of the concurrent form (kda_chunk_fwd with a
+ * workspace) took their state-independent operands from the pre-pass rather than
+ * forming them in the fused kernel, since the last call (a diagnostic of how much
+ * of the work the idle SMs took over).  Synchronises `stream`, reads the current
+ * device's counter into *chunks and clears it.  KDA_ERR_INVALID_ARG for a NULL
+ * chunks, KDA_ERR_CUDA if the stream or the read failed.  No counterpart on the pages.
+ */
+kda_status kda_chunk_prepass_hits(void *stream, uint64_t *chunks);
+
+/*
  * kda_chunk_fwd -- chunked prefill over whole prompts.
  *
  * Pages: nnterp "Kimi-Linear" section 03 "Loading" (the chunked kernel carries
@@ -148,15 +159,20 @@ kda_status kda_set_wait_limit(int64_t polls);
  * chunk: tokens per chunk, 16, 32 or 64 (the tensor path needs 64).
  * scale: applied to q^ (1/sqrt(K) for the layer).  use_qk_l2norm: 0 or 1.
  * Supported K, V: 32, 64, 128 (fp32 path); 128 (tensor path).
- * workspace: caller-owned device scratch of workspace_bytes, or NULL.  On the
- *   tensor path a workspace of at least kda_chunk_workspace_size(B, T, H, n_seqs)
- *   bytes selects the split form: one kernel forms every chunk's state-independent
- *   operands (grams, UT transform) in parallel over all chunks and heads and writes
- *   them there, then one CTA per (sequence, head) runs the state through the chunks;
- *   with NULL one fused kernel per (sequence, head) does both.  The two forms give
- *   the same bits.  A workspace that is too small, misaligned or overlaps a tensor of
- *   the call is KDA_ERR_INVALID_ARG; the fp32 path ignores it.  Its contents are
- *   scratch: overwritten by the call, meaningless after it.
+ * workspace: caller-owned device scratch of workspace_bytes, or NULL.  With NULL
+ *   the tensor path runs one fused kernel per (sequence, head).  A workspace of at
+ *   least kda_chunk_workspace_size(B, T, H, n_seqs) bytes lets it use the SMs that
+ *   kernel leaves idle (N * H below the SM count): a pre-pass kernel on a stream the
+ *   call creates forms chunks' state-independent operands (grams, UT transform) ahead
+ *   of the fused kernel, which takes each one that is ready when it gets there and
+ *   forms the rest itself, never waiting (the concurrent form; the caller's stream
+ *   covers both kernels).  With mode KDA_MODE_SPLIT the pre-pass instead forms every
+ *   chunk's operands first, then one CTA per (sequence, head) runs the state through
+ *   the chunks (the split form).  All forms give the same bits.  A workspace that is
+ *   too small, misaligned or overlaps a tensor of the call is KDA_ERR_INVALID_ARG; the
+ *   fp32 path ignores it.  Its contents are scratch: overwritten by the call,
+ *   meaningless after it.  Calls that may overlap on the GPU need workspaces of
+ *   their own.
  * mode: a kda_mode.  Returns a kda_status.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
@@ -170,9 +186,11 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, kda_dtype 
 
 /*
  * kda_chunk_workspace_size -- bytes of the workspace kda_chunk_fwd and
- * kda_chunk_fwd_logits need for the split tensor-core form: 32 KiB per (chunk slot,
- * head) for (ceil(B * T / 64) + N) slots, N = n_seqs in varlen mode (n_seqs > 0),
- * else B.  0 for arguments no call accepts.  Host only; launches nothing.
+ * kda_chunk_fwd_logits take for the concurrent and split tensor-core forms: 32 KiB per
+ * (chunk slot, head) for (ceil(B * T / 64) + N) slots, N = n_seqs in varlen mode
+ * (n_seqs > 0), else B, then a 4-byte flag per (slot, head) and a 4-byte progress
+ * word per (sequence, head), each array 256-byte aligned.  0 for arguments no call
+ * accepts.  Host only; launches nothing.
  */
 size_t kda_chunk_workspace_size(int B, int T, int H, int n_seqs);
 
@@ -198,9 +216,10 @@ size_t kda_chunk_workspace_size(int B, int T, int H, int n_seqs);
  *     the array's device address (cudaGetSymbolAddress, once per device); make that
  *     first call before any stream capture.
  *   - Every call shares the one array and leaves its contents behind.  Nothing in it
- *     needs to start at zero: the first kernel of a call writes every byte the second
- *     reads.  Calls whose work can overlap on the GPU (different streams, different
- *     host threads) race on the array and must be ordered by the caller.
+ *     needs to start at zero: a call clears the flags it uses itself and writes every
+ *     other byte before reading it.  Calls whose work can overlap on the GPU
+ *     (different streams, different host threads) race on the array and must be
+ *     ordered by the caller.
  *   - Results are identical to kda_chunk_fwd with a workspace (the same kernels).
  * No counterpart on the pages: it is an interface for a class of callers.
  */

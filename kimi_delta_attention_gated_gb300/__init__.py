@@ -24,8 +24,8 @@ import torch
 
 __all__ = ["chunk_fwd", "chunk_fwd_logits", "recurrent_fwd", "recurrent_step", "recurrent_step_logits",
            "gated_rmsnorm", "short_conv", "o_proj", "launch_count", "device_status", "set_wait_limit",
-           "workspace_size", "release_workspaces",
-           "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32"]
+           "workspace_size", "release_workspaces", "prepass_hits",
+           "library_path", "KDAError", "MODE_AUTO", "MODE_TENSOR", "MODE_FP32", "MODE_SPLIT"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda.so")
@@ -33,8 +33,8 @@ _lib = None
 _lock = threading.Lock()
 
 BF16, F32 = 0, 1
-MODE_AUTO, MODE_TENSOR, MODE_FP32 = 0, 1, 2
-_MODES = {"auto": MODE_AUTO, "tensor": MODE_TENSOR, "fp32": MODE_FP32}
+MODE_AUTO, MODE_TENSOR, MODE_FP32, MODE_SPLIT = 0, 1, 2, 3
+_MODES = {"auto": MODE_AUTO, "tensor": MODE_TENSOR, "fp32": MODE_FP32, "split": MODE_SPLIT}
 _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
            4: "KDA_ERR_TIMEOUT"}
 
@@ -93,6 +93,8 @@ def _load():
             getattr(lib, fn).restype = ctypes.c_int
         lib.kda_device_status.argtypes = [P]
         lib.kda_device_status.restype = ctypes.c_int
+        lib.kda_chunk_prepass_hits.argtypes = [P, ctypes.POINTER(ctypes.c_uint64)]
+        lib.kda_chunk_prepass_hits.restype = ctypes.c_int
         lib.kda_set_wait_limit.argtypes = [ctypes.c_int64]
         lib.kda_set_wait_limit.restype = ctypes.c_int
         lib.kda_last_error.restype = ctypes.c_char_p
@@ -118,6 +120,15 @@ def device_status(stream=None):
     (those outputs hold NaN).  Clears the device's counters."""
     st = ctypes.c_void_p((stream or torch.cuda.current_stream()).cuda_stream)
     _check(_load().kda_device_status(st))
+
+
+def prepass_hits(stream=None) -> int:
+    """Chunks of the concurrent prefill form that took their grams and UT transform from the
+    pre-pass since the last call (synchronises the stream; clears the device's counter)."""
+    st = ctypes.c_void_p((stream or torch.cuda.current_stream()).cuda_stream)
+    n = ctypes.c_uint64(0)
+    _check(_load().kda_chunk_prepass_hits(st, ctypes.byref(n)))
+    return int(n.value)
 
 
 def set_wait_limit(polls):
@@ -201,11 +212,13 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, scale=None, chunk=64, use
     Returns (o, final_state) or, with ``gate``/``norm_w``, (o, final_state, y) where
     y [B,T,H*V] is the sigmoid-gated RMSNorm of o (o is None when return_o=False).
     Preallocated outputs may be passed as o / y / final_state (final_state may be
-    initial_state itself for an in-place update).  ``workspace``: None (the default: the
-    fused one-kernel tensor-core form, the faster one on every measured workload), a uint8
-    device tensor of at least workspace_size(...) bytes, or "auto" (a per-device buffer this
-    binding keeps); either of the last two selects the split form (a state-independent
-    pre-pass over all chunks and heads, then the per-head chain kernel).  The kept buffer is
+    initial_state itself for an in-place update).  ``workspace``: None (the fused one-kernel
+    tensor-core form), a uint8 device tensor of at least workspace_size(...) bytes, or
+    "auto" (a per-device buffer this binding keeps).  With a workspace the fused kernel is
+    joined by a pre-pass on the SMs it leaves idle (fewer (sequence, head) units than SMs),
+    which forms chunks' grams and UT transform ahead of it (the concurrent form); with
+    ``mode="split"`` the pre-pass instead forms every chunk's first and a per-head chain
+    kernel follows (the split form).  Every form gives the same bits.  The kept buffer is
     shared by every "auto" call on a device: calls on streams that may run at the same time
     need workspaces of their own."""
     return _chunk(q, k, v, (g, beta), None, initial_state, scale, chunk, use_qk_l2norm, cu_seqlens,

@@ -263,11 +263,13 @@ kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *
     if (s != KDA_OK) return s;
     KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, KDA_ERR_UNSUPPORTED, "%s: chunk=%d (supported: 16, 32, 64)",
                 fn, chunk);
-    KDA_REQUIRE(mode == KDA_MODE_AUTO || mode == KDA_MODE_TENSOR || mode == KDA_MODE_FP32, KDA_ERR_INVALID_ARG,
-                "%s: unknown mode %d", fn, mode);
+    KDA_REQUIRE(mode == KDA_MODE_AUTO || mode == KDA_MODE_TENSOR || mode == KDA_MODE_FP32 || mode == KDA_MODE_SPLIT,
+                KDA_ERR_INVALID_ARG, "%s: unknown mode %d", fn, mode);
     const bool tc_ok = kda::chunk_tc_supported(K, V, chunk) && qkv_dtype == KDA_BF16;
-    KDA_REQUIRE(mode != KDA_MODE_TENSOR || tc_ok, KDA_ERR_UNSUPPORTED,
+    KDA_REQUIRE((mode != KDA_MODE_TENSOR && mode != KDA_MODE_SPLIT) || tc_ok, KDA_ERR_UNSUPPORTED,
                 "%s: the tensor path needs bf16 q/k/v, K = V = 128 and chunk = 64", fn);
+    KDA_REQUIRE(mode != KDA_MODE_SPLIT || workspace, KDA_ERR_INVALID_ARG,
+                "%s: the split form needs a workspace (kda_chunk_workspace_size)", fn);
     cudaStream_t st = (cudaStream_t)stream;
     // an empty prompt only hands the state through: the fp32 path does that without a tensor map
     const bool use_tc = tc_ok && mode != KDA_MODE_FP32 && T > 0;
@@ -298,6 +300,7 @@ kda_status chunk_impl(const char *fn, const void *q, const void *k, const void *
             for (const Span &x : all)
                 KDA_REQUIRE(!overlaps(ws, x), KDA_ERR_INVALID_ARG, "%s: the workspace must not overlap %s", fn, x.name);
         }
+        if (mode != KDA_MODE_SPLIT) return kda::launch_chunk_concurrent(p, workspace, st);
         s = kda::launch_chunk_prep(p, workspace, st);
         if (s != KDA_OK) return s;
         return kda::launch_chunk_chain(p, workspace, st);
@@ -492,6 +495,15 @@ kda_status kda_device_status(void *stream) {
                   n_tc, n_dec, n_conv, n_proj);
         return KDA_ERR_TIMEOUT;
     }
+    return KDA_OK;
+}
+
+kda_status kda_chunk_prepass_hits(void *stream, uint64_t *chunks) {
+    kda::g_err[0] = 0;
+    KDA_REQUIRE(chunks, KDA_ERR_INVALID_ARG, "kda_chunk_prepass_hits: chunks must not be NULL");
+    const long long n = kda::take_chunk_blob_chunks((cudaStream_t)stream);
+    if (n < 0) return KDA_ERR_CUDA;
+    *chunks = (uint64_t)n;
     return KDA_OK;
 }
 

@@ -43,6 +43,43 @@ __host__ __device__ __forceinline__ int64_t blob_slot(int64_t bos, int n, int c)
 
 __host__ __device__ __forceinline__ int64_t blob_slots(int64_t rows, int N) { return (rows + C - 1) / C + N; }
 
+// Workspace layout: the blobs, then (256-byte aligned) one ready flag per blob and one
+// progress word per (sequence, head).  The split form uses the blobs only; the concurrent
+// form also the flags (set by the pre-pass once a blob is complete) and the progress
+// words (how many chunks each fused CTA has begun), both zeroed before each call.
+struct WorkspaceLayout {
+    size_t flags, progress, bytes;
+    __host__ __device__ WorkspaceLayout(int64_t rows, int N, int H) {
+        const size_t blobs = (size_t)blob_slots(rows, N) * H;
+        flags = blobs * kBlobBytes;
+        progress = flags + ((blobs * 4 + 255) & ~(size_t)255);
+        bytes = progress + (((size_t)N * H * 4 + 255) & ~(size_t)255);
+    }
+};
+
+// Global-memory accesses of the concurrent form's flags and progress words (GPU scope).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's global accesses across the generic and the asynchronous proxy
+// (bulk copies): a blob written by bulk stores before its flag, read by bulk loads after.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

@@ -57,8 +57,8 @@ constexpr uint32_t PF_RQ = 64;             // q scale per token (norm * scale) [
 constexpr uint32_t PF_RK = 128;            // k norm per token [64]
 constexpr uint32_t PF_TOT = 192;           // decay totals of the 16 groups of 4 tokens [16][128]
 constexpr uint32_t PF_END = PF_TOT + 2048;
-constexpr uint32_t P_BARS = P_SMALL + PF_END * 4;  // 3 mbarriers + tmem slot
-constexpr uint32_t PREP_SMEM = P_BARS + 32 + 1024;
+constexpr uint32_t P_BARS = P_SMALL + PF_END * 4;  // 3 mbarriers, tmem slot, the next item's index
+constexpr uint32_t PREP_SMEM = P_BARS + 48 + 1024;
 // fallback (decay range too wide): exact G in the Km tile, P in fp32 where T goes
 constexpr uint32_t P_FB_G = P_KM;
 
@@ -73,6 +73,12 @@ struct PrepArgs {
     SeqParams p;
     uint8_t *ws;      // workspace: n_slots x H blobs of kBlobBytes
     int64_t n_slots;  // blob_slots(rows, N)
+    // concurrent form (null: split form): a blob's flag is set once its stores are complete;
+    // an item is skipped while its (sequence, head)'s fused CTA has begun (progress) within
+    // `lead` chunks of it, since that CTA decides for itself before the blob could be ready
+    uint32_t *flags;
+    const uint32_t *progress;
+    int lead;
 };
 
 // Sequence n and chunk c of slot `slot`; false for a slot no chunk uses.  Slot starts
@@ -118,6 +124,19 @@ __device__ __forceinline__ Item next_item(const SeqParams &p, int64_t idx, int64
     it.idx = n_items;
     it.n = it.c = it.h = it.bos = it.cn = 0;
     return it;
+}
+
+// The index of the next item to run, at or after idx: next_item's choice, then, in the
+// concurrent form, past every item whose fused CTA is already close to it (thread 0 only:
+// the progress words change under it, so the CTA takes this one thread's choice).
+__device__ __forceinline__ int64_t choose_item(const PrepArgs &a, int64_t idx, int64_t step, int64_t n_items) {
+    for (;;) {
+        const Item it = next_item(a.p, idx, step, n_items);
+        if (it.idx >= n_items || !a.progress) return it.idx;
+        const uint32_t begun = ld_relaxed_gpu(a.progress + (size_t)it.n * a.p.H + it.h);
+        if ((int64_t)begun + a.lead <= it.c) return it.idx;
+        idx = it.idx + step;
+    }
 }
 
 // One item's q and k for this thread's 8 tokens x 4 key channels, and beta (or its logit's
@@ -198,22 +217,19 @@ __global__ void __launch_bounds__(kPT, 2)
     uint64_t *g_bar = gram_bar + 1;                                   // g tile of an item
     uint64_t *drain_bar = gram_bar + 2;                               // drain after a failure
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + P_BARS + 24);
+    volatile int64_t *next_idx = reinterpret_cast<volatile int64_t *>(sm + P_BARS + 32);  // thread 0's choice
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, l4 = lane * 4;
     const int H = p.H;
     const int64_t n_items = a.n_slots * H, step = gridDim.x;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-    Item cur = next_item(p, blockIdx.x, step, n_items);
-    uint2 q[8], k[8];
-    float beta_r = 0.f;
-    load_item<GL>(p, cur, q, k, beta_r, warp, lane);
-
     if (tid == 0) {
         mbar_init(gram_bar, 1);
         mbar_init(g_bar, 1);
         mbar_init(drain_bar, 1);
         fence_mbar_init();
+        *next_idx = choose_item(a, blockIdx.x, step, n_items);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);
@@ -223,6 +239,10 @@ __global__ void __launch_bounds__(kPT, 2)
     __syncthreads();
     fence_after_sync();
     const uint32_t tb = *tmem_slot;
+    Item cur = next_item(p, *next_idx, step, n_items);
+    uint2 q[8], k[8];
+    float beta_r = 0.f;
+    load_item<GL>(p, cur, q, k, beta_r, warp, lane);
 
     const uint32_t g_bytes = (GL && p.g_logits_bf16) ? C * DK * 2 : C * DK * 4;
     auto issue_g = [&](const Item &it) {
@@ -231,6 +251,15 @@ __global__ void __launch_bounds__(kPT, 2)
     };
     uint32_t g_issued = 0, g_seen = 0;  // thread 0: g tiles issued, and seen complete
     bool stores_pending = false;         // thread 0: blob stores not yet known to have read the staging
+    int64_t flag_pending = -1;           // thread 0: the flag of the blob those stores write
+    // thread 0: once the pending stores have completed, the blob's flag (concurrent form)
+    auto publish = [&]() {
+        if (flag_pending >= 0) {
+            fence_proxy_async_global();
+            st_release_gpu(a.flags + flag_pending, 1u);
+            flag_pending = -1;
+        }
+    };
     if (tid == 0 && cur.idx < n_items) {
         issue_g(cur);
         ++g_issued;
@@ -338,9 +367,15 @@ __global__ void __launch_bounds__(kPT, 2)
             *reinterpret_cast<float4 *>(fs + PF_TOT + (2 * warp + half) * 128 + l4) = make_float4(t01.x, t01.y, t23.x, t23.y);
         }
         // the previous item's blob stores must have read the staging before the tiles below
-        // overwrite it
+        // overwrite it; in the concurrent form they must also be complete, and the blob's
+        // flag is set
         if (tid == 0 && stores_pending) {
-            bulk_wait_read_all();
+            if (a.flags) {
+                bulk_wait_all();
+                publish();
+            } else {
+                bulk_wait_read_all();
+            }
             stores_pending = false;
         }
         __syncthreads();
@@ -410,6 +445,7 @@ __global__ void __launch_bounds__(kPT, 2)
         }
         fence_async_smem();
         fence_before_sync();
+        if (tid == 0) *next_idx = choose_item(a, cur.idx + step, step, n_items);
         const int fallback = __syncthreads_or(oor);
 
         // ---- gram [-Kd;Qd] [Km_hi;Km_lo]^T (+ lo x hi) on the tensor cores
@@ -434,7 +470,7 @@ __global__ void __launch_bounds__(kPT, 2)
         }
         __syncwarp();
         // the next item's q, k and beta while the gram runs
-        const Item nxt = next_item(p, cur.idx + step, step, n_items);
+        const Item nxt = next_item(p, *next_idx, step, n_items);
         load_item<GL>(p, nxt, q, k, beta_r, warp, lane);
         if (!mbar_wait(gram_bar, par, kPolls)) failed = 1;
         fence_after_sync();
@@ -619,12 +655,16 @@ __global__ void __launch_bounds__(kPT, 2)
             bulk_store(blob + 16384, sb + P_PIMG, 16384);
             bulk_commit();
             stores_pending = true;
+            flag_pending = (int64_t)blob_slot(cur.bos, cur.n, cur.c) * H + h;
         }
         cur = nxt;
         ++n_done;
     }
 
-    if (tid == 0 && stores_pending) bulk_wait_all();
+    if (tid == 0 && stores_pending) {  // (issued after the CTA's last failure check passed)
+        bulk_wait_all();
+        if (a.flags) publish();
+    }
     if (__syncthreads_or(failed)) {
         // drain what is in flight, then poison the blobs of this item and of every later item
         // of this CTA: NaN there reaches o, y and the state through the chain kernel
@@ -661,9 +701,24 @@ int take_chunk_prep_timeouts(cudaStream_t st) {
     return n;
 }
 
-size_t chunk_workspace_bytes(int64_t rows, int N, int H) { return (size_t)blob_slots(rows, N) * H * kBlobBytes; }
+size_t chunk_workspace_bytes(int64_t rows, int N, int H) { return WorkspaceLayout(rows, N, H).bytes; }
 
-kda_status launch_chunk_prep(const SeqParams &p, void *ws, cudaStream_t st) {
+kda_status configure_chunk_prep() {
+    static DeviceOnce configured;
+    const int dev = current_device();
+    if (configured.done(dev)) return KDA_OK;
+    for (void *fn : {(void *)chunk_prep_kernel<false>, (void *)chunk_prep_kernel<true>}) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+        if (e != cudaSuccess) {
+            set_error("chunk_prep: cannot reserve %u bytes of shared memory: %s", PREP_SMEM, cudaGetErrorString(e));
+            return KDA_ERR_CUDA;
+        }
+    }
+    configured.set(dev);
+    return KDA_OK;
+}
+
+kda_status launch_chunk_prep(const SeqParams &p, void *ws, cudaStream_t st, const PrepConcurrent *cc) {
     const int64_t rows = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
     const int64_t n_slots = blob_slots(rows, p.N);
     const int64_t n_items = n_slots * p.H;
@@ -689,24 +744,20 @@ kda_status launch_chunk_prep(const SeqParams &p, void *ws, cudaStream_t st) {
         set_error("chunk_prep: cuTensorMapEncodeTiled failed for g (%d)", (int)cres);
         return KDA_ERR_CUDA;
     }
-    static DeviceOnce configured;
-    const int dev = current_device();
-    if (!configured.done(dev)) {
-        for (void *fn : {(void *)chunk_prep_kernel<false>, (void *)chunk_prep_kernel<true>}) {
-            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
-            if (e != cudaSuccess) {
-                set_error("chunk_prep: cannot reserve %u bytes of shared memory: %s", PREP_SMEM, cudaGetErrorString(e));
-                return KDA_ERR_CUDA;
-            }
-        }
-        configured.set(dev);
-    }
+    const kda_status cs = configure_chunk_prep();
+    if (cs != KDA_OK) return cs;
     PrepArgs a;
     memset(&a, 0, sizeof(a));
     a.p = p;
     a.ws = static_cast<uint8_t *>(ws);
     a.n_slots = n_slots;
-    const int64_t cap = 2 * (int64_t)sm_count();
+    if (cc) {
+        const WorkspaceLayout L(rows, p.N, p.H);
+        a.flags = reinterpret_cast<uint32_t *>(a.ws + L.flags);
+        a.progress = reinterpret_cast<const uint32_t *>(a.ws + L.progress);
+        a.lead = cc->lead;
+    }
+    const int64_t cap = cc ? (int64_t)cc->grid : 2 * (int64_t)sm_count();
     const int grid = (int)(n_items < cap ? n_items : cap);
     if (p.g_logits)
         chunk_prep_kernel<true><<<grid, kPT, PREP_SMEM, st>>>(tmap_g, a);

@@ -93,9 +93,10 @@ constexpr uint32_t F_BETA0 = 576; // beta of tokens 0-3 (warp 0 prepares them wh
 constexpr uint32_t F_SCAN0 = 580; // decay totals of tokens 0-3 [128]
 constexpr uint32_t F_AH = 708;    // gates from logits: exp(A_log) of the head [1 of 4]
 constexpr uint32_t F_DB = 712;    // gates from logits: dt_bias of the head's channels [128]
-constexpr uint32_t F_END = 840;
-constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 8 mbarriers + tmem slot
-constexpr uint32_t SMEM_BYTES = S_BARS + 80 + 1024;  // + alignment slack
+constexpr uint32_t F_BLOB = 840;  // concurrent form: this chunk's blob is ready (thread 0 -> all)
+constexpr uint32_t F_END = 844;
+constexpr uint32_t S_BARS = S_SMALL + F_END * 4;     // 8 mbarriers, tmem slot, gate and blob mbarriers
+constexpr uint32_t SMEM_BYTES = S_BARS + 96 + 1024;  // + alignment slack
 // scan scratch aliases T (free during prep): [16 warps][128] floats of decay totals, then
 // their exclusive prefixes [16][128] and the chunk total [128]
 constexpr uint32_t S_SCAN = S_T;
@@ -108,11 +109,18 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // Set by a CTA whose bounded wait on the tensor core or the TMA gave up; that CTA
 // also writes NaN into its final state, o and y so the failure cannot pass unnoticed.
 __device__ int g_chunk_tc_timeouts = 0;
+// Chunks whose T diag(beta) and P came from the concurrent pre-pass (a diagnostic).
+__device__ unsigned long long g_chunk_tc_blob_chunks = 0;
 
 struct TcParams {
     SeqParams p;
     int order_n;            // > 0: blockIdx -> sequence through order[]
     int order[64];
+    // concurrent form (null: none): the pre-pass's blobs, their ready flags, and this
+    // kernel's progress words (chunks begun per (sequence, head)), in one workspace
+    const uint8_t *ws;
+    const uint32_t *flags;
+    uint32_t *progress;
 };
 
 
@@ -237,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *gt_bar = bar_g + 6;                                   // g tile
     uint64_t *pre_bar = bar_g + 7;                                  // decay prefix written (128 arrivals)
     uint64_t *gate_bar = reinterpret_cast<uint64_t *>(sm + S_BARS + 72);  // fused norm: gate tile
+    uint64_t *blob_bar = reinterpret_cast<uint64_t *>(sm + S_BARS + 80);  // concurrent form: a chunk's blob
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S_BARS + 64);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -260,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 7; ++b) mbar_init(bar_g + b, 1);
         mbar_init(pre_bar, 128);
         if (NORM) mbar_init(gate_bar, 1);
+        mbar_init(blob_bar, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -304,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sb + S_KM, &tmap_g, gt_bar, 0, h, bos + chunk * C);
     };
     int g_pending = -1;  // chunk whose g tile is in flight (thread 0 only)
+    int b_pending = -1;  // blob copy in flight (thread 0 only): the phase of blob_bar it completes
+    uint32_t n_blobs = 0;  // blob copies issued (thread 0 only)
     int failed = 0;      // a bounded wait gave up
     if (tid == 0 && nchunks > 0) {
         issue_v(0);
@@ -568,13 +580,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cn = min(C, len - t0);
         fence_async_smem();
         fence_before_sync();  // the previous state pass (or the initial state) wrote TMEM
+        // concurrent form: has the pre-pass already formed this chunk's T diag(beta) and P?
+        // (read once, never waited for: otherwise this CTA forms them itself, as always)
+        size_t blob_idx = 0;
+        if (tp.flags) {
+            blob_idx = (size_t)blob_slot(bos, n, ch) * H + h;
+            if (tid == 0) {
+                st_relaxed_gpu(tp.progress + unit, (uint32_t)ch + 1u);
+                reinterpret_cast<volatile uint32_t *>(fs)[F_BLOB] = ld_acquire_gpu(tp.flags + blob_idx);
+            }
+        }
         // ---- operand tiles of this chunk and S(n-1) are ready
         const int fallback = __syncthreads_or(oor_next);
+        // a wide-decay chunk keeps its exact path (its Kg^T is formed there too)
+        const bool use_blob = tp.flags && !fallback && reinterpret_cast<volatile uint32_t *>(fs)[F_BLOB] != 0u;
 
-        // ================= gram [-Kd;Qd] [Km_hi;Km_lo]^T (+ lo x hi)
+        // ================= gram [-Kd;Qd] [Km_hi;Km_lo]^T (+ lo x hi), or the blob
         if (tid == 0) {
             fence_after_sync();
-            if (!fallback) {
+            if (use_blob) {
+                // T diag(beta) hi/lo and P hi/lo straight into their operand tiles: T diag(beta)
+                // was last read by the previous D product, P by the previous O/S product
+                fence_proxy_async_global();
+                const uint8_t *blob = tp.ws + blob_idx * kBlobBytes;
+                mbar_arrive_expect_tx(blob_bar, kBlobBytes);
+                bulk_load(sb + S_TBH, blob, 16384, blob_bar);
+                bulk_load(sb + S_PKGH, blob + 16384, 8192, blob_bar);
+                bulk_load(sb + S_PKGL, blob + 24576, 8192, blob_bar);
+                b_pending = (int)(n_blobs++ & 1);
+                atomicAdd(&g_chunk_tc_blob_chunks, 1ull);
+            } else if (!fallback) {
                 const uint32_t id128 = idesc_bf16(128, 128, false, false);
                 const uint32_t id64 = idesc_bf16(128, 64, false, false);
 #pragma unroll 1
@@ -600,7 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its tokens after the gram pass)
         if (warp > 0 && ch + 1 < nchunks) load_chunk<GL>(p, cr, bos, t0 + C, min(C, len - t0 - C), h, warp, l4);
         if (!wait_group(bar_g, par)) failed = 1;
-        if (!fallback) {
+        if (use_blob) {
+            // nothing to form: the pre-pass did the gram pass and the solve
+        } else if (!fallback) {
             uint32_t r1[16], r2[16];
             tmem_ld16(tb + lane_off + T_G + wg * 16, r1);
             tmem_ld16(tb + lane_off + T_G + 64 + wg * 16, r2);
@@ -740,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ts(tb + T_R, a, sdesc_at(sb16, (combo_b(cb) ? S_KQL : S_KQH) + koff, 16, 1024), id128, 1u);
                 }
             mma_commit(bar_r);
-        } else if (warp > 0) {
+        } else if (warp > 0 && !use_blob) {
             // ================= T = (I + A)^-1, blocked with 16 x 16 diagonal blocks (warps 1-15)
             const int ctid = tid - 32;
             if (tid >= kThreads - 64) {
@@ -822,6 +859,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ================= D^T = R^T (T diag beta)^T
         if (tid == 0) {
+            if (use_blob) {  // the blob's tiles have landed (the O/S product reads P after this too)
+                if (mbar_wait(blob_bar, (uint32_t)b_pending, kPolls))
+                    b_pending = -1;
+                else
+                    failed = 1;
+            }
             fence_after_sync();
             // R^T_hi [T diag(beta)_hi ; _lo]^T (N = 128: the two tiles are contiguous) into
             // [D_a | D_b], then R^T_lo (T diag beta)_hi^T onto D_a
@@ -1042,6 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (v_pending >= 0) mbar_wait(tma_bar, (uint32_t)(v_pending & 1), kPolls);  // V copy in flight
             if (g_pending >= 0) mbar_wait(gt_bar, (uint32_t)(g_pending & 1), kPolls);   // g copy in flight
             if (q_pending >= 0) mbar_wait(gate_bar, (uint32_t)(q_pending & 1), kPolls);  // gate copy in flight
+            if (b_pending >= 0) mbar_wait(blob_bar, (uint32_t)b_pending, kPolls);       // blob copy in flight
         }
         __syncthreads();
         mbar_wait(drain_bar, 0, kPolls);
@@ -1104,9 +1148,23 @@ int take_chunk_tc_timeouts(cudaStream_t st) {
     return n;
 }
 
+long long take_chunk_blob_chunks(cudaStream_t st) {
+    unsigned long long n = 0;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&n, g_chunk_tc_blob_chunks, sizeof(n), 0, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_chunk_tc_blob_chunks, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        set_error("chunk_tc: cannot read the blob counter: %s", cudaGetErrorString(cudaGetLastError()));
+        return -1;
+    }
+    return (long long)n;
+}
+
 bool chunk_tc_supported(int K, int V, int chunk) { return K == DK && V == DV && chunk == C; }
 
-kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaStream_t st) {
+kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaStream_t st, const void *ws) {
     if (!chunk_tc_supported(K, V, chunk)) {
         set_error("chunk_tc: needs K = V = 128 and chunk = 64");
         return KDA_ERR_UNSUPPORTED;
@@ -1199,9 +1257,82 @@ kda_status launch_chunk_tc(const SeqParams &p_in, int K, int V, int chunk, cudaS
     }
     auto kern = p_in.g_logits ? (p_in.gate ? chunk_tc_kernel<true, true> : chunk_tc_kernel<true, false>)
                               : (p_in.gate ? chunk_tc_kernel<false, true> : chunk_tc_kernel<false, false>);
-    kern<<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tmap_gate, tp);
+    if (!ws) {
+        kern<<<units, kThreads, SMEM_BYTES, st>>>(tmap, tmap_g, tmap_gate, tp);
+        note_launch();
+        return check_launch("chunk_tc_kernel");
+    }
+    // concurrent form: this kernel's CTAs must take their SMs before the pre-pass's, which
+    // is launched right after on another stream, so it runs at the highest priority
+    const WorkspaceLayout L(rows, p_in.N, p_in.H);
+    tp.ws = static_cast<const uint8_t *>(ws);
+    tp.flags = reinterpret_cast<const uint32_t *>(tp.ws + L.flags);
+    tp.progress = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(tp.ws) + L.progress);
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) {
+        cudaGetLastError();
+        greatest = 0;
+    }
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(units, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributePriority;
+    attr[0].val.priority = greatest;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmap, tmap_g, tmap_gate, tp);
     note_launch();
+    if (e != cudaSuccess) {
+        set_error("chunk_tc_kernel: %s", cudaGetErrorString(e));
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
     return check_launch("chunk_tc_kernel");
+}
+
+kda_status launch_chunk_concurrent(const SeqParams &p, void *ws, cudaStream_t st) {
+    const int units = p.N * p.H, sms = sm_count();
+    const int64_t rows = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
+    if (units >= sms || rows <= 0) return launch_chunk_tc(p, DK, DV, C, st);  // no SM would be left over
+    kda_status s = configure_chunk_prep();  // before the fused kernel is launched
+    if (s != KDA_OK) return s;
+    const WorkspaceLayout L(rows, p.N, p.H);
+    cudaStream_t side = nullptr;
+    cudaEvent_t ready = nullptr, done = nullptr;
+    auto cuda_fail = [&](const char *what, cudaError_t e) {
+        set_error("chunk (concurrent form): %s failed: %s", what, cudaGetErrorString(e));
+        cudaGetLastError();
+        s = KDA_ERR_CUDA;
+    };
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking)) != cudaSuccess) {
+        cuda_fail("creating a stream", e);
+        return s;
+    }
+    if ((e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming)) != cudaSuccess) {
+        cuda_fail("creating an event", e);
+    } else if ((e = cudaMemsetAsync(static_cast<uint8_t *>(ws) + L.flags, 0, L.bytes - L.flags, st)) != cudaSuccess) {
+        cuda_fail("clearing the flags", e);
+    } else if ((e = cudaEventRecord(ready, st)) != cudaSuccess || (e = cudaStreamWaitEvent(side, ready, 0)) != cudaSuccess) {
+        cuda_fail("ordering the streams", e);
+    } else if ((s = launch_chunk_tc(p, DK, DV, C, st, ws)) == KDA_OK) {
+        PrepConcurrent cc;
+        cc.grid = 2 * (sms - units);  // two pre-pass CTAs per idle SM
+        cc.lead = 2;
+        s = launch_chunk_prep(p, ws, side, &cc);
+        // the caller's stream covers the pre-pass too, even after a failed launch
+        if ((e = cudaEventRecord(done, side)) != cudaSuccess || (e = cudaStreamWaitEvent(st, done, 0)) != cudaSuccess)
+            cuda_fail("joining the streams", e);
+    }
+    if (ready) cudaEventDestroy(ready);
+    if (done) cudaEventDestroy(done);
+    cudaStreamDestroy(side);  // released once its work completes
+    return s;
 }
 
 }  // namespace kda

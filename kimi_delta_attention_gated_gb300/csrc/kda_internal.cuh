@@ -48,6 +48,9 @@ int take_chunk_chain_timeouts(cudaStream_t st);
 int take_oproj_timeouts(cudaStream_t st);
 int take_decode_timeouts(cudaStream_t st);
 int take_short_conv_timeouts(cudaStream_t st);
+// Chunks of the concurrent form that took the pre-pass's operands, read and cleared on
+// `st` after it has drained; -1 with the error message set when CUDA fails.
+long long take_chunk_blob_chunks(cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // parameter blocks
@@ -195,12 +198,27 @@ kda_status chunk_call(const char *fn, const void *q, const void *k, const void *
 kda_status launch_recurrent(const SeqParams &p, int K, int V, cudaStream_t st);
 kda_status launch_chunk_fp32(const SeqParams &p, int K, int V, int chunk, const int *order,
                              cudaStream_t st);
-kda_status launch_chunk_tc(const SeqParams &p, int K, int V, int chunk, cudaStream_t st);
+// ws: a workspace of chunk_workspace_bytes with zeroed flags and progress words, whose
+// blobs the pre-pass fills while this kernel runs (the concurrent form), or null.
+kda_status launch_chunk_tc(const SeqParams &p, int K, int V, int chunk, cudaStream_t st, const void *ws = nullptr);
+// The concurrent form: the fused kernel on `st` at the highest launch priority, the
+// pre-pass beside it on a stream of the call, on the SMs the fused kernel leaves idle.
+kda_status launch_chunk_concurrent(const SeqParams &p, void *ws, cudaStream_t st);
 // The split tensor-core prefill: the state-independent pre-pass writes every chunk's
 // operand images into ws (chunk_workspace_bytes long), then the chain kernel runs the
 // state through the chunks.  Both need K = V = 128, chunk = 64, bf16 q/k/v.
 size_t chunk_workspace_bytes(int64_t rows, int N, int H);
-kda_status launch_chunk_prep(const SeqParams &p, void *ws, cudaStream_t st);
+// The pre-pass alongside the fused kernel (the concurrent form): `grid` CTAs, flags set as
+// blobs complete, items skipped within `lead` chunks of their fused CTA's progress.
+struct PrepConcurrent {
+    int grid;
+    int lead;
+};
+kda_status launch_chunk_prep(const SeqParams &p, void *ws, cudaStream_t st, const PrepConcurrent *cc = nullptr);
+// The pre-pass kernels' one-time setup on the current device (this also loads them: done
+// before the fused kernel starts, so that loading cannot hold the pre-pass back until the
+// fused kernel has finished).
+kda_status configure_chunk_prep();
 kda_status launch_chunk_chain(const SeqParams &p, const void *ws, cudaStream_t st);
 kda_status launch_gated_rmsnorm(const void *o, int o_bf16, const void *gate, int gate_bf16,
                                 const float *w, float eps, void *y, int y_bf16, int64_t rows,

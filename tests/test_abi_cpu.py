@@ -124,11 +124,15 @@ def test_chunk_fwd_rejects_overlapping_buffers(lib, over, what):
 
 
 def test_workspace_size(lib):
-    """32 KiB per (chunk slot, head); ceil(rows / 64) + N slots (N = n_seqs in varlen mode)."""
+    """32 KiB per (chunk slot, head) for ceil(rows / 64) + N slots (N = n_seqs in varlen mode),
+    then a 4-byte flag per (slot, head) and a 4-byte progress word per (sequence, head), each
+    array rounded up to 256 bytes."""
     lib.kda_chunk_workspace_size.restype = ctypes.c_size_t
-    assert lib.kda_chunk_workspace_size(1, 8192, 96, 0) == (128 + 1) * 96 * 32768
-    assert lib.kda_chunk_workspace_size(2, 65536, 96, 0) == (2048 + 2) * 96 * 32768
-    assert lib.kda_chunk_workspace_size(1, 100, 3, 4) == (2 + 4) * 3 * 32768
+    r256 = lambda x: (x + 255) // 256 * 256
+    size = lambda slots, H, N: slots * H * 32768 + r256(slots * H * 4) + r256(N * H * 4)
+    assert lib.kda_chunk_workspace_size(1, 8192, 96, 0) == size(128 + 1, 96, 1)
+    assert lib.kda_chunk_workspace_size(2, 65536, 96, 0) == size(2048 + 2, 96, 2)
+    assert lib.kda_chunk_workspace_size(1, 100, 3, 4) == size(2 + 4, 3, 4)
     assert lib.kda_chunk_workspace_size(0, 64, 2, 0) == 0
 
 

@@ -1,4 +1,4 @@
-"""GPU tests of the split tensor-core prefill (a workspace given): the state-independent
+"""GPU tests of the split tensor-core prefill (mode "split", a workspace given): the state-independent
 pre-pass over every chunk and head, then the per-head chain kernel.  The two forms run the
 same products at the same split-bf16 precision; the split form accumulates the R/O product's
 hi and lo parts in separate TMEM columns and adds them afterwards, so its fp32 sums differ
@@ -27,9 +27,9 @@ def built():
 def both(d, **kw):
     """The same call through the fused form (no workspace) and the split form."""
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("initial_state"))
-    kw = dict(scale=d["scale"], chunk=64, mode="tensor", cu_seqlens=d.get("cu_seqlens"), **kw)
-    fused = kda.chunk_fwd(*args, workspace=None, **kw)
-    split = kda.chunk_fwd(*args, workspace="auto", **kw)
+    kw = dict(scale=d["scale"], chunk=64, cu_seqlens=d.get("cu_seqlens"), **kw)
+    fused = kda.chunk_fwd(*args, workspace=None, mode="tensor", **kw)
+    split = kda.chunk_fwd(*args, workspace="auto", mode="split", **kw)
     kda.device_status()
     return fused, split
 
@@ -93,9 +93,9 @@ def test_split_matches_fused_norm_without_o():
 def test_split_matches_fused_gate_logits():
     d = make_logit_inputs("prefill", device="cuda", T=300, H=3)
     args = (d["q"], d["k"], d["v"], d["g_logits"], d["beta_logits"], d["A_log"])
-    kw = dict(dt_bias=d["dt_bias"], g_lower_bound=d["g_lower_bound"], scale=d["scale"], mode="tensor")
-    fused = kda.chunk_fwd_logits(*args, workspace=None, **kw)
-    split = kda.chunk_fwd_logits(*args, workspace="auto", **kw)
+    kw = dict(dt_bias=d["dt_bias"], g_lower_bound=d["g_lower_bound"], scale=d["scale"])
+    fused = kda.chunk_fwd_logits(*args, workspace=None, mode="tensor", **kw)
+    split = kda.chunk_fwd_logits(*args, workspace="auto", mode="split", **kw)
     kda.device_status()
     assert_agrees(fused, split)
     g, beta = oracle.gates(np32(d["g_logits"]), np32(d["A_log"]), np32(d["beta_logits"]), np32(d["dt_bias"]),
@@ -143,7 +143,7 @@ def test_split_workspace_tensor_and_reuse():
                      device="cuda")
     for d in (a, b, a):
         out = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("initial_state"), scale=d["scale"],
-                            cu_seqlens=d.get("cu_seqlens"), workspace=ws, mode="tensor")
+                            cu_seqlens=d.get("cu_seqlens"), workspace=ws, mode="split")
         ref = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("initial_state"), scale=d["scale"],
                             cu_seqlens=d.get("cu_seqlens"), workspace=None, mode="tensor")
         assert_agrees(ref, out)
@@ -153,5 +153,8 @@ def test_split_workspace_tensor_and_reuse():
 def test_split_rejects_a_small_workspace():
     d = make_inputs("prefill", device="cuda", T=128, H=2)
     ws = torch.empty(kda.workspace_size(1, 128, 2) - 16, dtype=torch.uint8, device="cuda")
-    with pytest.raises(kda.KDAError):
-        kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"], workspace=ws, mode="tensor")
+    for mode in ("tensor", "split"):
+        with pytest.raises(kda.KDAError):
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"], workspace=ws, mode=mode)
+    with pytest.raises(kda.KDAError):  # the split form has nowhere to put its operands without one
+        kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"], mode="split")
