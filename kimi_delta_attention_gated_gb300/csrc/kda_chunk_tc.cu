@@ -127,6 +127,16 @@ struct TcParams {
 // barrier over warps 1-15 (the triangular solve, while warp 0 issues MMAs)
 __device__ __forceinline__ void tbar() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
 
+// barrier over the 4 warps of warpgroup wg (named barriers 2-5, one per warpgroup)
+__device__ __forceinline__ void wg_bar(int wg) {
+    switch (wg) {
+        case 0: asm volatile("bar.sync 2, 128;" ::: "memory"); break;
+        case 1: asm volatile("bar.sync 3, 128;" ::: "memory"); break;
+        case 2: asm volatile("bar.sync 4, 128;" ::: "memory"); break;
+        default: asm volatile("bar.sync 5, 128;" ::: "memory"); break;
+    }
+}
+
 
 
 
@@ -1006,8 +1016,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(lane & 1)) red[(wg * 4 + wq) * 16 + ((lane >> 1) & 15)] = e;
                 const float w = __ldg(p.norm_w + v);
                 // sigmoid of the gates before the barrier, where the warps wait for the last
-                // one, with the correctly rounded reciprocal (the value 1 / x has).  A bf16
-                // gate comes from the tile in shared memory; an fp32 one from global memory
+                // one (a fast reciprocal: 2 ulp).  A bf16 gate comes from the tile in shared
+                // memory; an fp32 one from global memory
                 float sg[16];
                 if (p.gate_bf16) {
                     if (!mbar_wait(gate_bar, (uint32_t)(ch & 1), kPolls))
@@ -1017,14 +1027,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint16_t *gs = reinterpret_cast<const uint16_t *>(sm + S_A) + i0 * DV + v;
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        sg[c] = __frcp_rn(1.0f + __expf(-__uint_as_float((uint32_t)gs[c * DV] << 16)));
+                        sg[c] = __fdividef(1.0f, 1.0f + __expf(-__uint_as_float((uint32_t)gs[c * DV] << 16)));
                 } else {
                     const float *gp = reinterpret_cast<const float *>(p.gate) + ((size_t)(bos + t0) * H + h) * DV + v;
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        sg[c] = __frcp_rn(1.0f + __expf(-__ldg(gp + (size_t)min(i0 + c, cn - 1) * H * DV)));
+                        sg[c] = __fdividef(1.0f, 1.0f + __expf(-__ldg(gp + (size_t)min(i0 + c, cn - 1) * H * DV)));
                 }
-                __syncthreads();
+                // a row's statistics come from the 4 warps of its warpgroup only: the other
+                // warpgroups need not wait for warp 0, the tensor-core issuer and last here
+                wg_bar(wg);
                 // lane l forms 1 / rms of row l % 16 once; the others take it by shuffle
                 const int cl = lane & 15;
                 const float ssl = red[(wg * 4 + 0) * 16 + cl] + red[(wg * 4 + 1) * 16 + cl] +
