@@ -490,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     red[(hf * 4 + q4) * 32 + lane] = e;
                     const float w = __ldg(p.norm_w + v);
-                    // sigmoid of the gates before the barrier, with the correctly rounded
-                    // reciprocal.  A bf16 gate comes from its tile, an fp32 one from global memory
+                    // sigmoid of the gates before the barrier, with the fast reciprocal (2 ulp).
+                    // A bf16 gate comes from its tile, an fp32 one from global memory
                     float sg[32];
                     if (p.gate_bf16) {
                         if (!mbar_wait(gate_bar, (uint32_t)par, kPolls))
@@ -501,12 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint16_t *gs = reinterpret_cast<const uint16_t *>(sm + S_GATE) + i0 * DV + v;
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            sg[c] = __frcp_rn(1.0f + __expf(-__uint_as_float((uint32_t)gs[c * DV] << 16)));
+                            sg[c] = __fdividef(1.0f, 1.0f + __expf(-__uint_as_float((uint32_t)gs[c * DV] << 16)));
                     } else {
                         const float *gp = reinterpret_cast<const float *>(p.gate) + ((size_t)(bos + t0) * H + h) * DV + v;
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            sg[c] = __frcp_rn(1.0f + __expf(-__ldg(gp + (size_t)min(i0 + c, cn - 1) * H * DV)));
+                            sg[c] = __fdividef(1.0f, 1.0f + __expf(-__ldg(gp + (size_t)min(i0 + c, cn - 1) * H * DV)));
                     }
                     group_sync_or<1, kGroup>(0);
                     // lane j forms 1 / rms of row j once; the others take it by shuffle

@@ -119,7 +119,8 @@ __device__ __forceinline__ void st_out(void *base, size_t idx, float x, int is_b
         reinterpret_cast<float *>(base)[idx] = x;
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// sigmoid with the fast exponential and the fast reciprocal (a few ulp)
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // log(1 + t) for t in [0, 1] with full relative accuracy at small t (the decay logits sit
 // near -4, where log(1 + t) formed from a rounded 1 + t and the fast logarithm loses up to
