@@ -577,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's tensor-core waits)
     int oor_next = 0;
     float kgv[4][4];  // the next chunk's Kg, stored while that chunk's gram runs
+    const float norm_wv = NORM ? __ldg(p.norm_w + m) : 0.f;  // the norm weight of this thread's value channel
     if (nchunks > 0) {
         prep_norms(cr, min(C, len), 0);
         beta0_publish();
@@ -1014,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float e = (u2 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, u2 ? a2[0] : a2[1], 2);
                 e += __shfl_xor_sync(0xffffffffu, e, 1);
                 if (!(lane & 1)) red[(wg * 4 + wq) * 16 + ((lane >> 1) & 15)] = e;
-                const float w = __ldg(p.norm_w + v);
+                const float w = norm_wv;
                 // sigmoid of the gates before the barrier, where the warps wait for the last
                 // one (a fast reciprocal: 2 ulp).  A bf16 gate comes from the tile in shared
                 // memory; an fp32 one from global memory
