@@ -78,12 +78,12 @@ MEASURED_TRAFFIC = {
                     "capture": "ncu, decode B=64 H=96, short convolutions fused"},
     # full-size captures: mean of two launches per (token, channel) element
     "conv_prefill": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
-                     "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
-                     "bytes_per_unit": 1179.379712e6 / (8192 * 36864),
+                     "sha256": "5455c4ca65aa3564cc58dfe31e882936cc835e7c78b214ec91bc918376e0107f",
+                     "bytes_per_unit": 1180.691584e6 / (8192 * 36864),
                      "capture": "ncu, full size"},
     "conv_decode": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_short_conv.cu",
-                    "sha256": "86ee6af4e0d2d7215c44733b822895a89e8668c38dc3b160bacb763bc5223948",
-                    "bytes_per_unit": 204.395008e6 / (256 * 36864),
+                    "sha256": "5455c4ca65aa3564cc58dfe31e882936cc835e7c78b214ec91bc918376e0107f",
+                    "bytes_per_unit": 204.401152e6 / (256 * 36864),
                     "capture": "ncu, full size"},
 }
 
