@@ -419,16 +419,23 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// NSUB = 1: a 256-feature x 256-row tile.  NSUB = 2 (long prompts): 256 features x 512
+// rows, two N = 256 products per K step on the same w_o slice, so an SM takes 48 KB per
+// 8 products instead of 32 KB per 4: 42 instead of 56 bytes per cycle of tensor work at
+// the bf16 rate, and the same bytes in flight (4 stages instead of 6) cover a third more
+// load latency.  Its 512 TMEM columns hold one accumulator, so a tile's epilogue no
+// longer overlaps the next tile's products.
+template <int NSUB>
 struct PairCfg {
-    static constexpr int BN = 256;                     // rows of y per tile (128 staged per CTA)
-    static constexpr int STAGES = 6;
+    static constexpr int BN = 256 * NSUB;              // rows of y per tile (128 of each 256 staged per CTA)
+    static constexpr int STAGES = NSUB == 1 ? 6 : 4;
     static constexpr uint32_t A_BYTES = 128 * BK * 2;  // this CTA's 128 w_o rows
-    static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's 128 y rows
-    static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+    static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's 128 y rows of each 256-row sub-tile
+    static constexpr uint32_t STAGE = A_BYTES + NSUB * B_BYTES;
     static constexpr uint32_t BARS = STAGES * STAGE;   // full[S], empty[S], acc_full[2], acc_empty[2], drain
     static constexpr uint32_t SMEM = BARS + (2 * STAGES + 5) * 8 + 16 + 1024;
 };
-static_assert(PairCfg::SMEM <= 232448, "shared memory budget");
+static_assert(PairCfg<1>::SMEM <= 232448 && PairCfg<2>::SMEM <= 232448, "shared memory budget");
 
 // Tile id -> (256-feature tile, 256-row tile): groups of 14 feature tiles (3584 features)
 // across every row tile, so the pairs running together share w_o and y through L2.  At
@@ -445,13 +452,14 @@ __device__ __forceinline__ void pair_tile_coords(int id, int n_ft, int n_tt, int
     t = r / gsz;
 }
 
-template <int SPLIT>
+template <int SPLIT, int NSUB>
 __global__ void __launch_bounds__(kWarps * 32, 1)
     oproj_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ GemmArgs a) {
-    using L = PairCfg;
+    static_assert(SPLIT == 1 || NSUB == 1, "the split-K form runs 256-row tiles");
+    using L = PairCfg<NSUB>;
     constexpr int BN = L::BN;
-    constexpr uint32_t NACC = SPLIT == 1 ? 2 : 1;  // accumulator buffers (256 TMEM columns each)
+    constexpr uint32_t NACC = SPLIT == 1 && NSUB == 1 ? 2 : 1;  // accumulator buffers (BN TMEM columns each)
     constexpr uint32_t TMEM_COLS = NACC * BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -517,8 +525,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                     }
                     if (pr == 0) mbar_arrive_expect_tx(full + s, 2 * L::STAGE);  // both CTAs' bytes
                     tma_load_2d_pair(sb + s * L::STAGE, &tmap_w, full_leader + s * 8, kb * BK, f * 256 + (int)pr * 128);
-                    tma_load_2d_pair(sb + s * L::STAGE + L::A_BYTES, &tmap_y, full_leader + s * 8, kb * BK,
-                                     t * BN + (int)pr * 128);
+#pragma unroll
+                    for (int u = 0; u < NSUB; ++u)  // rows past M (or a whole sub-tile) arrive as zeros
+                        tma_load_2d_pair(sb + s * L::STAGE + L::A_BYTES + u * L::B_BYTES, &tmap_y, full_leader + s * 8,
+                                         kb * BK, t * BN + u * 256 + (int)pr * 128);
                 }
             }
             // the loads issued have landed once the products that read them have completed
@@ -530,7 +540,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && pr == 0) {  // ---- MMA issuer (even CTA)
-            const uint32_t idesc = idesc_bf16(256, BN, false, false);
+            const uint32_t idesc = idesc_bf16(256, 256, false, false);
             uint32_t it = 0, tc = 0;
             for (int id = pair_id; id < a.n_tiles && !failed; id += pair_stride, ++tc) {
                 const uint32_t acc = tc % NACC, use = tc / NACC;
@@ -552,8 +562,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                     const uint32_t sa = s * L::STAGE, sbb = sa + L::A_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        mma_pair_ss(d, sdesc_at(sb16, sa + k * 32, 16, 1024), sdesc_at(sb16, sbb + k * 32, 16, 1024),
-                                    idesc, (kb > kb0 || k) ? 1u : 0u);
+#pragma unroll
+                        for (int u = 0; u < NSUB; ++u)  // sub-tile u: rows u * 256.. in TMEM columns u * 256..
+                            mma_pair_ss(d + u * 256, sdesc_at(sb16, sa + k * 32, 16, 1024),
+                                        sdesc_at(sb16, sbb + u * L::B_BYTES + k * 32, 16, 1024), idesc,
+                                        (kb > kb0 || k) ? 1u : 0u);
                     mma_pair_commit(empty + s, pair_mask);  // both CTAs' stage s is free once these complete
                 }
                 if (failed) break;
@@ -744,11 +757,14 @@ kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, 
         // the pair form: 256-feature tiles on CTA pairs; a decode batch splits K over two pairs
         static DeviceOnce configured_pair;
         if (!configured_pair.done(dev)) {
-            cudaError_t e = cudaFuncSetAttribute(oproj_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 PairCfg::SMEM);
+            cudaError_t e = cudaFuncSetAttribute(oproj_pair_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 PairCfg<1>::SMEM);
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(oproj_pair_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PairCfg::SMEM);
+                e = cudaFuncSetAttribute(oproj_pair_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairCfg<2>::SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(oproj_pair_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairCfg<1>::SMEM);
             if (e != cudaSuccess) {
                 set_error("o_proj: cannot reserve shared memory: %s", cudaGetErrorString(e));
                 return KDA_ERR_CUDA;
@@ -770,6 +786,9 @@ kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, 
         }
         const int n_ft2 = N / 256;
         const bool split = M <= 256 && (K / BK) % 2 == 0 && 4 * n_ft2 <= sms;
+        // 512-row tiles where they still give every pair at least one tile
+        const bool wide = !split && (int64_t)n_ft2 * ((M + 511) / 512) >= sms / 2;
+        const int tile_rows = wide ? 512 : 256;
         GemmArgs ga;
         memset(&ga, 0, sizeof(ga));
         ga.out = out;
@@ -778,14 +797,14 @@ kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, 
         ga.N = N;
         ga.K = K;
         ga.n_ft = n_ft2;
-        ga.n_tt = split ? 1 : (int)((M + 255) / 256);
+        ga.n_tt = split ? 1 : (int)((M + tile_rows - 1) / tile_rows);
         ga.n_tiles = ga.n_ft * ga.n_tt;
         const int pairs = ga.n_tiles < sms / 2 ? ga.n_tiles : sms / 2;
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(split ? 4 * n_ft2 : 2 * pairs, 1, 1);
         cfg.blockDim = dim3(kWarps * 32, 1, 1);
-        cfg.dynamicSmemBytes = PairCfg::SMEM;
+        cfg.dynamicSmemBytes = wide ? PairCfg<2>::SMEM : PairCfg<1>::SMEM;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -794,8 +813,9 @@ kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, 
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = split ? cudaLaunchKernelEx(&cfg, oproj_pair_kernel<2>, tw, ty128, ga)
-                                    : cudaLaunchKernelEx(&cfg, oproj_pair_kernel<1>, tw, ty128, ga);
+        const cudaError_t e = split  ? cudaLaunchKernelEx(&cfg, oproj_pair_kernel<2, 1>, tw, ty128, ga)
+                              : wide ? cudaLaunchKernelEx(&cfg, oproj_pair_kernel<1, 2>, tw, ty128, ga)
+                                     : cudaLaunchKernelEx(&cfg, oproj_pair_kernel<1, 1>, tw, ty128, ga);
         note_launch();
         if (e != cudaSuccess) {
             set_error("oproj_pair_kernel: %s", cudaGetErrorString(e));

@@ -31,13 +31,15 @@ def _check(out, ref, out_dtype):
 
 
 @pytest.mark.parametrize("rows,K,N", [(1, 512, 1024), (129, 512, 1024), (300, 256, 640), (5, 576, 512),
-                                      (700, 256, 7168)])  # the last one fills the GPU: 256-row tiles
+                                      (700, 256, 7168),  # 256-row tiles, several per pair
+                                      (1100, 256, 7168),  # 512-row tiles, the last one's upper half empty
+                                      (1500, 256, 7168)])  # 512-row tiles, the last one ending in its upper half
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_tile_edges(rows, K, N, out_dtype):
     """Row counts that end inside a token tile: the pair kernels (out_features a multiple of
     256; K split over two pairs for at most 256 rows and an even count of 64-wide K slices,
-    else the persistent form, here with several tiles per pair at 700 rows) and the
-    single-CTA kernel (640 features)."""
+    else the persistent form: 256-row tiles at 700 rows, 512-row tiles once every pair still
+    gets one, at 1100 and 1500 rows) and the single-CTA kernel (640 features)."""
     y, w = _data(rows, K, N, rows)
     out = kda.o_proj(y, w, out_dtype=out_dtype)
     torch.cuda.synchronize()
