@@ -517,7 +517,9 @@ def bench_o_proj(args, world, peaks):
     g = torch.Generator(device="cuda")
     g.manual_seed(7)
     w = (torch.randn((N, K), generator=g, device="cuda") * K ** -0.5).to(torch.bfloat16)
-    for name, rows in (("decode", 256), ("prefill", 8192)):
+    legs = (("decode", 256), ("prefill", 8192)) if not args.oproj_rows else \
+        (("decode" if args.oproj_rows <= 256 else "prefill", args.oproj_rows),)
+    for name, rows in legs:
         y = torch.randn((rows, K), generator=g, device="cuda").to(torch.bfloat16)
         o = torch.empty((rows, N), device="cuda", dtype=torch.bfloat16)
         fn = lambda: kda.o_proj(y, w, out=o)
@@ -660,6 +662,8 @@ def main():
                                        "logits", "norm", "varlen", "long", "oproj"], default="all",
                     help="profiling runs: time one workload only")
     ap.add_argument("--prefill-T", type=int, default=None, help="shorter prefill (profiling cases only)")
+    ap.add_argument("--oproj-rows", type=int, default=None,
+                    help="with --only oproj: one o_proj leg of this many rows (profiling cases only)")
     ap.add_argument("--headline", choices=["fused", "concurrent"], default="fused",
                     help="the prefill form timed as the headline value (the other is reported beside it)")
     ap.add_argument("--decode-B", type=int, default=None, help="smaller decode batch (profiling cases only)")
