@@ -786,8 +786,8 @@ kda_status launch_o_proj(const void *y, const void *w, void *out, int out_bf16, 
         }
         const int n_ft2 = N / 256;
         const bool split = M <= 256 && (K / BK) % 2 == 0 && 4 * n_ft2 <= sms;
-        // 512-row tiles where they still give every pair at least one tile
-        const bool wide = !split && (int64_t)n_ft2 * ((M + 511) / 512) >= sms / 2;
+        // 512-row tiles where there are more than 256 rows and every pair still gets a tile
+        const bool wide = !split && M > 256 && (int64_t)n_ft2 * ((M + 511) / 512) >= sms / 2;
         const int tile_rows = wide ? 512 : 256;
         GemmArgs ga;
         memset(&ga, 0, sizeof(ga));
