@@ -197,9 +197,9 @@ size_t kda_chunk_workspace_size(int B, int T, int H, int n_seqs);
 /*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate device memory.
  *
- * The split tensor-core prefill keeps every chunk's state-independent operands in
- * scratch memory between its two kernels, and kda_chunk_fwd takes that scratch from
- * the caller as a workspace.  Some callers have no way to provide one: code behind a
+ * The concurrent and split tensor-core prefill forms keep chunks' state-independent
+ * operands in scratch memory between their two kernels, and kda_chunk_fwd takes that
+ * scratch from the caller as a workspace.  Some callers have no way to provide one: code behind a
  * fixed operator or plugin interface that passes only input and output tensors, and
  * code that runs where device allocation is not allowed or not possible (a memory
  * pool owned by another component, a latency-critical path that must not allocate).
