@@ -422,13 +422,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
 // NSUB = 1: a 256-feature x 256-row tile.  NSUB = 2 (long prompts): 256 features x 512
 // rows, two N = 256 products per K step on the same w_o slice, so an SM takes 48 KB per
 // 8 products instead of 32 KB per 4: 42 instead of 56 bytes per cycle of tensor work at
-// the bf16 rate, and the same bytes in flight (4 stages instead of 6) cover a third more
-// load latency.  Its 512 TMEM columns hold one accumulator, so a tile's epilogue no
-// longer overlaps the next tile's products.
+// the bf16 rate, and about the same bytes in flight (4 stages of 48 KB against 6-7 of
+// 32 KB) cover a third more load latency.  Its 512 TMEM columns hold one accumulator, so
+// a tile's epilogue no longer overlaps the next tile's products.  NSUB = 1 takes a seventh
+// stage (224 KB), which the shared memory just holds.
 template <int NSUB>
 struct PairCfg {
     static constexpr int BN = 256 * NSUB;              // rows of y per tile (128 of each 256 staged per CTA)
-    static constexpr int STAGES = NSUB == 1 ? 6 : 4;
+    static constexpr int STAGES = NSUB == 1 ? 7 : 4;
     static constexpr uint32_t A_BYTES = 128 * BK * 2;  // this CTA's 128 w_o rows
     static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's 128 y rows of each 256-row sub-tile
     static constexpr uint32_t STAGE = A_BYTES + NSUB * B_BYTES;
