@@ -438,12 +438,13 @@ struct PairCfg {
 };
 static_assert(PairCfg<1>::SMEM <= 232448 && PairCfg<2>::SMEM <= 232448, "shared memory budget");
 
-// Tile id -> (256-feature tile, 256-row tile): groups of 14 feature tiles (3584 features)
-// across every row tile, so the pairs running together share w_o and y through L2.  At
-// 76 pairs the tiles in flight cover 14 feature tiles by about 5.4 row tiles, about 120 MB
-// of operands (the L2 holds 129 MB), and y is read from DRAM twice per call at 7168
-// features.  Measured at 8192 x 12288 -> 7168 on one GPU: 0.767 ms with 14, 0.776 with 7,
-// 0.790 with 4, 0.815 with 28.
+// Tile id -> (256-feature tile, row tile): groups of 14 feature tiles (3584 features)
+// across every row tile, so the pairs running together share w_o and y through L2.  With
+// 256-row tiles, the 76 pairs' tiles in flight cover 14 feature tiles by about 5.4 row
+// tiles, about 120 MB of operands (the L2 holds 129 MB), and y is read from DRAM twice per
+// call at 7168 features.  Measured at 8192 x 12288 -> 7168 on one GPU: 0.767 ms with 14,
+// 0.776 with 7, 0.790 with 4, 0.815 with 28; with 512-row tiles 0.716 ms with 14, 0.718
+// with 10, 0.720 with 28, 0.733 with 7.
 __device__ __forceinline__ void pair_tile_coords(int id, int n_ft, int n_tt, int &f, int &t) {
     constexpr int G = 14;
     const int per_group = G * n_tt;
