@@ -107,16 +107,18 @@ uint64_t kda_launch_count(void);
 kda_status kda_device_status(void *stream);
 
 /*
- * kda_set_wait_limit -- bound on the first-line waits of the streaming kernels.
+ * kda_set_wait_limit -- bound on the first-line waits on copies from global memory.
  *
  * The decode step's copy waits (kda_recurrent_step, kda_recurrent_step_logits with
- * K = V = 128) and the short convolution's tile waits (kda_short_conv_fwd over a
- * prompt) poll their mbarrier at most this many times before they give up, for the
- * calls made after this one (process-wide).  polls < 0 restores the default (2^26);
- * 0 makes every such wait give up at once, which tests of the failure handling use
- * (kda_device_status then reports KDA_ERR_TIMEOUT and the outputs hold NaN).  The
- * waits that let copies in flight land before a CTA exits, and the tensor-core
- * waits of the chunked prefill, always keep their full bound.  Returns KDA_OK, or
+ * K = V = 128), the short convolution's tile waits (kda_short_conv_fwd over a prompt)
+ * and the fused tensor-core prefill's tile and blob waits (kda_chunk_fwd,
+ * kda_chunk_fwd_logits without a workspace or with one in the concurrent form) poll
+ * their mbarrier at most this many times before they give up, for the calls made after
+ * this one (process-wide).  polls < 0 restores the default (2^26); 0 makes every such
+ * wait give up at once, which tests of the failure handling use (kda_device_status then
+ * reports KDA_ERR_TIMEOUT and the outputs hold NaN).  The waits that let copies in
+ * flight land before a CTA exits, the tensor-core waits, and the split form's kernels
+ * always keep their full bound.  Returns KDA_OK, or
  * KDA_ERR_INVALID_ARG above 2^32 - 1.  No counterpart on the pages.
  */
 kda_status kda_set_wait_limit(int64_t polls);

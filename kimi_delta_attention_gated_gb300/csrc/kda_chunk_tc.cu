@@ -108,6 +108,9 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Set by a CTA whose bounded wait on the tensor core or the TMA gave up; that CTA
 // also writes NaN into its final state, o and y so the failure cannot pass unnoticed.
+// The waits on copies from global memory (the V, g and gate tiles, a pre-pass blob) take
+// the caller's bound (SeqParams::polls, kda_set_wait_limit); the waits on the tensor core
+// and those that let copies land before the CTA exits keep kPolls.
 __device__ int g_chunk_tc_timeouts = 0;
 // Chunks whose T diag(beta) and P came from the concurrent pre-pass (a diagnostic).
 __device__ unsigned long long g_chunk_tc_blob_chunks = 0;
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The 8 sums of squares of a warp's 4 tokens are reduced with a reduce-scatter
     // (9 shuffles); lanes 4v..4v+3 end with sum v (q of tokens 0-3, then k).
     auto prep_norms = [&](ChunkRegs &c, int cnn, int chunk) {
-        if (!mbar_wait(gt_bar, (uint32_t)(chunk & 1), kPolls))
+        if (!mbar_wait(gt_bar, (uint32_t)(chunk & 1), p.polls))
             failed = 1;
         else if (tid == 0)
             g_pending = -1;
@@ -768,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid == 0) {
             // ================= R^T = V^T I + S^T (-Kd)^T, O^T = S^T Qd^T (while warps 1-15 solve T)
-            if (mbar_wait(tma_bar, (uint32_t)par, kPolls))
+            if (mbar_wait(tma_bar, (uint32_t)par, p.polls))
                 v_pending = -1;
             else
                 failed = 1;
@@ -871,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= D^T = R^T (T diag beta)^T
         if (tid == 0) {
             if (use_blob) {  // the blob's tiles have landed (the O/S product reads P after this too)
-                if (mbar_wait(blob_bar, (uint32_t)b_pending, kPolls))
+                if (mbar_wait(blob_bar, (uint32_t)b_pending, p.polls))
                     b_pending = -1;
                 else
                     failed = 1;
@@ -1021,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // memory; an fp32 one from global memory
                 float sg[16];
                 if (p.gate_bf16) {
-                    if (!mbar_wait(gate_bar, (uint32_t)(ch & 1), kPolls))
+                    if (!mbar_wait(gate_bar, (uint32_t)(ch & 1), p.polls))
                         failed = 1;
                     else if (tid == 0)
                         q_pending = -1;

@@ -20,9 +20,10 @@ void note_launch(int n = 1);
 // Turns a pending CUDA error into KDA_ERR_CUDA with a message naming `what`.
 kda_status check_launch(const char *what);
 
-// Bound (in polls) on the first-line waits of the streaming kernels (decode step, short
-// convolution): kDefaultWaitPolls unless kda_set_wait_limit changed it.  The waits that
-// drain copies still in flight before a CTA exits always keep the default.
+// Bound (in polls) on the first-line waits on copies from global memory (decode step,
+// short convolution, the fused chunked prefill): kDefaultWaitPolls unless
+// kda_set_wait_limit changed it.  The waits that drain copies still in flight before a
+// CTA exits, and the waits on the tensor core, always keep the default.
 constexpr uint32_t kDefaultWaitPolls = 1u << 26;
 uint32_t wait_polls();
 

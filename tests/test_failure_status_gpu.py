@@ -1,6 +1,7 @@
 """GPU tests of the library's failure detection, made to happen without a fault: the
-streaming kernels' first-line waits get a bound of zero polls (kda_set_wait_limit), so
-every such wait gives up at once while its copy is still in flight.  The kernel then lets
+first-line waits on copies from global memory (decode step, short convolution, the fused
+prefill kernel) get a bound of zero polls (kda_set_wait_limit), so every such wait gives
+up at once while its copy is still in flight.  The kernel then lets
 the copy land (that wait keeps its full bound), writes NaN into every output it was
 responsible for and counts the event; kda_device_status reports KDA_ERR_TIMEOUT once and
 clears the count, and the next call on the same context computes correctly.  No test
@@ -11,8 +12,8 @@ import torch
 
 import kimi_delta_attention_gated_gb300 as kda
 import oracle
-from kimi_delta_attention_gated_gb300.inputs import make_conv_inputs
-from tests.gpu_helpers import FP32_TOL, np32, rel_err
+from kimi_delta_attention_gated_gb300.inputs import make_conv_inputs, make_inputs
+from tests.gpu_helpers import FP32_TOL, PARITY, np32, oracle_run, rel_err
 from tests.test_parity_gpu import decode_inputs, decode_oracle
 
 pytestmark = pytest.mark.gpu
@@ -88,6 +89,38 @@ def test_short_conv_timeout_poisons_outputs_and_states(zero_wait_limit):
     yo, so = oracle.short_conv(np32(d["x"]), np32(d["weight"]), None, np32(d["conv_state"]))
     assert rel_err(y, yo) <= FP32_TOL
     assert rel_err(s, so) <= FP32_TOL
+
+
+@pytest.mark.parametrize("norm", [False, True])
+def test_prefill_timeout_poisons_every_unit(zero_wait_limit, norm):
+    """The fused tensor-core prefill: every CTA's first g-tile wait gives up, the CTA lets
+    its V and g copies land, and o, y and the final state (updated in place, where an
+    unwritten unit would keep its old, valid-looking state) hold NaN for every unit; two
+    sequences of different lengths, one with a ragged last chunk."""
+    d = make_inputs("long", device="cuda", lengths=[150, 64], H=3)
+    state = 0.02 * torch.randn((2, 3, 128, 128), device="cuda")
+    kw = dict(gate=d["gate"], norm_w=d["norm_w"], eps=d["eps"]) if norm else {}
+    res = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], state, scale=d["scale"], mode="tensor",
+                        cu_seqlens=d["cu_seqlens"], final_state=state, **kw)
+    expect_timeout()
+    for t in res:
+        assert torch.isnan(t).all()
+
+
+def test_prefill_after_a_timeout_is_correct():
+    """After the poisoned call, the same prompt with the default bound matches the oracle."""
+    d = make_inputs("prefill", device="cuda", T=200, H=2)
+    kda.set_wait_limit(0)
+    try:
+        kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"], mode="tensor")
+        expect_timeout()
+    finally:
+        kda.set_wait_limit(None)
+    o, s = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"], mode="tensor")
+    kda.device_status()
+    oo, so = oracle_run(d)
+    assert rel_err(o, oo) <= PARITY
+    assert rel_err(s, so) <= PARITY
 
 
 def test_status_is_clean_after_normal_work():
