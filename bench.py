@@ -46,23 +46,23 @@ PREFILL_LONG_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 512  # q,k,v bf16 + g fp32
 # ncu capture summarised under profiles/, valid only for the kernel source it was
 # taken on: `traffic` is reported as null as soon as that source file changes.
 MEASURED_TRAFFIC = {
-    # B=1 T=2048 H=96 capture, mean of two launches: (328.139648 MB - 6.29 MB of final state)
+    # B=1 T=2048 H=96 capture, mean of two launches: (328.410112 MB - 6.29 MB of final state)
     # / (2048 * 96) token-heads
     "prefill_fused": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                      "sha256": "c6816f6ef21d53d561edbd55e6405fae9a1edf02d9558ca41593d43ccde7fc7d",
-                      "bytes_per_unit": (328.139648e6 - 6.291456e6) / (2048 * 96),
+                      "sha256": "78a254e0b521b659e9c1ca535b80449b1df1bcbe1f85ecc50bf4286205bef4eb",
+                      "bytes_per_unit": (328.410112e6 - 6.291456e6) / (2048 * 96),
                       "capture": "ncu, B=1 T=2048 H=96, g and beta given"},
     # the same kernel with gates from bf16 logits, B=1 T=2048 H=96 capture, mean of two
-    # launches: (274.32 MB - 6.29 MB of final state) / (2048 * 96) token-heads
+    # launches: (274.22208 MB - 6.29 MB of final state) / (2048 * 96) token-heads
     "prefill_logits": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                       "sha256": "c6816f6ef21d53d561edbd55e6405fae9a1edf02d9558ca41593d43ccde7fc7d",
-                       "bytes_per_unit": (274.32e6 - 6.291456e6) / (2048 * 96),
+                       "sha256": "78a254e0b521b659e9c1ca535b80449b1df1bcbe1f85ecc50bf4286205bef4eb",
+                       "bytes_per_unit": (274.22208e6 - 6.291456e6) / (2048 * 96),
                        "capture": "ncu, B=1 T=2048 H=96, bf16 logits"},
     # the same kernel with the fused gated norm (bf16 gate in, bf16 y out), B=1 T=2048 H=96
-    # capture, mean of two launches: (342.078208 MB - 6.29 MB of final state) / (2048 * 96)
+    # capture, mean of two launches: (342.155648 MB - 6.29 MB of final state) / (2048 * 96)
     "prefill_norm": {"source": "kimi_delta_attention_gated_gb300/csrc/kda_chunk_tc.cu",
-                     "sha256": "c6816f6ef21d53d561edbd55e6405fae9a1edf02d9558ca41593d43ccde7fc7d",
-                     "bytes_per_unit": (342.078208e6 - 6.291456e6) / (2048 * 96),
+                     "sha256": "78a254e0b521b659e9c1ca535b80449b1df1bcbe1f85ecc50bf4286205bef4eb",
+                     "bytes_per_unit": (342.155648e6 - 6.291456e6) / (2048 * 96),
                      "capture": "ncu, B=1 T=2048 H=96, fused gated norm"},
     # B=64 capture: mean of two launches, 754.667264 MB / (64 * 96) (sequence, head) units
     # (part of the state written back stays in L2 at the kernel's end: below the algorithmic bytes)
